@@ -1,0 +1,316 @@
+"""Python binding of ``libmoe.so``: the B300 forward pass of a DeepSeekMoE layer with
+auxiliary-loss-free load balancing.
+
+Every function here only marshals arguments (device pointers, sizes, the current
+CUDA stream) and calls the C ABI declared in ``include/moe.h`` of the same name; all
+arithmetic runs in the library's CUDA kernels.  There is no CPU or PyTorch fallback:
+if the library is missing or a call fails, a ``MoEError`` is raised.
+
+Tensors are ``torch.Tensor`` on a CUDA device, contiguous, in the layouts of moe.h.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "MoEError", "Shape", "load_library", "route", "dispatch", "quantize_e4m3",
+    "expert_gate_up", "expert_down", "expert_ffn", "combine", "bias_update",
+    "seq_balance_stat", "device_error", "route_workspace_bytes",
+    "dispatch_workspace_bytes", "expert_ffn_workspace_bytes", "MoELayer",
+    "LIB_PATH", "STATUS", "launch_counter", "launch_counter_reset", "make_shape",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
+F32, BF16, E4M3 = 0, 1, 2
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "d", "N_r", "K_r", "N_s", "I", "G", "M")]
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int)] + [
+        (n, ctypes.c_void_p) for n in (
+            "gate", "up", "down", "gate_scale", "up_scale", "down_scale",
+            "s_gate", "s_up", "s_down", "s_gate_scale", "s_up_scale", "s_down_scale")]
+
+
+_P, _S, _I32, _I64, _F = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_abi_version": (ctypes.c_int, []),
+    "moe_route_workspace": (_S, [Shape, _I32]),
+    "moe_route": (ctypes.c_int, [_P, _P, ctypes.c_int, _P, Shape, _P, _I32, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_dispatch_workspace": (_S, [Shape]),
+    "moe_dispatch": (ctypes.c_int, [_P, Shape, _P, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_quantize_e4m3": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I32, _P, _P, _P]),
+    "moe_expert_ffn_workspace": (_S, [Shape, ctypes.c_int]),
+    "moe_expert_gate_up": (ctypes.c_int, [_P, _P, _P, _P, _P, Shape, ctypes.POINTER(_Weights), _P, _P, _P]),
+    "moe_expert_down": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.POINTER(_Weights), _P, _P]),
+    "moe_expert_ffn": (ctypes.c_int, [_P, _P, _P, _P, _P, Shape, ctypes.POINTER(_Weights), _P, _P, _S, _P]),
+    "moe_combine": (ctypes.c_int, [_P, _P, ctypes.c_int, _P, _P, Shape, _P, ctypes.c_int, _P]),
+    "moe_bias_update": (ctypes.c_int, [_P, _P, Shape, _F, _P]),
+    "moe_seq_balance_stat": (ctypes.c_int, [_P, _P, _P, _I32, Shape, _F, _P, _P, _P]),
+    "moe_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _I32]),
+}
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so (once).  Raises MoEError-free ``OSError`` if it is missing:
+    build it with ``python -m aux_loss_free_router_b300.build``."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise OSError(f"{path} not found: run `python -m aux_loss_free_router_b300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+# Kernels each call enqueues for a non-empty batch (the launch count of a step).
+_KERNELS = {"moe_route": 1, "moe_dispatch": 3, "moe_quantize_e4m3": 1, "moe_expert_gate_up": 1,
+            "moe_expert_down": 1, "moe_expert_ffn": 2, "moe_combine": 1, "moe_bias_update": 1,
+            "moe_seq_balance_stat": 1}
+_launches = 0
+
+
+def launch_counter_reset() -> None:
+    global _launches
+    _launches = 0
+
+
+def launch_counter() -> int:
+    """Kernels launched through this binding since the last reset."""
+    return _launches
+
+
+def _call(name: str, *args, extra_kernels: int = 0) -> None:
+    global _launches
+    code = getattr(load_library(), name)(*args)
+    if code != 0:
+        raise MoEError(name, code)
+    _launches += _KERNELS.get(name, 0) + extra_kernels
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the MoE library must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the MoE library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return E4M3
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def make_shape(T, d, N_r, K_r, N_s, I, G=1, M=1) -> Shape:
+    return Shape(T, d, N_r, K_r, N_s, I, G, M)
+
+
+# ----------------------------------------------------------------- workspaces -----
+
+def route_workspace_bytes(sh: Shape, n_seq: int) -> int:
+    return load_library().moe_route_workspace(sh, n_seq)
+
+
+def dispatch_workspace_bytes(sh: Shape) -> int:
+    return load_library().moe_dispatch_workspace(sh)
+
+
+def expert_ffn_workspace_bytes(sh: Shape, w_dtype: int) -> int:
+    return load_library().moe_expert_ffn_workspace(sh, w_dtype)
+
+
+def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device) if nbytes else None
+
+
+# ------------------------------------------------------------------ the calls -----
+
+def route(u, e, b, sh: Shape, topk_idx, topk_gate, s_out=None, seq_offsets=None, n_seq=0,
+          seq_p_sum=None, workspace=None, stream=None):
+    ws = workspace
+    if seq_p_sum is not None and ws is None:
+        ws = _workspace(route_workspace_bytes(sh, n_seq), u.device)
+    _call("moe_route", _ptr(u), _ptr(e), _dt(u), _ptr(b), sh, _ptr(seq_offsets), n_seq,
+          _ptr(topk_idx), _ptr(topk_gate), _ptr(s_out), _ptr(seq_p_sum), _ptr(ws),
+          ws.numel() if ws is not None else 0, _stream(stream),
+          extra_kernels=2 if seq_p_sum is not None else 0)
+
+
+def dispatch(topk_idx, sh: Shape, load, expert_offset, perm_token, inv_row, u=None,
+             x_perm=None, u_scale=None, x_perm_scale=None, workspace=None, stream=None):
+    ws = workspace if workspace is not None else _workspace(dispatch_workspace_bytes(sh), topk_idx.device)
+    _call("moe_dispatch", _ptr(topk_idx), sh, _ptr(u), _dt(u) if u is not None else BF16,
+          _ptr(u_scale), _ptr(load), _ptr(expert_offset), _ptr(perm_token), _ptr(inv_row),
+          _ptr(x_perm), _ptr(x_perm_scale), _ptr(ws), ws.numel() if ws is not None else 0,
+          _stream(stream), extra_kernels=1 if x_perm is not None else 0)
+
+
+def quantize_e4m3(x, block_rows: int, q, scale, stream=None):
+    rows, cols = x.shape[0] if x.dim() == 2 else x.numel() // x.shape[-1], x.shape[-1]
+    _call("moe_quantize_e4m3", _ptr(x), _dt(x), rows, cols, block_rows, _ptr(q), _ptr(scale),
+          _stream(stream))
+
+
+def _weights(w: dict) -> _Weights:
+    g = w["w_gate"]
+    dt = E4M3 if g.dtype in (torch.uint8, torch.float8_e4m3fn) else _dt(g)
+    get = lambda k: _ptr(w.get(k))
+    return _Weights(dt, get("w_gate"), get("w_up"), get("w_down"), get("w_gate_scale"),
+                    get("w_up_scale"), get("w_down_scale"), get("ws_gate"), get("ws_up"),
+                    get("ws_down"), get("ws_gate_scale"), get("ws_up_scale"), get("ws_down_scale"))
+
+
+def expert_gate_up(x_perm, u, expert_offset, sh: Shape, weights: dict, h, x_perm_scale=None,
+                   u_scale=None, h_scale=None, stream=None):
+    wt = _weights(weights)
+    _call("moe_expert_gate_up", _ptr(x_perm), _ptr(x_perm_scale), _ptr(u), _ptr(u_scale),
+          _ptr(expert_offset), sh, ctypes.byref(wt), _ptr(h), _ptr(h_scale), _stream(stream))
+
+
+def expert_down(h, expert_offset, sh: Shape, weights: dict, y, h_scale=None, stream=None):
+    wt = _weights(weights)
+    _call("moe_expert_down", _ptr(h), _ptr(h_scale), _ptr(expert_offset), sh, ctypes.byref(wt),
+          _ptr(y), _stream(stream))
+
+
+def expert_ffn(x_perm, u, expert_offset, sh: Shape, weights: dict, y, workspace=None,
+               x_perm_scale=None, u_scale=None, stream=None):
+    wt = _weights(weights)
+    ws = workspace if workspace is not None else _workspace(
+        expert_ffn_workspace_bytes(sh, wt.dtype), u.device)
+    _call("moe_expert_ffn", _ptr(x_perm), _ptr(x_perm_scale), _ptr(u), _ptr(u_scale),
+          _ptr(expert_offset), sh, ctypes.byref(wt), _ptr(y), _ptr(ws),
+          ws.numel() if ws is not None else 0, _stream(stream))
+
+
+def combine(u, y, topk_gate, inv_row, sh: Shape, h_out, stream=None):
+    _call("moe_combine", _ptr(u), _ptr(y), _dt(u), _ptr(topk_gate), _ptr(inv_row), sh,
+          _ptr(h_out), _dt(h_out), _stream(stream))
+
+
+def bias_update(b, load, sh: Shape, gamma: float, stream=None):
+    _call("moe_bias_update", _ptr(b), _ptr(load), sh, gamma, _stream(stream))
+
+
+def seq_balance_stat(seq_p_sum, topk_idx, seq_offsets, n_seq: int, sh: Shape, alpha: float,
+                     stat_per_seq, stat_mean=None, stream=None):
+    _call("moe_seq_balance_stat", _ptr(seq_p_sum), _ptr(topk_idx), _ptr(seq_offsets), n_seq, sh,
+          alpha, _ptr(stat_per_seq), _ptr(stat_mean), _stream(stream))
+
+
+def device_error(clear: bool = True) -> int:
+    code = ctypes.c_int32(0)
+    _call("moe_device_error", ctypes.byref(code), int(clear))
+    return code.value
+
+
+# --------------------------------------------------------------- whole layer -----
+
+@dataclasses.dataclass
+class MoELayer:
+    """One layer's parameters and preallocated buffers; ``step()`` runs the whole
+    forward pass plus the end-of-step bias update and sequence statistic through the
+    C ABI on the current stream (no host synchronisation, no allocation)."""
+
+    T: int
+    d: int
+    N_r: int
+    K_r: int
+    N_s: int
+    I: int
+    G: int
+    M: int
+    e: torch.Tensor
+    b: torch.Tensor
+    weights: dict
+    n_seq: int = 1
+    gamma: float = 0.001
+    alpha: float = 0.0001
+    want_s: bool = False
+    out_dtype: Optional[torch.dtype] = torch.float32   # h' (fp32 keeps the layer output
+    # within 2e-2 max-abs: a bf16 store alone errs by up to 0.0156 once |h'| >= 4)
+
+    def __post_init__(self):
+        dev, dt = self.e.device, self.e.dtype
+        T, K_r, N_r = self.T, self.K_r, self.N_r
+        self.shape = make_shape(self.T, self.d, N_r, K_r, self.N_s, self.I, self.G, self.M)
+        z = lambda *s, dtype=torch.int32: torch.empty(*s, dtype=dtype, device=dev)
+        self.topk_idx = z(T, K_r)
+        self.topk_gate = z(T, K_r, dtype=torch.float32)
+        self.s_out = z(T, N_r, dtype=torch.float32) if self.want_s else None
+        self.seq_p_sum = z(self.n_seq, N_r, dtype=torch.float32)
+        self.load = z(N_r)
+        self.expert_offset = z(N_r + 1)
+        self.perm_token = z(T * K_r)
+        self.inv_row = z(T, K_r)
+        self.x_perm = z(T * K_r, self.d, dtype=dt)
+        R = T * K_r + self.N_s * T
+        self.h_mid = z(R, self.I, dtype=dt)
+        self.y = z(R, self.d, dtype=dt)
+        self.out = z(T, self.d, dtype=self.out_dtype or dt)
+        self.stat = z(self.n_seq, dtype=torch.float32)
+        self.stat_mean = z(1, dtype=torch.float32)
+        self.ws_route = _workspace(route_workspace_bytes(self.shape, self.n_seq), dev)
+        self.ws_dispatch = _workspace(dispatch_workspace_bytes(self.shape), dev)
+
+    def step(self, u: torch.Tensor, seq_offsets: torch.Tensor, update_bias: bool = True,
+             events: Optional[list] = None, stream=None) -> torch.Tensor:
+        """Forward pass h' for the tokens u; then b <- b + gamma*sign(mean - load) and the
+        per-sequence statistic.  ``events`` (optional list of 6 CUDA events) are recorded
+        between the stages for per-stage timing (6 events)."""
+        sh = self.shape
+        ev = (lambda i: events[i].record(stream)) if events else (lambda i: None)
+        ev(0)
+        route(u, self.e, self.b, sh, self.topk_idx, self.topk_gate, self.s_out, seq_offsets,
+              self.n_seq, self.seq_p_sum, self.ws_route, stream)
+        ev(1)
+        dispatch(self.topk_idx, sh, self.load, self.expert_offset, self.perm_token, self.inv_row,
+                 u, self.x_perm, workspace=self.ws_dispatch, stream=stream)
+        ev(2)
+        expert_gate_up(self.x_perm, u, self.expert_offset, sh, self.weights, self.h_mid,
+                       stream=stream)
+        ev(3)
+        expert_down(self.h_mid, self.expert_offset, sh, self.weights, self.y, stream=stream)
+        ev(4)
+        combine(u, self.y, self.topk_gate, self.inv_row, sh, self.out, stream=stream)
+        if update_bias:
+            bias_update(self.b, self.load, sh, self.gamma, stream=stream)
+        seq_balance_stat(self.seq_p_sum, self.topk_idx, seq_offsets, self.n_seq, sh, self.alpha,
+                         self.stat, self.stat_mean, stream=stream)
+        ev(5)
+        return self.out

@@ -1,0 +1,284 @@
+// The C ABI: argument validation, workspace layout and kernel selection.  Nothing is
+// launched unless every check passes; no call synchronises or allocates.
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+#include "launch.h"
+#include "ffn_sched.cuh"
+#include "route_select.cuh"
+
+using namespace moe;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+inline bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
+inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status check_shape(const moe_shape& s) {
+  if (s.T < 0 || s.d <= 0 || s.I <= 0 || s.N_s < 0 || s.N_s > kMaxShared) return MOE_ERR_INVALID_ARG;
+  if (s.N_r < 1 || s.N_r > kMaxExperts || s.K_r < 1 || s.K_r > s.N_r || s.K_r > 32)
+    return MOE_ERR_INVALID_ARG;
+  if (s.G < 1 || s.G > 32 || s.M < 1 || s.M > s.G || s.N_r % s.G != 0 || s.K_r % s.M != 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)s.M * (s.N_r / s.G) < s.K_r) return MOE_ERR_INVALID_ARG;
+  if (s.d % 8 != 0 || s.I % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if ((long long)s.T * s.K_r + (long long)s.N_s * s.T >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+bool is_float_dtype(moe_dtype dt) { return dt == MOE_F32 || dt == MOE_BF16; }
+size_t elem_bytes(moe_dtype dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dtype or shape";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA launch error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+// ------------------------------------------------------------------------ route ----
+
+size_t moe_route_workspace(moe_shape sh, int32_t n_seq) {
+  if (n_seq <= 0 || sh.T <= 0 || sh.N_r <= 0) return 0;
+  return align256((size_t)sh.T * sh.N_r * sizeof(float)) +
+         align256((size_t)n_seq * kSeqSlabs * sh.N_r * sizeof(double));
+}
+
+moe_status moe_route(const void* u, const void* e, moe_dtype dt, const float* b, moe_shape sh,
+                     const int32_t* seq_offsets, int32_t n_seq, int32_t* topk_idx,
+                     float* topk_gate, float* s_out, float* seq_p_sum, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if (!is_float_dtype(dt)) return MOE_ERR_UNSUPPORTED;
+  if (sh.T > 0 && (!ok_ptr(u) || !ok_ptr(e) || !ok_ptr(b) || !ok_ptr(topk_idx) || !ok_ptr(topk_gate)))
+    return MOE_ERR_INVALID_ARG;
+  if (!ok_opt(s_out) || !ok_opt(seq_p_sum) || n_seq < 0) return MOE_ERR_INVALID_ARG;
+  const bool want_stat = seq_p_sum != nullptr;
+  if (want_stat && (n_seq < 1 || seq_offsets == nullptr)) return MOE_ERR_INVALID_ARG;
+  float* sprime = nullptr;
+  double* partial = nullptr;
+  if (want_stat && sh.T > 0) {
+    const size_t need = moe_route_workspace(sh, n_seq);
+    if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    sprime = static_cast<float*>(workspace);
+    partial = reinterpret_cast<double*>(static_cast<char*>(workspace) +
+                                        align256((size_t)sh.T * sh.N_r * sizeof(float)));
+  }
+  RouteOut p{sh.T, sh.N_r, sh.K_r, sh.G, sh.M, topk_idx, topk_gate, s_out, sprime};
+  cudaError_t err = cudaSuccess;
+  if (sh.T > 0) {
+    const bool tc_ok = dt == MOE_BF16 && sh.N_r % 32 == 0;
+    err = tc_ok ? launch_router_tc(u, e, b, sh.d, p, S(stream))
+                : launch_router_simt(u, e, dt, b, sh.d, p, S(stream));
+  }
+  if (err == cudaSuccess && want_stat) {
+    if (sh.T > 0) {
+      err = launch_seq_psum(sprime, seq_offsets, n_seq, sh.N_r, partial, seq_p_sum, S(stream));
+    } else {
+      err = cudaMemsetAsync(seq_p_sum, 0, sizeof(float) * n_seq * sh.N_r, S(stream));
+    }
+  }
+  return cuda_status(err);
+}
+
+// --------------------------------------------------------------------- dispatch ----
+
+size_t moe_dispatch_workspace(moe_shape sh) {
+  if (sh.T <= 0 || sh.N_r <= 0) return 0;
+  const size_t chunks = ((size_t)sh.T + kDispatchChunk - 1) / kDispatchChunk;
+  return align256(chunks * sh.N_r * sizeof(int32_t));
+}
+
+moe_status moe_dispatch(const int32_t* topk_idx, moe_shape sh, const void* u, moe_dtype u_dt,
+                        const float* u_scale, int32_t* load, int32_t* expert_offset,
+                        int32_t* perm_token, int32_t* inv_row, void* x_perm,
+                        float* x_perm_scale, void* workspace, size_t ws_bytes, void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(load) || !ok_ptr(expert_offset)) return MOE_ERR_INVALID_ARG;
+  if (sh.T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(perm_token) || !ok_ptr(inv_row)))
+    return MOE_ERR_INVALID_ARG;
+  const bool gather = u != nullptr && x_perm != nullptr;
+  if ((u == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (gather && (!aligned16(u) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+  size_t row_bytes = 0;
+  int scale_cols = 0;
+  if (gather) {
+    if (u_dt != MOE_F32 && u_dt != MOE_BF16 && u_dt != MOE_E4M3) return MOE_ERR_UNSUPPORTED;
+    row_bytes = (size_t)sh.d * elem_bytes(u_dt);
+    if (row_bytes % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (u_dt == MOE_E4M3) {
+      if (sh.d % 128 != 0 || !ok_ptr(u_scale) || !ok_ptr(x_perm_scale)) return MOE_ERR_INVALID_ARG;
+      scale_cols = sh.d / 128;
+    }
+  }
+  const size_t need = moe_dispatch_workspace(sh);
+  if (need > 0 && (workspace == nullptr || !aligned16(workspace) || ws_bytes < need))
+    return MOE_ERR_WORKSPACE;
+  const cudaError_t err = launch_dispatch(
+      topk_idx, sh.T, sh.N_r, sh.K_r, gather ? u : nullptr, row_bytes,
+      u_dt == MOE_E4M3 ? u_scale : nullptr, scale_cols, load, expert_offset, perm_token, inv_row,
+      gather ? x_perm : nullptr, u_dt == MOE_E4M3 ? x_perm_scale : nullptr,
+      static_cast<int32_t*>(workspace), S(stream));
+  return cuda_status(err);
+}
+
+// ------------------------------------------------------------------------- quant ----
+
+moe_status moe_quantize_e4m3(const void* x, moe_dtype x_dt, int64_t rows, int64_t cols,
+                             int32_t block_rows, uint8_t* q, float* scale, void* stream) {
+  if (!is_float_dtype(x_dt)) return MOE_ERR_UNSUPPORTED;
+  if (rows < 0 || cols <= 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (block_rows != 1 && block_rows != 128) return MOE_ERR_INVALID_ARG;
+  if (block_rows == 128 && rows % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!ok_ptr(x) || !ok_ptr(q) || !ok_ptr(scale))) return MOE_ERR_INVALID_ARG;
+  if (block_rows == 128 && rows / 128 > 65535) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_e4m3(x, x_dt, rows, cols, block_rows, q, scale, S(stream)));
+}
+
+// ------------------------------------------------------------------- expert FFN ----
+
+namespace {
+
+moe_status check_weights(const moe_shape& sh, const moe_expert_weights* w) {
+  if (w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(w->gate) || !ok_ptr(w->up) || !ok_ptr(w->down)) return MOE_ERR_INVALID_ARG;
+  if (sh.N_s > 0 && (!ok_ptr(w->s_gate) || !ok_ptr(w->s_up) || !ok_ptr(w->s_down)))
+    return MOE_ERR_INVALID_ARG;
+  if (w->dtype == MOE_E4M3) return MOE_ERR_UNSUPPORTED;
+  if (!is_float_dtype(w->dtype)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+FfnShape ffn_shape(const moe_shape& sh) { return FfnShape{sh.T, sh.d, sh.I, sh.N_r, sh.K_r, sh.N_s}; }
+
+size_t h_bytes(const moe_shape& sh, moe_dtype dt) {
+  const size_t rows = (size_t)sh.T * sh.K_r + (size_t)sh.N_s * sh.T;
+  return rows * sh.I * elem_bytes(dt);
+}
+
+}  // namespace
+
+size_t moe_expert_ffn_workspace(moe_shape sh, moe_dtype w_dt) {
+  if (sh.T <= 0) return 0;
+  return align256(h_bytes(sh, w_dt));
+}
+
+moe_status moe_expert_gate_up(const void* x_perm, const float* x_perm_scale, const void* u,
+                              const float* u_scale, const int32_t* expert_offset, moe_shape sh,
+                              const moe_expert_weights* w, void* h, float* h_scale,
+                              void* stream) {
+  (void)x_perm_scale; (void)u_scale; (void)h_scale;
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(sh, w)) != MOE_OK) return st;
+  if (sh.T == 0) return MOE_OK;
+  if (!ok_ptr(x_perm) || !ok_ptr(u) || !ok_ptr(expert_offset) || !ok_ptr(h))
+    return MOE_ERR_INVALID_ARG;
+  const FfnShape fs = ffn_shape(sh);
+  cudaError_t err;
+  if (w->dtype == MOE_F32)
+    err = launch_ffn_up_simt(fs, (const float*)x_perm, (const float*)u, expert_offset, w,
+                             (float*)h, S(stream));
+  else
+    err = launch_ffn_up_tc(fs, x_perm, u, expert_offset, w, h, S(stream));
+  return cuda_status(err);
+}
+
+moe_status moe_expert_down(const void* h, const float* h_scale, const int32_t* expert_offset,
+                           moe_shape sh, const moe_expert_weights* w, void* y, void* stream) {
+  (void)h_scale;
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(sh, w)) != MOE_OK) return st;
+  if (sh.T == 0) return MOE_OK;
+  if (!ok_ptr(h) || !ok_ptr(expert_offset) || !ok_ptr(y)) return MOE_ERR_INVALID_ARG;
+  const FfnShape fs = ffn_shape(sh);
+  cudaError_t err;
+  if (w->dtype == MOE_F32)
+    err = launch_ffn_down_simt(fs, (const float*)h, expert_offset, w, (float*)y, S(stream));
+  else
+    err = launch_ffn_down_tc(fs, h, expert_offset, w, y, S(stream));
+  return cuda_status(err);
+}
+
+moe_status moe_expert_ffn(const void* x_perm, const float* x_perm_scale, const void* u,
+                          const float* u_scale, const int32_t* expert_offset, moe_shape sh,
+                          const moe_expert_weights* w, void* y, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(sh, w)) != MOE_OK) return st;
+  if (sh.T == 0) return MOE_OK;
+  const size_t need = moe_expert_ffn_workspace(sh, w->dtype);
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  st = moe_expert_gate_up(x_perm, x_perm_scale, u, u_scale, expert_offset, sh, w, workspace,
+                          nullptr, stream);
+  if (st != MOE_OK) return st;
+  return moe_expert_down(workspace, nullptr, expert_offset, sh, w, y, stream);
+}
+
+// ---------------------------------------------------------------------- combine ----
+
+moe_status moe_combine(const void* u, const void* y, moe_dtype dt, const float* topk_gate,
+                       const int32_t* inv_row, moe_shape sh, void* h_out, moe_dtype out_dt,
+                       void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if (!is_float_dtype(dt) || !is_float_dtype(out_dt)) return MOE_ERR_UNSUPPORTED;
+  if (sh.T == 0) return MOE_OK;
+  if (!ok_ptr(u) || !ok_ptr(y) || !ok_ptr(topk_gate) || !ok_ptr(inv_row) || !ok_ptr(h_out))
+    return MOE_ERR_INVALID_ARG;
+  if (((size_t)sh.d * elem_bytes(dt)) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(u, y, dt, topk_gate, inv_row, sh.T, sh.d, sh.K_r, sh.N_s,
+                                    h_out, out_dt, S(stream)));
+}
+
+// ------------------------------------------------------------------ end of step ----
+
+moe_status moe_bias_update(float* b, const int32_t* load, moe_shape sh, float gamma,
+                           void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(b) || !ok_ptr(load)) return MOE_ERR_INVALID_ARG;
+  if (!(gamma >= 0.f) || gamma > 1e30f) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_bias_update(b, load, sh.T, sh.N_r, sh.K_r, gamma, S(stream)));
+}
+
+moe_status moe_seq_balance_stat(const float* seq_p_sum, const int32_t* topk_idx,
+                                const int32_t* seq_offsets, int32_t n_seq, moe_shape sh,
+                                float alpha, float* stat_per_seq, float* stat_mean,
+                                void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if (n_seq < 1 || !ok_ptr(seq_p_sum) || !ok_ptr(seq_offsets) || !ok_ptr(stat_per_seq) ||
+      !ok_opt(stat_mean))
+    return MOE_ERR_INVALID_ARG;
+  if (sh.T > 0 && !ok_ptr(topk_idx)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_seq_stat(seq_p_sum, topk_idx, seq_offsets, n_seq, sh.N_r, sh.K_r,
+                                     alpha, stat_per_seq, stat_mean, S(stream)));
+}
+
+moe_status moe_device_error(int32_t* code, int32_t clear) {
+  if (code == nullptr) return MOE_ERR_INVALID_ARG;
+  return cuda_status(read_dev_error(code, clear != 0));
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// Combine: h'_t = u_t + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx_k}(u_t)
+// (DeepSeek-V3 Technical Report reading guide, Method §2, equation for h'_t;
+// pwwt.cn notes §四: the gate-weighted sum of the experts' outputs back at the token).
+//
+// One warp per token; each lane owns 16-byte column vectors, so every row read is a
+// fully coalesced 512-byte warp access.  The fp32 accumulation order is fixed: u,
+// shared experts ascending, routed slots k ascending (deterministic).
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+template <typename TIn> struct Vec;
+template <> struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const float* p, float (&v)[4]) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  }
+};
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(h[q]);
+      v[2 * q] = f.x; v[2 * q + 1] = f.y;
+    }
+  }
+};
+
+template <typename TOut, int N> __device__ void store_vec(TOut* p, const float (&v)[N]);
+template <> __device__ void store_vec<float, 4>(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <> __device__ void store_vec<float, 8>(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <> __device__ void store_vec<__nv_bfloat16, 8>(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 x;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&x);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+  *reinterpret_cast<uint4*>(p) = x;
+}
+template <> __device__ void store_vec<__nv_bfloat16, 4>(__nv_bfloat16* p, const float (&v)[4]) {
+  uint2 x;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&x);
+  h[0] = __floats2bfloat162_rn(v[0], v[1]);
+  h[1] = __floats2bfloat162_rn(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) = x;
+}
+
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
+                                                      const TIn* __restrict__ y,
+                                                      const float* __restrict__ gate,
+                                                      const int32_t* __restrict__ inv_row,
+                                                      int T, int d, int K_r, int N_s,
+                                                      TOut* __restrict__ out) {
+  constexpr int V = Vec<TIn>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  const float my_g = lane < K_r ? gate[(size_t)t * K_r + lane] : 0.f;
+  const int my_r = lane < K_r ? inv_row[(size_t)t * K_r + lane] : 0;
+  const size_t routed_rows = (size_t)T * K_r;
+  for (int c0 = 0; c0 < d; c0 += 32 * V) {
+    const int c = c0 + lane * V;
+    const bool ok = c < d;
+    float acc[V], tmp[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) acc[q] = 0.f;
+    if (ok) Vec<TIn>::load(u + (size_t)t * d + c, acc);
+    for (int s = 0; s < N_s; ++s) {
+      if (ok) {
+        Vec<TIn>::load(y + (routed_rows + (size_t)s * T + t) * d + c, tmp);
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] = __fadd_rn(acc[q], tmp[q]);
+      }
+    }
+#pragma unroll 4
+    for (int k = 0; k < K_r; ++k) {
+      const float g = __shfl_sync(0xffffffffu, my_g, k);
+      const int r = __shfl_sync(0xffffffffu, my_r, k);
+      if (ok) {
+        Vec<TIn>::load(y + (size_t)r * d + c, tmp);
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] = fmaf(g, tmp[q], acc[q]);
+      }
+    }
+    if (ok) store_vec<TOut, V>(out + (size_t)t * d + c, acc);
+  }
+}
+
+template <typename TIn, typename TOut>
+cudaError_t run(const void* u, const void* y, const float* gate, const int32_t* inv_row, int T,
+                int d, int K_r, int N_s, void* out, cudaStream_t st) {
+  combine_kernel<TIn, TOut><<<(T + 7) / 8, 256, 0, st>>>(
+      (const TIn*)u, (const TIn*)y, gate, inv_row, T, d, K_r, N_s, (TOut*)out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const void* u, const void* y, moe_dtype dt, const float* gate,
+                           const int32_t* inv_row, int T, int d, int K_r, int N_s,
+                           void* out, moe_dtype out_dt, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  if (dt == MOE_F32)
+    return out_dt == MOE_F32 ? run<float, float>(u, y, gate, inv_row, T, d, K_r, N_s, out, st)
+                             : run<float, __nv_bfloat16>(u, y, gate, inv_row, T, d, K_r, N_s, out, st);
+  return out_dt == MOE_F32
+             ? run<__nv_bfloat16, float>(u, y, gate, inv_row, T, d, K_r, N_s, out, st)
+             : run<__nv_bfloat16, __nv_bfloat16>(u, y, gate, inv_row, T, d, K_r, N_s, out, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,69 @@
+// Shared device helpers: error word, bounded waits, warp reductions, dtype loads.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Kernels that can time out receive the device address of the library's error word
+// (MOE_OK or MOE_ERR_TIMEOUT) and raise it with this.
+__device__ __forceinline__ void record_error(int32_t* err, int32_t code) {
+  if (err) atomicMax(err, code);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Every spin in this library gives up after this long, records MOE_ERR_TIMEOUT and
+// lets the kernel return.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// (key, index) is better than (key', index') when key > key', or equal keys and a
+// lower index.  A total order on finite keys, so every lane of a butterfly reduction
+// ends with the same winner.
+__device__ __forceinline__ bool better(float k, int i, float k2, int i2) {
+  return k > k2 || (k == k2 && i < i2);
+}
+
+struct KeyIdxVal {
+  float key;
+  int idx;
+  float val;
+};
+
+__device__ __forceinline__ KeyIdxVal warp_argmax(KeyIdxVal a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float k2 = __shfl_xor_sync(0xffffffffu, a.key, o);
+    int i2 = __shfl_xor_sync(0xffffffffu, a.idx, o);
+    float v2 = __shfl_xor_sync(0xffffffffu, a.val, o);
+    if (better(k2, i2, a.key, a.idx)) { a.key = k2; a.idx = i2; a.val = v2; }
+  }
+  return a;
+}
+
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+}  // namespace moe

@@ -1,0 +1,196 @@
+// Dispatch: whole-batch expert load, stable per-expert token lists and the gather of
+// token rows into expert order.  No token is dropped: an expert's segment holds
+// anywhere from 0 to T rows (pwwt.cn notes §1.4; szhzxw.cn "无Token丢弃").
+//
+// The token range is cut into chunks of kDispatchChunk tokens, one warp each.
+//   count:   per-chunk expert histogram (shared-memory integer atomics: exact).
+//   scan:    per expert, exclusive scan over chunks; load = column total; expert
+//            offsets = exclusive scan of load; chunk bases = offsets + column scan.
+//   scatter: each warp walks its chunk's (t, k) entries in order, 32 at a time;
+//            __match_any_sync groups equal experts, the rank inside a group is the
+//            number of lower lanes with the same expert.  Positions therefore grow
+//            with t inside every expert: the order is deterministic and stable.
+//   gather:  one warp per token reads its row once and writes it to its K_r rows.
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kMaxExpertsScan = 256;
+
+__global__ void __launch_bounds__(kWarps * 32) dispatch_count_kernel(
+    const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r, int32_t* __restrict__ counts) {
+  extern __shared__ int32_t cnt_sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kWarps + warp;
+  const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+  int32_t* cnt = cnt_sm + warp * N_r;
+  for (int i = lane; i < N_r; i += 32) cnt[i] = 0;
+  __syncwarp();
+  if (chunk < n_chunks) {
+    const int t0 = chunk * kDispatchChunk;
+    const int n_ent = (min(T, t0 + kDispatchChunk) - t0) * K_r;
+    const int32_t* src = topk_idx + (size_t)t0 * K_r;
+    for (int x = lane; x < n_ent; x += 32) atomicAdd(&cnt[src[x]], 1);
+    __syncwarp();
+    for (int i = lane; i < N_r; i += 32) counts[(size_t)chunk * N_r + i] = cnt[i];
+  }
+}
+
+// One block: column scans over chunks (one warp per expert at a time), then the scan
+// over experts, then chunk base = expert offset + column prefix.
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict__ counts,
+                                                             int n_chunks, int N_r,
+                                                             int32_t* __restrict__ load,
+                                                             int32_t* __restrict__ expert_offset) {
+  __shared__ int32_t tot[kMaxExpertsScan];
+  __shared__ int32_t excl[kMaxExpertsScan];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int i = warp; i < N_r; i += nw) {
+    int carry = 0;
+    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < n_chunks ? counts[(size_t)c * N_r + i] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (c < n_chunks) counts[(size_t)c * N_r + i] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tot[i] = carry;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of the N_r totals: each lane takes a contiguous span
+    const int span = (N_r + 31) / 32;
+    int local = 0;
+    for (int q = 0; q < span; ++q) {
+      const int i = lane * span + q;
+      if (i < N_r) local += tot[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int run = incl - local;
+    for (int q = 0; q < span; ++q) {
+      const int i = lane * span + q;
+      if (i < N_r) {
+        excl[i] = run;
+        expert_offset[i] = run;
+        load[i] = tot[i];
+        run += tot[i];
+      }
+    }
+    if (lane == 31) expert_offset[N_r] = incl;
+  }
+  __syncthreads();
+  const long long n = (long long)n_chunks * N_r;
+  for (long long x = threadIdx.x; x < n; x += blockDim.x) counts[x] += excl[x % N_r];
+}
+
+__global__ void __launch_bounds__(kWarps * 32) dispatch_scatter_kernel(
+    const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r,
+    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_token,
+    int32_t* __restrict__ inv_row) {
+  extern __shared__ int32_t run_sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kWarps + warp;
+  const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+  if (chunk >= n_chunks) return;
+  int32_t* run = run_sm + warp * N_r;
+  for (int i = lane; i < N_r; i += 32) run[i] = chunk_base[(size_t)chunk * N_r + i];
+  __syncwarp();
+  const int t0 = chunk * kDispatchChunk;
+  const int n_ent = (min(T, t0 + kDispatchChunk) - t0) * K_r;
+  const size_t e0 = (size_t)t0 * K_r;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = 0; base < n_ent; base += 32) {
+    const int x = base + lane;
+    const bool valid = x < n_ent;
+    const int ex = valid ? topk_idx[e0 + x] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, ex);
+    const int rank = __popc(peers & lt_mask);
+    int pos = 0;
+    if (valid) pos = run[ex] + rank;
+    __syncwarp();
+    if (valid && rank == 0) run[ex] += __popc(peers);
+    __syncwarp();
+    if (valid) {
+      perm_token[pos] = (int32_t)((e0 + x) / K_r);
+      inv_row[e0 + x] = pos;
+    }
+  }
+}
+
+// 16-byte vector copy of each token's row to its K_r destination rows.
+__global__ void __launch_bounds__(256) dispatch_gather_kernel(
+    const uint8_t* __restrict__ u, size_t row_bytes, const float* __restrict__ u_scale,
+    int scale_cols, const int32_t* __restrict__ inv_row, int T, int K_r,
+    uint8_t* __restrict__ x_perm, float* __restrict__ x_perm_scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  const int my_row = lane < K_r ? inv_row[(size_t)t * K_r + lane] : 0;
+  const uint4* src = reinterpret_cast<const uint4*>(u + (size_t)t * row_bytes);
+  const size_t nvec = row_bytes / 16;
+  // Every lane runs every iteration so that the shuffles below see the full warp.
+  for (size_t v0 = 0; v0 < nvec; v0 += 32) {
+    const size_t v = v0 + lane;
+    const bool ok = v < nvec;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (ok) val = __ldg(src + v);
+    for (int k = 0; k < K_r; ++k) {
+      const int r = __shfl_sync(0xffffffffu, my_row, k);
+      if (ok) reinterpret_cast<uint4*>(x_perm + (size_t)r * row_bytes)[v] = val;
+    }
+  }
+  if (u_scale) {
+    for (int c0 = 0; c0 < scale_cols; c0 += 32) {
+      const int c = c0 + lane;
+      const bool ok = c < scale_cols;
+      const float sc = ok ? u_scale[(size_t)t * scale_cols + c] : 0.f;
+      for (int k = 0; k < K_r; ++k) {
+        const int r = __shfl_sync(0xffffffffu, my_row, k);
+        if (ok) x_perm_scale[(size_t)r * scale_cols + c] = sc;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
+                            const void* u, size_t row_bytes, const float* u_scale,
+                            int scale_cols, int32_t* load, int32_t* expert_offset,
+                            int32_t* perm_token, int32_t* inv_row, void* x_perm,
+                            float* x_perm_scale, int32_t* ws_counts, cudaStream_t st) {
+  const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+  if (n_chunks == 0) {
+    cudaError_t err = cudaMemsetAsync(load, 0, sizeof(int32_t) * N_r, st);
+    if (err == cudaSuccess) err = cudaMemsetAsync(expert_offset, 0, sizeof(int32_t) * (N_r + 1), st);
+    return err;
+  }
+  const int blocks = (n_chunks + kWarps - 1) / kWarps;
+  const size_t smem = sizeof(int32_t) * kWarps * N_r;
+  dispatch_count_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts);
+  dispatch_scan_kernel<<<1, 1024, 0, st>>>(ws_counts, n_chunks, N_r, load, expert_offset);
+  dispatch_scatter_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
+                                                            perm_token, inv_row);
+  if (u && x_perm) {
+    dispatch_gather_kernel<<<(T + 7) / 8, 256, 0, st>>>(
+        (const uint8_t*)u, row_bytes, u_scale, scale_cols, inv_row, T, K_r,
+        (uint8_t*)x_perm, x_perm_scale);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

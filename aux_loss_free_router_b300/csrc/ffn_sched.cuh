@@ -1,0 +1,98 @@
+// Tile schedule over the variable-size expert segments, built on the device from
+// expert_offset (no host round trip).  Segment i < N_r is routed expert i with
+// rows [expert_offset[i], expert_offset[i+1]); segment N_r + s is shared expert s
+// over all T tokens.  Tiles are numbered segment-major, then n-tile, then m-tile,
+// so CTAs running at the same time share an expert's weight tile through L2.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kMaxShared = 32;
+constexpr int kMaxSegs = 256 + kMaxShared;
+
+struct SegTable {
+  int total, nseg, T, K_r, N_r;
+  int prefix[kMaxSegs + 1];  // tiles before segment i
+  int row0[kMaxSegs];        // first input row of the segment
+  int rows[kMaxSegs];        // rows in the segment (0..T)
+  int mt[kMaxSegs];          // m-tiles in the segment
+};
+
+struct TileCoord {
+  int seg, m, n;
+  int row0;      // first input row (x_perm row for routed, u row 0 for shared)
+  int rows;      // rows in the segment
+  int out_row0;  // first row in the FFN row space [T*K_r + N_s*T]
+};
+
+// All threads of the block call this; the caller synchronises afterwards.
+__device__ __forceinline__ void build_seg_table(SegTable& tab, const int32_t* __restrict__ off,
+                                                int T, int K_r, int N_r, int N_s, int BM,
+                                                int n_tiles_n) {
+  const int nseg = N_r + N_s;
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) {
+    int r0 = 0, rows = T;
+    if (i < N_r) {
+      r0 = off[i];
+      rows = off[i + 1] - r0;
+    }
+    tab.row0[i] = r0;
+    tab.rows[i] = rows;
+    tab.mt[i] = (rows + BM - 1) / BM;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int span = (nseg + 31) / 32;
+    int local = 0;
+    for (int q = 0; q < span; ++q) {
+      const int i = lane * span + q;
+      if (i < nseg) local += tab.mt[i] * n_tiles_n;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int q = 0; q < span; ++q) {
+      const int i = lane * span + q;
+      if (i < nseg) {
+        tab.prefix[i] = run;
+        run += tab.mt[i] * n_tiles_n;
+      }
+    }
+    if (lane == 31) {
+      tab.prefix[nseg] = incl;
+      tab.total = incl;
+      tab.nseg = nseg;
+      tab.T = T;
+      tab.K_r = K_r;
+      tab.N_r = N_r;
+    }
+  }
+}
+
+__device__ __forceinline__ TileCoord decode_tile(const SegTable& tab, int tile, int n_tiles_n) {
+  // largest segment i with prefix[i] <= tile; then prefix[i+1] > tile, so i is non-empty
+  int lo = 0, hi = tab.nseg;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tab.prefix[mid] <= tile) lo = mid; else hi = mid;
+  }
+  TileCoord c;
+  c.seg = lo;
+  const int within = tile - tab.prefix[lo];
+  const int mt = tab.mt[lo];
+  c.n = within / mt;
+  c.m = within - c.n * mt;
+  c.row0 = tab.row0[lo];
+  c.rows = tab.rows[lo];
+  c.out_row0 = lo < tab.N_r ? c.row0 : tab.T * tab.K_r + (lo - tab.N_r) * tab.T;
+  return c;
+}
+
+}  // namespace moe

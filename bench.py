@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Throughput of the DeepSeekMoE layer forward with auxiliary-loss-free routing.
+
+Workload (default): the DeepSeek-V3-shaped bf16 layer — T=8192 tokens (2 sequences of
+4096), d=7168, 256 routed experts with top-8 routing limited to 4 of 8 expert groups,
+1 shared expert, SwiGLU width 2048.  One step = route (affinity GEMM, sigmoid, biased
+group-limited top-8, gates, per-sequence P sums) -> dispatch (counts, permutation,
+row gather) -> gate/up GEMM with SwiGLU -> down GEMM -> combine with residual -> bias
+update -> sequence-wise balance statistic, all through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Under torchrun each rank runs an independent replica of the
+layer on its own batch (weak scaling); rank 0 prints the line with the whole-job
+throughput computed from the slowest rank's time.  ``--impl reference`` times the
+CPU oracle on bounded samples of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s at d=7168, 256e top-8; tensor-pipe & HBM % of peak"
+
+# ncu DRAM traffic (read + write bytes) of one gate/up GEMM launch at this workload,
+# valid only for the kernel source with this hash (null otherwise).
+NCU_TRAFFIC = {"kernel_src_sha": None, "bytes": None}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ environment ---
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, v: float) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.index = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.index, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.out.flush()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.out.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ algorithmic counts ---
+
+def work(cfg):
+    T, d, N_r, K_r, N_s, I = cfg.T, cfg.d, cfg.N_r, cfg.K_r, cfg.N_s, cfg.I
+    rows = T * K_r + N_s * T
+    return {
+        "router_flop": 2.0 * T * d * N_r,
+        "router_bytes": T * d * 2 + N_r * d * 2 + T * K_r * 8,
+        "gather_bytes": T * d * 2 + T * K_r * d * 2,
+        "gate_up_flop": 2.0 * rows * d * 2 * I,
+        "gate_up_bytes": (N_r + N_s) * 2 * I * d * 2 + rows * d * 2 + rows * I * 2,
+        "down_flop": 2.0 * rows * I * d,
+        "down_bytes": (N_r + N_s) * d * I * 2 + rows * I * 2 + rows * d * 2,
+        "combine_bytes": T * d * 2 + rows * d * 2 + T * d * 4 + T * K_r * 8,
+        "layer_flop": 2.0 * T * d * N_r + 2.0 * rows * d * 3 * I,
+    }
+
+
+def kernel_src_sha() -> str:
+    with open(os.path.join(ROOT, "aux_loss_free_router_b300", "csrc", "tc_ffn.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ oracle timing ---
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+class OracleSample:
+    """The CPU oracle on single tokens of the workload (inputs drawn on the host)."""
+
+    def __init__(self, cfg):
+        import oracle
+        self.oracle = oracle
+        self.cfg = cfg
+        x = synth.make_inputs(cfg, device="cpu", with_weights=False)
+        self.u = x["u"].float().numpy()
+        self.e = x["e"].float().numpy()
+        self.b = x["b"].numpy()
+        self.cache = {}
+        self.shared = [tuple(w.float().numpy() for w in synth.expert_weights(cfg, "shared", j))
+                       for j in range(cfg.N_s)]
+
+    def expert(self, i):
+        if i not in self.cache:
+            self.cache[i] = tuple(w.float().numpy() for w in synth.expert_weights(self.cfg, "routed", i))
+        return self.cache[i]
+
+    def prepare(self, tokens):
+        """Draw (untimed) the weights of every expert these tokens select."""
+        r = self.oracle.route(self.u[tokens], self.e, self.b, self.cfg.K_r, self.cfg.G, self.cfg.M)
+        for i in np.unique(r["idx"]):
+            self.expert(int(i))
+
+    def run(self, tokens) -> float:
+        o, c = self.oracle, self.cfg
+        t0 = time.perf_counter()
+        u = self.u[tokens]
+        r = o.route(u, self.e, self.b, c.K_r, c.G, c.M)
+        o.layer_output(u, r["idx"], r["gate"], self.expert, self.shared)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, n_tokens: int) -> dict:
+    s = OracleSample(cfg)
+    tokens = list(range(n_tokens))
+    s.prepare(tokens)
+    dt = s.run(tokens)
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"{n_tokens} tokens of the {cfg.name} workload (route + all "
+                      f"{cfg.K_r} routed and {cfg.N_s} shared expert FFNs + combine), "
+                      f"float64 NumPy, {dt:.2f} s"}
+
+
+def run_reference(args, cfg, ws, rank):
+    if rank != 0:
+        return
+    s = OracleSample(cfg)
+    tok = lambda k: [k % cfg.T]
+    for k in range(args.warmup + args.steps):
+        s.prepare(tok(k))
+    for k in range(args.warmup):
+        s.run(tok(k))
+    total = 0.0
+    for k in range(args.steps):
+        total += s.run(tok(args.warmup + k))
+    value = args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": "one token of the workload per step (route + expert FFNs "
+                                   "+ combine), float64 NumPy on the host cores"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(cfg):
+    return {"workload": f"{cfg.name}: DeepSeek-V3-shaped MoE layer forward" if cfg.name == "v3"
+            else f"{cfg.name} MoE layer forward",
+            "T": cfg.T, "d": cfg.d, "N_r": cfg.N_r, "K_r": cfg.K_r, "N_s": cfg.N_s, "I": cfg.I,
+            "G": cfg.G, "M": cfg.M, "n_seq": cfg.n_seq, "parallelism": "replicas",
+            "l2": "inputs larger than L2: every step reads all expert weights "
+                  f"({(cfg.N_r + cfg.N_s) * 3 * cfg.I * cfg.d * 2 / 1e9:.1f} GB)"}
+
+
+# --------------------------------------------------------------------- our arm ---
+
+def run_ours(args, cfg, ws, rank, local):
+    import aux_loss_free_router_b300 as moe
+    moe.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = synth.make_inputs(cfg, device=dev, u_seed=cfg.seed + rank)
+    w = {k: x[k] for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")}
+    layer = moe.MoELayer(T=cfg.T, d=cfg.d, N_r=cfg.N_r, K_r=cfg.K_r, N_s=cfg.N_s, I=cfg.I,
+                         G=cfg.G, M=cfg.M, e=x["e"], b=x["b"].clone(), weights=w,
+                         n_seq=cfg.n_seq, gamma=cfg.gamma, alpha=cfg.alpha)
+    u, off = x["u"], x["seq_offsets"]
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        layer.step(u, off)
+    torch.cuda.synchronize()
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    moe.launch_counter_reset()
+    t0.record(stream)
+    for k in range(K):
+        layer.step(u, off, events=evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    launches = moe.launch_counter()
+    clk = clocks.stop()
+    ms = max_over_ranks(ws, t0.elapsed_time(t1) / K)
+    stage_names = ["route", "dispatch", "gate_up", "down", "combine_bias_stat"]
+    stages = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
+              for i, n in enumerate(stage_names)}
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during the timed steps")
+
+    # end to end: pinned host tokens in, layer output + loads + statistic out
+    u_host = u.cpu().pin_memory()
+    h_host = torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory()
+    load_host = torch.empty(cfg.N_r, dtype=torch.int32).pin_memory()
+    stat_host = torch.empty(cfg.n_seq, dtype=torch.float32).pin_memory()
+    u_dev = torch.empty_like(u)
+    for _ in range(2):
+        u_dev.copy_(u_host, non_blocking=True)
+        layer.step(u_dev, off)
+        h_host.copy_(layer.out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        u_dev.copy_(u_host, non_blocking=True)
+        layer.step(u_dev, off)
+        h_host.copy_(layer.out, non_blocking=True)
+        load_host.copy_(layer.load, non_blocking=True)
+        stat_host.copy_(layer.stat, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(ws, e0.elapsed_time(e1) / K)
+
+    if rank != 0:
+        return
+    wk = work(cfg)
+    pk = peaks()
+    t_gu = stages["gate_up"] / 1e3
+    achieved = wk["gate_up_flop"] / t_gu / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    sha = kernel_src_sha()
+    traffic = NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["kernel_src_sha"] == sha else None
+    tok_s = cfg.T * ws / (ms / 1e3)
+    kernels = {
+        "route": {"ms": stages["route"], "GB/s": wk["router_bytes"] / (stages["route"] / 1e3) / 1e9,
+                  "TFLOP/s": wk["router_flop"] / (stages["route"] / 1e3) / 1e12},
+        "dispatch": {"ms": stages["dispatch"],
+                     "GB/s": wk["gather_bytes"] / (stages["dispatch"] / 1e3) / 1e9},
+        "gate_up": {"ms": stages["gate_up"], "TFLOP/s": achieved},
+        "down": {"ms": stages["down"],
+                 "TFLOP/s": wk["down_flop"] / (stages["down"] / 1e3) / 1e12},
+        "combine_bias_stat": {"ms": stages["combine_bias_stat"],
+                              "GB/s": wk["combine_bytes"] / (stages["combine_bias_stat"] / 1e3) / 1e9},
+    }
+    layer_roof_ms = 1e3 * max(wk["layer_flop"] / (pk["bf16_tflops_sustained"] * 1e12),
+                              ((cfg.N_r + cfg.N_s) * 3 * cfg.I * cfg.d * 2 + cfg.T * cfg.d * 6)
+                              / (pk["hbm_gbs"] * 1e9))
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(cfg),
+        "roofline": {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU GEMM, tcgen05)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{pk['source']} bf16 sustained"},
+        "layer_roofline_frac": layer_roof_ms / ms,
+        "kernels": kernels,
+        "e2e": {"value": cfg.T * ws / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": u_host.numel() * u_host.element_size(),
+                "d2h_bytes_per_step": h_host.numel() * h_host.element_size()
+                + load_host.numel() * 4 + stat_host.numel() * 4},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        del layer, x, w
+        torch.cuda.empty_cache()
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_tokens)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="v3", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--cpu-tokens", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    cfg = synth.config(args.config)
+    if args.impl == "reference":
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        run_reference(args, cfg, ws, int(os.environ.get("RANK", "0")))
+        return
+    ws, rank, local = dist_setup()
+    run_ours(args, cfg, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -17,8 +17,9 @@ u_t from a 4-component Gaussian mixture whose component means are 3*sqrt(d) alon
 random orthonormal directions, so that each component shifts every expert logit
 u_t.e_i by about N(0, 9) and a few experts dominate (see ``mixture_tokens``).
 
-Draw order for a given seed: u, e, b, then the shared experts' weights, then the
-routed experts' weights (per expert: gate, up, down).
+Every tensor has its own seeded random stream (``stream_seed``): u, e and b each,
+and each expert's weights (gate, up, down drawn in that order), so one expert can be
+drawn on its own.
 """
 from __future__ import annotations
 
@@ -29,7 +30,7 @@ from typing import Optional
 import torch
 
 __all__ = ["MoEConfig", "CONFIGS", "config", "make_inputs", "mixture_tokens",
-           "make_seq_offsets"]
+           "make_seq_offsets", "expert_weights", "stream_seed"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -94,6 +95,15 @@ def _gen(seed: int, device) -> torch.Generator:
     return g
 
 
+_TAGS = {"u": 1, "e": 2, "b": 3, "shared": 4, "routed": 5}
+
+
+def stream_seed(seed: int, tag: str, index: int = 0) -> int:
+    """Seed of one named random stream: every tensor (and every expert's weights) has
+    its own stream, so any single expert can be drawn without drawing the others."""
+    return (seed * 1_000_003 + _TAGS[tag] * 7_919 + index * 104_729) % (2 ** 62)
+
+
 def _normal(shape, std, g, device, dtype):
     x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
     if std != 1.0:
@@ -118,44 +128,49 @@ def mixture_tokens(T: int, d: int, seed: int, device="cpu", scale: float = 3.0,
     return noise + means[comp]
 
 
+def expert_weights(cfg: MoEConfig, kind: str, i: int, device="cpu", seed=None):
+    """(gate [I, d], up [I, d], down [d, I]) of routed (kind="routed") or shared
+    (kind="shared") expert i, drawn from that expert's own stream."""
+    seed = cfg.seed if seed is None else seed
+    g = _gen(stream_seed(seed, kind, i), device)
+    dt = cfg.torch_dtype
+    sg, sd = 1.0 / math.sqrt(cfg.d), 1.0 / math.sqrt(cfg.I)
+    return (_normal((cfg.I, cfg.d), sg, g, device, dt), _normal((cfg.I, cfg.d), sg, g, device, dt),
+            _normal((cfg.d, cfg.I), sd, g, device, dt))
+
+
 def make_inputs(cfg: MoEConfig, device="cpu", seed: Optional[int] = None,
                 u_seed: Optional[int] = None, with_weights: bool = True) -> dict:
     """All layer inputs for ``cfg`` as torch tensors on ``device``.
 
     Storage dtype is ``cfg.torch_dtype`` (bf16 values are rounded once from the fp32
     draws).  ``b`` is always fp32.  ``u_seed`` redraws only the tokens (used by the
-    skewed multi-step run, where step s uses seed 1000+s for u).
+    skewed multi-step run, where step s uses seed 1000+s for u).  The values depend
+    on the device's generator (CPU and CUDA streams differ), never on anything else.
     """
     seed = cfg.seed if seed is None else seed
     dt = cfg.torch_dtype
-    g = _gen(seed, device)
     T, d, N_r, N_s, I = cfg.T, cfg.d, cfg.N_r, cfg.N_s, cfg.I
     out = {}
+    us = u_seed if u_seed is not None else seed
     if cfg.skew:
-        out["u"] = mixture_tokens(T, d, seed=(u_seed if u_seed is not None else seed),
-                                  device=device).to(dt)
-        _ = torch.randn(1, generator=g, device=device)      # keep the draw order fixed
-    elif u_seed is not None:
-        out["u"] = _normal((T, d), 1.0, _gen(u_seed, device), device, dt)
-        _ = torch.randn(1, generator=g, device=device)
+        out["u"] = mixture_tokens(T, d, seed=us, device=device).to(dt)
     else:
-        out["u"] = _normal((T, d), 1.0, g, device, dt)
-    out["e"] = _normal((N_r, d), 1.0 / math.sqrt(d), g, device, dt)
+        out["u"] = _normal((T, d), 1.0, _gen(stream_seed(us, "u"), device), device, dt)
+    out["e"] = _normal((N_r, d), 1.0 / math.sqrt(d), _gen(stream_seed(seed, "e"), device),
+                       device, dt)
     if cfg.bias == "uniform":
-        out["b"] = (torch.rand(N_r, generator=g, device=device, dtype=torch.float32)
-                    * 0.02 - 0.01)
+        gb = _gen(stream_seed(seed, "b"), device)
+        out["b"] = torch.rand(N_r, generator=gb, device=device, dtype=torch.float32) * 0.02 - 0.01
     else:
         out["b"] = torch.zeros(N_r, device=device, dtype=torch.float32)
     if with_weights:
-        sg, sd = 1.0 / math.sqrt(d), 1.0 / math.sqrt(I)
-        for prefix, E in (("ws_", N_s), ("w_", N_r)):
+        for prefix, kind, E in (("ws_", "shared", N_s), ("w_", "routed", N_r)):
             wg = torch.empty(E, I, d, dtype=dt, device=device)
             wu = torch.empty(E, I, d, dtype=dt, device=device)
             wd = torch.empty(E, d, I, dtype=dt, device=device)
             for i in range(E):
-                wg[i] = _normal((I, d), sg, g, device, dt)
-                wu[i] = _normal((I, d), sg, g, device, dt)
-                wd[i] = _normal((d, I), sd, g, device, dt)
+                wg[i], wu[i], wd[i] = expert_weights(cfg, kind, i, device, seed)
             out[prefix + "gate"], out[prefix + "up"], out[prefix + "down"] = wg, wu, wd
     out["seq_offsets"] = make_seq_offsets(T, cfg.n_seq).to(device)
     return out

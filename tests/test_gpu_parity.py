@@ -1,0 +1,164 @@
+"""GPU parity of the whole path against the CPU oracle (marked gpu).
+
+Sizes: the tiny fp32 layer and the mid bf16 layer are compared element by element;
+the DeepSeek-V3-shaped layer is compared at full size on sampled tokens (routing,
+dispatch and the bias update on every token).  Edge cases: ragged token counts and
+hidden sizes that are not tile multiples, an empty batch, a single token, experts with
+no tokens and an expert with every token.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import aux_loss_free_router_b300 as moe
+from tests.layer_harness import (check_affinity, check_output_full, check_output_sampled,
+                                 check_routing, check_seq_stat, rel_l2, run_layer, to_np)
+
+pytestmark = pytest.mark.gpu
+
+# bf16 layer outputs: 2e-2 max-abs and 1e-2 relative L2 against the float64 oracle
+BF16_ABS, BF16_REL = 2e-2, 1e-2
+
+
+def test_tiny_fp32_layer_matches_oracle():
+    cfg = synth.config("tiny")
+    r = run_layer(cfg)
+    check_affinity(cfg, r, atol=2e-6)
+    idx, _ = check_routing(cfg, r)
+    check_seq_stat(cfg, r, idx)
+    check_output_full(cfg, r, rel_tol=1e-5)
+
+
+def test_mid_bf16_layer_matches_oracle():
+    cfg = synth.config("mid")
+    r = run_layer(cfg)
+    check_affinity(cfg, r, atol=2e-5)
+    idx, _ = check_routing(cfg, r)
+    check_seq_stat(cfg, r, idx)
+    check_output_full(cfg, r, rel_tol=BF16_REL, abs_tol=BF16_ABS)
+
+
+def test_v3_layer_full_size_sampled():
+    cfg = synth.config("v3")
+    r = run_layer(cfg)
+    # affinities on a token sample (the oracle's float64 GEMM over all tokens is slow)
+    x = r["inputs"]
+    sample = np.random.default_rng(0).choice(cfg.T, 48, replace=False)
+    sample = np.concatenate([sample, [0, cfg.T - 1]])
+    s_ref = oracle.affinity(to_np(x["u"][torch.as_tensor(sample, device="cuda")]), to_np(x["e"]))
+    assert np.abs(r["s_out"][sample] - s_ref).max() <= 5e-5
+    idx, _ = check_routing(cfg, r)
+    per = cfg.N_r // cfg.G
+    assert max(len(set((row // per).tolist())) for row in r["topk_idx"]) <= cfg.M
+    check_seq_stat(cfg, r, idx)
+    check_output_sampled(cfg, r, sample[:8], BF16_REL, BF16_ABS)
+
+
+def test_routing_with_own_scores_differs_only_at_near_ties():
+    """Full oracle routing (its own float64-derived s) against the library's: any
+    disagreement must sit where the competing keys are closer than the affinity
+    error bound."""
+    cfg = synth.config("mid", T=1024, n_seq=1)
+    r = run_layer(cfg)
+    x = r["inputs"]
+    s_ref = oracle.affinity(to_np(x["u"]), to_np(x["e"]))
+    b = to_np(r["b0"])
+    idx_ref = oracle.select_experts(s_ref, b, cfg.K_r)
+    keys = oracle.routing_keys(s_ref, b).astype(np.float64)
+    bad = np.nonzero((np.sort(idx_ref, 1) != np.sort(r["topk_idx"], 1)).any(1))[0]
+    for t in bad:
+        kth = np.sort(keys[t])[::-1]
+        gap = kth[cfg.K_r - 1] - kth[cfg.K_r]
+        assert gap <= 4e-5, (t, gap)
+    assert len(bad) <= cfg.T // 100
+
+
+@pytest.mark.parametrize("T,d,I,N_r,K_r,G,M,N_s", [
+    (300, 320, 200, 32, 4, 4, 2, 1),     # ragged T, d not a multiple of 64, I not of 128
+    (1, 256, 128, 64, 6, 1, 1, 2),       # a single token
+    (129, 512, 384, 64, 8, 8, 4, 0),     # no shared expert, group limit
+    (257, 1024, 256, 128, 8, 8, 2, 1),
+])
+def test_ragged_bf16_layers(T, d, I, N_r, K_r, G, M, N_s):
+    cfg = synth.MoEConfig("ragged", T=T, d=d, N_r=N_r, K_r=K_r, N_s=N_s, I=I, G=G, M=M,
+                          dtype="bf16", bias="uniform", seed=T)
+    r = run_layer(cfg)
+    check_affinity(cfg, r, atol=2e-5)
+    idx, _ = check_routing(cfg, r)
+    check_seq_stat(cfg, r, idx)
+    check_output_full(cfg, r, rel_tol=BF16_REL, abs_tol=BF16_ABS)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_empty_and_concentrated_experts(dtype):
+    # a bias of +1 on experts 0..K_r-1 sends every token there: the other experts get
+    # zero rows and the chosen ones all T rows
+    cfg = synth.MoEConfig("skewed", T=200, d=256, N_r=32, K_r=2, N_s=1, I=128,
+                          dtype=dtype, bias="zero", seed=3)
+    x = synth.make_inputs(cfg, device="cuda")
+    x["b"][:2] = 1.0
+    r = run_layer(cfg, x)
+    assert r["load"][:2].tolist() == [200, 200] and (r["load"][2:] == 0).all()
+    idx, _ = check_routing(cfg, r)
+    check_output_full(cfg, r, rel_tol=1e-5 if dtype == "f32" else BF16_REL)
+    # overloaded experts move down by gamma, the idle ones up
+    assert (r["b_new"][:2] < to_np(r["b0"])[:2]).all() and (r["b_new"][2:] > 0).all()
+
+
+def test_empty_batch():
+    cfg = synth.MoEConfig("empty", T=0, d=256, N_r=16, K_r=2, N_s=1, I=128, dtype="bf16")
+    sh = moe.make_shape(0, 256, 16, 2, 1, 128)
+    dev = "cuda"
+    e = torch.randn(16, 256, device=dev).bfloat16()
+    b = torch.zeros(16, device=dev)
+    idx = torch.empty(0, 2, dtype=torch.int32, device=dev)
+    gate = torch.empty(0, 2, device=dev)
+    load = torch.full((16,), 7, dtype=torch.int32, device=dev)
+    off = torch.full((17,), 7, dtype=torch.int32, device=dev)
+    u = torch.empty(0, 256, device=dev).bfloat16()
+    moe.route(u, e, b, sh, idx, gate)
+    moe.dispatch(idx, sh, load, off, torch.empty(0, dtype=torch.int32, device=dev),
+                 torch.empty(0, 2, dtype=torch.int32, device=dev))
+    moe.bias_update(b, load, sh, 0.001)
+    torch.cuda.synchronize()
+    assert (load == 0).all() and (off == 0).all()
+    assert (b == 0).all()        # zero load equals the zero mean: no change
+
+
+def test_layer_is_deterministic():
+    cfg = synth.config("mid", T=1024, n_seq=2)
+    x = synth.make_inputs(cfg, device="cuda")
+    r1 = run_layer(cfg, {k: v.clone() for k, v in x.items()})
+    r2 = run_layer(cfg, {k: v.clone() for k, v in x.items()})
+    for k in ("h", "topk_idx", "topk_gate", "perm_token", "inv_row", "stat", "b_new"):
+        np.testing.assert_array_equal(r1[k], r2[k], err_msg=k)
+
+
+def test_gathered_rows_are_token_rows():
+    cfg = synth.config("mid", T=512, n_seq=1)
+    r = run_layer(cfg)
+    layer, u = r["layer"], r["inputs"]["u"]
+    perm = layer.perm_token.long()
+    assert torch.equal(layer.x_perm, u[perm])
+
+
+def test_bias_update_moves_toward_balance_over_steps():
+    cfg = synth.config("skew", T=1024, n_seq=1)
+    x = synth.make_inputs(cfg, device="cuda")
+    w = {k: x[k] for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")}
+    layer = moe.MoELayer(T=cfg.T, d=cfg.d, N_r=cfg.N_r, K_r=cfg.K_r, N_s=cfg.N_s, I=cfg.I,
+                         G=1, M=1, e=x["e"], b=x["b"].clone(), weights=w, n_seq=1,
+                         gamma=0.01)
+    ratios = []
+    for step in range(40):
+        u = synth.make_inputs(cfg, device="cuda", u_seed=1000 + step, with_weights=False)["u"]
+        b_before = layer.b.clone()
+        layer.step(u, x["seq_offsets"])
+        load = layer.load.clone()
+        torch.cuda.synchronize()
+        ref = oracle.bias_update(to_np(b_before), to_np(load), cfg.T, cfg.K_r, 0.01)
+        np.testing.assert_array_equal(to_np(layer.b), ref)
+        ratios.append(load.max().item() / (cfg.T * cfg.K_r / cfg.N_r))
+    assert np.mean(ratios[-5:]) < np.mean(ratios[:5])
