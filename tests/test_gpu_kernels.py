@@ -1,0 +1,89 @@
+"""Single-call parity at the DeepSeek-V3 layer's full sizes (marked gpu): the router,
+the dispatch and the combine on their own, each against the CPU oracle.  These are
+also the small, weight-free cases used for detailed kernel profiles."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import aux_loss_free_router_b300 as moe
+from tests.layer_harness import to_np
+
+pytestmark = pytest.mark.gpu
+
+V3 = synth.config("v3")
+
+
+def _route(cfg, x, with_stat=True):
+    dev = "cuda"
+    sh = moe.make_shape(cfg.T, cfg.d, cfg.N_r, cfg.K_r, cfg.N_s, cfg.I, cfg.G, cfg.M)
+    idx = torch.empty(cfg.T, cfg.K_r, dtype=torch.int32, device=dev)
+    gate = torch.empty(cfg.T, cfg.K_r, dtype=torch.float32, device=dev)
+    s = torch.empty(cfg.T, cfg.N_r, dtype=torch.float32, device=dev)
+    psum = torch.empty(cfg.n_seq, cfg.N_r, dtype=torch.float32, device=dev) if with_stat else None
+    moe.route(x["u"], x["e"], x["b"], sh, idx, gate, s, x["seq_offsets"], cfg.n_seq, psum)
+    torch.cuda.synchronize()
+    return sh, idx, gate, s, psum
+
+
+def test_router_v3_shape_bit_exact():
+    x = synth.make_inputs(V3, device="cuda", with_weights=False)
+    for _ in range(3):                      # repeated launches: same bits every time
+        sh, idx, gate, s, psum = _route(V3, x)
+    s_np, b = to_np(s), to_np(x["b"])
+    idx_ref = oracle.select_experts(s_np, b, V3.K_r, V3.G, V3.M)
+    np.testing.assert_array_equal(to_np(idx), idx_ref)
+    np.testing.assert_allclose(to_np(gate), oracle.gate_values(s_np, idx_ref), rtol=1e-6)
+    np.testing.assert_allclose(to_np(psum), oracle.seq_p_sums(s_np, to_np(x["seq_offsets"])),
+                               rtol=1e-5)
+    rows = np.random.default_rng(1).choice(V3.T, 64, replace=False)
+    s_ref = oracle.affinity(to_np(x["u"][torch.as_tensor(rows, device="cuda")]), to_np(x["e"]))
+    assert np.abs(s_np[rows] - s_ref).max() < 5e-5
+
+
+def test_dispatch_v3_shape_bit_exact():
+    rng = np.random.default_rng(0)
+    # random distinct experts per token with a skewed popularity
+    p = rng.dirichlet(np.ones(V3.N_r) * 0.3)
+    idx = np.stack([rng.choice(V3.N_r, V3.K_r, replace=False, p=p) for _ in range(V3.T)])
+    dev = "cuda"
+    sh = moe.make_shape(V3.T, V3.d, V3.N_r, V3.K_r, V3.N_s, V3.I, V3.G, V3.M)
+    t_idx = torch.as_tensor(idx, dtype=torch.int32, device=dev)
+    u = synth.make_inputs(V3, device=dev, with_weights=False)["u"]
+    load = torch.empty(V3.N_r, dtype=torch.int32, device=dev)
+    off = torch.empty(V3.N_r + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(V3.T * V3.K_r, dtype=torch.int32, device=dev)
+    inv = torch.empty(V3.T, V3.K_r, dtype=torch.int32, device=dev)
+    xp = torch.empty(V3.T * V3.K_r, V3.d, dtype=torch.bfloat16, device=dev)
+    moe.dispatch(t_idx, sh, load, off, perm, inv, u, xp)
+    torch.cuda.synchronize()
+    ref = oracle.dispatch(idx, V3.N_r)
+    np.testing.assert_array_equal(to_np(load), ref["load"])
+    np.testing.assert_array_equal(to_np(off), ref["offset"])
+    np.testing.assert_array_equal(to_np(perm), ref["perm_token"])
+    np.testing.assert_array_equal(to_np(inv), ref["inv_row"])
+    assert torch.equal(xp, u[perm.long()])
+
+
+def test_combine_v3_shape_sampled():
+    dev = "cuda"
+    T, d, K_r, N_s = V3.T, V3.d, V3.K_r, V3.N_s
+    g = torch.Generator(device=dev).manual_seed(5)
+    u = torch.randn(T, d, device=dev, generator=g).bfloat16()
+    R = T * K_r + N_s * T
+    y = torch.randn(R, d, device=dev, generator=g).bfloat16()
+    gate = torch.rand(T, K_r, device=dev, generator=g)
+    gate /= gate.sum(1, keepdim=True)
+    inv = torch.randperm(T * K_r, device=dev, generator=g).int().view(T, K_r)
+    out = torch.empty(T, d, device=dev)
+    sh = moe.make_shape(T, d, V3.N_r, K_r, N_s, V3.I, V3.G, V3.M)
+    moe.combine(u, y, gate, inv, sh, out)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(2).choice(T, 32, replace=False)
+    for t in rows:
+        ref = to_np(u[t]).astype(np.float64)
+        ref = ref + sum(to_np(y[T * K_r + s * T + t]).astype(np.float64) for s in range(N_s))
+        for k in range(K_r):
+            ref = ref + float(gate[t, k]) * to_np(y[int(inv[t, k])]).astype(np.float64)
+        np.testing.assert_allclose(to_np(out[t]), ref, rtol=1e-5, atol=1e-5)
