@@ -87,7 +87,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 
 # Kernels each call enqueues for a non-empty batch (the launch count of a step).
-_KERNELS = {"moe_route": 1, "moe_dispatch": 3, "moe_quantize_e4m3": 1, "moe_expert_gate_up": 1,
+_KERNELS = {"moe_route": 2, "moe_dispatch": 3, "moe_quantize_e4m3": 1, "moe_expert_gate_up": 1,
             "moe_expert_down": 1, "moe_expert_ffn": 2, "moe_combine": 1, "moe_bias_update": 1,
             "moe_seq_balance_stat": 1}
 _launches = 0
@@ -163,8 +163,8 @@ def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
 def route(u, e, b, sh: Shape, topk_idx, topk_gate, s_out=None, seq_offsets=None, n_seq=0,
           seq_p_sum=None, workspace=None, stream=None):
     ws = workspace
-    if seq_p_sum is not None and ws is None:
-        ws = _workspace(route_workspace_bytes(sh, n_seq), u.device)
+    if ws is None:
+        ws = _workspace(route_workspace_bytes(sh, n_seq if seq_p_sum is not None else 0), u.device)
     _call("moe_route", _ptr(u), _ptr(e), _dt(u), _ptr(b), sh, _ptr(seq_offsets), n_seq,
           _ptr(topk_idx), _ptr(topk_gate), _ptr(s_out), _ptr(seq_p_sum), _ptr(ws),
           ws.numel() if ws is not None else 0, _stream(stream),
@@ -230,7 +230,8 @@ def bias_update(b, load, sh: Shape, gamma: float, stream=None):
 def seq_balance_stat(seq_p_sum, topk_idx, seq_offsets, n_seq: int, sh: Shape, alpha: float,
                      stat_per_seq, stat_mean=None, stream=None):
     _call("moe_seq_balance_stat", _ptr(seq_p_sum), _ptr(topk_idx), _ptr(seq_offsets), n_seq, sh,
-          alpha, _ptr(stat_per_seq), _ptr(stat_mean), _stream(stream))
+          alpha, _ptr(stat_per_seq), _ptr(stat_mean), _stream(stream),
+          extra_kernels=1 if stat_mean is not None else 0)
 
 
 def device_error(clear: bool = True) -> int:
@@ -314,3 +315,19 @@ class MoELayer:
                          self.stat, self.stat_mean, stream=stream)
         ev(5)
         return self.out
+
+    def capture(self, u: torch.Tensor, seq_offsets: torch.Tensor, steps: int = 1,
+                events: Optional[list] = None, pre=None, post=None) -> "torch.cuda.CUDAGraph":
+        """Capture `steps` consecutive steps (with optional per-step ``pre(k)`` /
+        ``post(k)`` callables, e.g. host<->device copies) into one CUDA graph; replaying it
+        runs them with no host work per kernel.  Per-step ``events`` must be created with
+        ``external=True``.  Call ``step()`` once before capturing (first-use setup)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for k in range(steps):
+                if pre is not None:
+                    pre(k)
+                self.step(u, seq_offsets, events=events[k] if events else None)
+                if post is not None:
+                    post(k)
+        return g

@@ -54,10 +54,32 @@ int moe_abi_version(void) { return MOE_ABI_VERSION; }
 
 // ------------------------------------------------------------------------ route ----
 
+namespace {
+
+bool router_uses_tc(const moe_shape& sh, moe_dtype dt) { return dt == MOE_BF16 && sh.N_r % 32 == 0; }
+
+struct RouteWs {
+  size_t z_bytes, sprime_bytes, partial_bytes;
+  size_t total() const { return z_bytes + sprime_bytes + partial_bytes; }
+};
+
+RouteWs route_ws(const moe_shape& sh, int n_seq, int S) {
+  RouteWs w{0, 0, 0};
+  if (sh.T <= 0) return w;
+  w.z_bytes = align256((size_t)S * sh.T * sh.N_r * sizeof(float));
+  if (n_seq > 0) {
+    w.sprime_bytes = align256((size_t)sh.T * sh.N_r * sizeof(float));
+    w.partial_bytes = align256((size_t)n_seq * kSeqSlabs * sh.N_r * sizeof(double));
+  }
+  return w;
+}
+
+}  // namespace
+
 size_t moe_route_workspace(moe_shape sh, int32_t n_seq) {
-  if (n_seq <= 0 || sh.T <= 0 || sh.N_r <= 0) return 0;
-  return align256((size_t)sh.T * sh.N_r * sizeof(float)) +
-         align256((size_t)n_seq * kSeqSlabs * sh.N_r * sizeof(double));
+  if (sh.T <= 0 || sh.N_r <= 0 || sh.d <= 0) return 0;
+  // sized for the tensor-core path's split-K partials (the CUDA-core path uses one)
+  return route_ws(sh, n_seq, router_tc_splits(sh.T, sh.d)).total();
 }
 
 moe_status moe_route(const void* u, const void* e, moe_dtype dt, const float* b, moe_shape sh,
@@ -72,29 +94,24 @@ moe_status moe_route(const void* u, const void* e, moe_dtype dt, const float* b,
   if (!ok_opt(s_out) || !ok_opt(seq_p_sum) || n_seq < 0) return MOE_ERR_INVALID_ARG;
   const bool want_stat = seq_p_sum != nullptr;
   if (want_stat && (n_seq < 1 || seq_offsets == nullptr)) return MOE_ERR_INVALID_ARG;
-  float* sprime = nullptr;
-  double* partial = nullptr;
-  if (want_stat && sh.T > 0) {
-    const size_t need = moe_route_workspace(sh, n_seq);
-    if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return MOE_ERR_WORKSPACE;
-    sprime = static_cast<float*>(workspace);
-    partial = reinterpret_cast<double*>(static_cast<char*>(workspace) +
-                                        align256((size_t)sh.T * sh.N_r * sizeof(float)));
+  if (sh.T == 0) {
+    if (!want_stat) return MOE_OK;
+    return cuda_status(cudaMemsetAsync(seq_p_sum, 0, sizeof(float) * n_seq * sh.N_r, S(stream)));
   }
+  const bool tc = router_uses_tc(sh, dt);
+  const int splits = tc ? router_tc_splits(sh.T, sh.d) : 1;
+  const RouteWs w = route_ws(sh, want_stat ? n_seq : 0, splits);
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < w.total()) return MOE_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  float* z_part = reinterpret_cast<float*>(ws);
+  float* sprime = want_stat ? reinterpret_cast<float*>(ws + w.z_bytes) : nullptr;
+  double* partial = want_stat ? reinterpret_cast<double*>(ws + w.z_bytes + w.sprime_bytes) : nullptr;
   RouteOut p{sh.T, sh.N_r, sh.K_r, sh.G, sh.M, topk_idx, topk_gate, s_out, sprime};
-  cudaError_t err = cudaSuccess;
-  if (sh.T > 0) {
-    const bool tc_ok = dt == MOE_BF16 && sh.N_r % 32 == 0;
-    err = tc_ok ? launch_router_tc(u, e, b, sh.d, p, S(stream))
-                : launch_router_simt(u, e, dt, b, sh.d, p, S(stream));
-  }
-  if (err == cudaSuccess && want_stat) {
-    if (sh.T > 0) {
-      err = launch_seq_psum(sprime, seq_offsets, n_seq, sh.N_r, partial, seq_p_sum, S(stream));
-    } else {
-      err = cudaMemsetAsync(seq_p_sum, 0, sizeof(float) * n_seq * sh.N_r, S(stream));
-    }
-  }
+  cudaError_t err = tc ? launch_router_gemm_tc(u, e, sh.T, sh.d, sh.N_r, z_part, S(stream))
+                       : launch_router_gemm_simt(u, e, dt, sh.T, sh.d, sh.N_r, z_part, S(stream));
+  if (err == cudaSuccess) err = launch_router_select(z_part, splits, b, p, S(stream));
+  if (err == cudaSuccess && want_stat)
+    err = launch_seq_psum(sprime, seq_offsets, n_seq, sh.N_r, partial, seq_p_sum, S(stream));
   return cuda_status(err);
 }
 

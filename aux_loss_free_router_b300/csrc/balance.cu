@@ -22,47 +22,49 @@ __global__ void bias_update_kernel(float* __restrict__ b, const int32_t* __restr
   b[i] = __fadd_rn(b[i], step);
 }
 
-// alpha * sum_i f_i P_i per sequence (pwwt.cn notes §1.2), one block for the batch:
-// per sequence an integer histogram of the selected experts, then a fixed-order fp64
-// sum.  f_i = N_r/(K_r*T_j) * count_i, P_i = seq_p_sum[j, i] / T_j.
-__global__ void __launch_bounds__(1024) seq_stat_kernel(const float* __restrict__ seq_p_sum,
-                                                        const int32_t* __restrict__ topk_idx,
-                                                        const int32_t* __restrict__ seq_offsets,
-                                                        int n_seq, int N_r, int K_r, float alpha,
-                                                        float* __restrict__ stat_per_seq,
-                                                        float* __restrict__ stat_mean) {
+// alpha * sum_i f_i P_i per sequence (pwwt.cn notes §1.2), one block per sequence: an
+// integer histogram of the experts selected in the sequence, then a fixed-order fp64
+// tree sum.  f_i = N_r/(K_r*T_j) * count_i, P_i = seq_p_sum[j, i] / T_j.
+__global__ void __launch_bounds__(256) seq_stat_kernel(const float* __restrict__ seq_p_sum,
+                                                       const int32_t* __restrict__ topk_idx,
+                                                       const int32_t* __restrict__ seq_offsets,
+                                                       int N_r, int K_r, float alpha,
+                                                       float* __restrict__ stat_per_seq) {
   __shared__ int32_t cnt[256];
   __shared__ double term[256];
-  double mean_acc = 0.0;
-  for (int j = 0; j < n_seq; ++j) {
-    for (int i = threadIdx.x; i < N_r; i += blockDim.x) cnt[i] = 0;
-    __syncthreads();
-    const int a = seq_offsets[j], z = seq_offsets[j + 1];
-    const long long n_ent = (long long)(z - a) * K_r;
-    const int32_t* src = topk_idx + (size_t)a * K_r;
-    for (long long x = threadIdx.x; x < n_ent; x += blockDim.x) atomicAdd(&cnt[src[x]], 1);
-    __syncthreads();
-    const int T_j = z - a;
-    for (int i = threadIdx.x; i < N_r; i += blockDim.x) {
-      double v = 0.0;
-      if (T_j > 0) {
-        const double f = (double)N_r / ((double)K_r * T_j) * (double)cnt[i];
-        const double P = (double)seq_p_sum[(size_t)j * N_r + i] / (double)T_j;
-        v = f * P;
-      }
-      term[i] = v;
+  const int j = blockIdx.x;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int a = seq_offsets[j], z = seq_offsets[j + 1];
+  const long long n_ent = (long long)(z - a) * K_r;
+  const int32_t* src = topk_idx + (size_t)a * K_r;
+  for (long long x = threadIdx.x; x < n_ent; x += blockDim.x) atomicAdd(&cnt[src[x]], 1);
+  __syncthreads();
+  const int T_j = z - a;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+    double v = 0.0;
+    if (i < N_r && T_j > 0) {
+      const double f = (double)N_r / ((double)K_r * T_j) * (double)cnt[i];
+      v = f * ((double)seq_p_sum[(size_t)j * N_r + i] / (double)T_j);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      double s = 0.0;
-      for (int i = 0; i < N_r; ++i) s += term[i];
-      const double st = (double)alpha * s;
-      stat_per_seq[j] = (float)st;
-      mean_acc += st;
-    }
+    term[i] = v;
+  }
+  __syncthreads();
+  for (int h = 128; h > 0; h >>= 1) {   // fixed pairing: deterministic
+    if (threadIdx.x < h) term[threadIdx.x] += term[threadIdx.x + h];
     __syncthreads();
   }
-  if (threadIdx.x == 0 && stat_mean) *stat_mean = n_seq > 0 ? (float)(mean_acc / n_seq) : 0.f;
+  if (threadIdx.x == 0) {
+    stat_per_seq[j] = (float)((double)alpha * term[0]);
+  }
+}
+
+// Mean over sequences, summed in order in fp64 (one thread: n_seq is small).
+__global__ void seq_mean_kernel(const float* __restrict__ stat_per_seq, int n_seq,
+                                float* __restrict__ stat_mean) {
+  double s = 0.0;
+  for (int j = 0; j < n_seq; ++j) s += (double)stat_per_seq[j];
+  *stat_mean = n_seq > 0 ? (float)(s / n_seq) : 0.f;
 }
 
 }  // namespace
@@ -93,8 +95,9 @@ cudaError_t launch_seq_stat(const float* seq_p_sum, const int32_t* topk_idx,
                             const int32_t* seq_offsets, int n_seq, int N_r, int K_r,
                             float alpha, float* stat_per_seq, float* stat_mean,
                             cudaStream_t st) {
-  seq_stat_kernel<<<1, 1024, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, n_seq, N_r, K_r, alpha,
-                                      stat_per_seq, stat_mean);
+  seq_stat_kernel<<<n_seq, 256, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, N_r, K_r, alpha,
+                                         stat_per_seq);
+  if (stat_mean) seq_mean_kernel<<<1, 1, 0, st>>>(stat_per_seq, n_seq, stat_mean);
   return cudaGetLastError();
 }
 

@@ -70,31 +70,40 @@ __global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
   const float my_g = lane < K_r ? gate[(size_t)t * K_r + lane] : 0.f;
   const int my_r = lane < K_r ? inv_row[(size_t)t * K_r + lane] : 0;
   const size_t routed_rows = (size_t)T * K_r;
-  for (int c0 = 0; c0 < d; c0 += 32 * V) {
-    const int c = c0 + lane * V;
-    const bool ok = c < d;
-    float acc[V], tmp[V];
+  // two 16-byte column vectors per lane per pass: twice the loads in flight
+  for (int c0 = 0; c0 < d; c0 += 64 * V) {
+    const int ca = c0 + lane * V, cb = ca + 32 * V;
+    const bool oka = ca < d, okb = cb < d;
+    float acc[2][V], tmp[2][V];
 #pragma unroll
-    for (int q = 0; q < V; ++q) acc[q] = 0.f;
-    if (ok) Vec<TIn>::load(u + (size_t)t * d + c, acc);
+    for (int q = 0; q < V; ++q) acc[0][q] = acc[1][q] = 0.f;
+    if (oka) Vec<TIn>::load(u + (size_t)t * d + ca, acc[0]);
+    if (okb) Vec<TIn>::load(u + (size_t)t * d + cb, acc[1]);
     for (int s = 0; s < N_s; ++s) {
-      if (ok) {
-        Vec<TIn>::load(y + (routed_rows + (size_t)s * T + t) * d + c, tmp);
+      const TIn* row = y + (routed_rows + (size_t)s * T + t) * d;
+      if (oka) Vec<TIn>::load(row + ca, tmp[0]);
+      if (okb) Vec<TIn>::load(row + cb, tmp[1]);
 #pragma unroll
-        for (int q = 0; q < V; ++q) acc[q] = __fadd_rn(acc[q], tmp[q]);
+      for (int q = 0; q < V; ++q) {
+        acc[0][q] = __fadd_rn(acc[0][q], tmp[0][q]);
+        acc[1][q] = __fadd_rn(acc[1][q], tmp[1][q]);
       }
     }
 #pragma unroll 4
     for (int k = 0; k < K_r; ++k) {
       const float g = __shfl_sync(0xffffffffu, my_g, k);
       const int r = __shfl_sync(0xffffffffu, my_r, k);
-      if (ok) {
-        Vec<TIn>::load(y + (size_t)r * d + c, tmp);
+      const TIn* row = y + (size_t)r * d;
+      if (oka) Vec<TIn>::load(row + ca, tmp[0]);
+      if (okb) Vec<TIn>::load(row + cb, tmp[1]);
 #pragma unroll
-        for (int q = 0; q < V; ++q) acc[q] = fmaf(g, tmp[q], acc[q]);
+      for (int q = 0; q < V; ++q) {
+        acc[0][q] = fmaf(g, tmp[0][q], acc[0][q]);
+        acc[1][q] = fmaf(g, tmp[1][q], acc[1][q]);
       }
     }
-    if (ok) store_vec<TOut, V>(out + (size_t)t * d + c, acc);
+    if (oka) store_vec<TOut, V>(out + (size_t)t * d + ca, acc[0]);
+    if (okb) store_vec<TOut, V>(out + (size_t)t * d + cb, acc[1]);
   }
 }
 

@@ -3,9 +3,11 @@
 // anywhere from 0 to T rows (pwwt.cn notes §1.4; szhzxw.cn "无Token丢弃").
 //
 // The token range is cut into chunks of kDispatchChunk tokens, one warp each.
-//   count:   per-chunk expert histogram (shared-memory integer atomics: exact).
-//   scan:    per expert, exclusive scan over chunks; load = column total; expert
-//            offsets = exclusive scan of load; chunk bases = offsets + column scan.
+//   count:   per-chunk expert histogram (shared-memory integer atomics: exact),
+//            stored expert-major.
+//   scan:    one warp per expert: exclusive scan over its chunks; load = the total.
+//   scatter: each warp scans load into expert offsets (the first warp publishes
+//            them); chunk base = expert offset + the expert's chunk prefix.
 //   scatter: each warp walks its chunk's (t, k) entries in order, 32 at a time;
 //            __match_any_sync groups equal experts, the rank inside a group is the
 //            number of lower lanes with the same expert.  Positions therefore grow
@@ -19,7 +21,6 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kMaxExpertsScan = 256;
 
 __global__ void __launch_bounds__(kWarps * 32) dispatch_count_kernel(
     const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r, int32_t* __restrict__ counts) {
@@ -36,70 +37,68 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_count_kernel(
     const int32_t* src = topk_idx + (size_t)t0 * K_r;
     for (int x = lane; x < n_ent; x += 32) atomicAdd(&cnt[src[x]], 1);
     __syncwarp();
-    for (int i = lane; i < N_r; i += 32) counts[(size_t)chunk * N_r + i] = cnt[i];
+    for (int i = lane; i < N_r; i += 32) counts[(size_t)i * n_chunks + chunk] = cnt[i];
   }
 }
 
-// One block: column scans over chunks (one warp per expert at a time), then the scan
-// over experts, then chunk base = expert offset + column prefix.
-__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict__ counts,
-                                                             int n_chunks, int N_r,
-                                                             int32_t* __restrict__ load,
-                                                             int32_t* __restrict__ expert_offset) {
-  __shared__ int32_t tot[kMaxExpertsScan];
-  __shared__ int32_t excl[kMaxExpertsScan];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int i = warp; i < N_r; i += nw) {
-    int carry = 0;
-    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < n_chunks ? counts[(size_t)c * N_r + i] : 0;
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      if (c < n_chunks) counts[(size_t)c * N_r + i] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) tot[i] = carry;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // exclusive scan of the N_r totals: each lane takes a contiguous span
-    const int span = (N_r + 31) / 32;
-    int local = 0;
-    for (int q = 0; q < span; ++q) {
-      const int i = lane * span + q;
-      if (i < N_r) local += tot[i];
-    }
-    int incl = local;
+// One warp per expert: exclusive scan of its chunk counts (expert-major rows, so the
+// loads are coalesced) in place; the row total is the expert's load.
+__global__ void __launch_bounds__(256) dispatch_scan_kernel(int32_t* __restrict__ counts,
+                                                            int n_chunks, int N_r,
+                                                            int32_t* __restrict__ load) {
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (i >= N_r) return;
+  int32_t* row = counts + (size_t)i * n_chunks;
+  int carry = 0;
+  for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+    const int c = c0 + lane;
+    const int v = c < n_chunks ? row[c] : 0;
+    int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += n;
     }
-    int run = incl - local;
-    for (int q = 0; q < span; ++q) {
-      const int i = lane * span + q;
-      if (i < N_r) {
-        excl[i] = run;
-        expert_offset[i] = run;
-        load[i] = tot[i];
-        run += tot[i];
-      }
-    }
-    if (lane == 31) expert_offset[N_r] = incl;
+    if (c < n_chunks) row[c] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
   }
-  __syncthreads();
-  const long long n = (long long)n_chunks * N_r;
-  for (long long x = threadIdx.x; x < n; x += blockDim.x) counts[x] += excl[x % N_r];
+  if (lane == 0) load[i] = carry;
+}
+
+// Exclusive scan of load over the N_r experts by one warp (each lane a contiguous span);
+// result in shared memory, and in expert_offset when `out` is set.
+__device__ __forceinline__ void expert_offsets(const int32_t* __restrict__ load, int N_r,
+                                               int32_t* off_sm, int32_t* out) {
+  const int lane = threadIdx.x & 31;
+  const int span = (N_r + 31) / 32;
+  int local = 0;
+  for (int q = 0; q < span; ++q) {
+    const int i = lane * span + q;
+    if (i < N_r) local += load[i];
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  int run = incl - local;
+  for (int q = 0; q < span; ++q) {
+    const int i = lane * span + q;
+    if (i < N_r) {
+      off_sm[i] = run;
+      if (out) out[i] = run;
+      run += load[i];
+    }
+  }
+  if (out && lane == 31) out[N_r] = incl;
 }
 
 __global__ void __launch_bounds__(kWarps * 32) dispatch_scatter_kernel(
     const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r,
-    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_token,
+    const int32_t* __restrict__ chunk_prefix, const int32_t* __restrict__ load,
+    int32_t* __restrict__ expert_offset, int32_t* __restrict__ perm_token,
     int32_t* __restrict__ inv_row) {
   extern __shared__ int32_t run_sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,7 +106,10 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_scatter_kernel(
   const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
   if (chunk >= n_chunks) return;
   int32_t* run = run_sm + warp * N_r;
-  for (int i = lane; i < N_r; i += 32) run[i] = chunk_base[(size_t)chunk * N_r + i];
+  // every warp derives the expert offsets itself; the first one also publishes them
+  expert_offsets(load, N_r, run, chunk == 0 ? expert_offset : nullptr);
+  __syncwarp();
+  for (int i = lane; i < N_r; i += 32) run[i] += chunk_prefix[(size_t)i * n_chunks + chunk];
   __syncwarp();
   const int t0 = chunk * kDispatchChunk;
   const int n_ent = (min(T, t0 + kDispatchChunk) - t0) * K_r;
@@ -182,9 +184,10 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
   const int blocks = (n_chunks + kWarps - 1) / kWarps;
   const size_t smem = sizeof(int32_t) * kWarps * N_r;
   dispatch_count_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts);
-  dispatch_scan_kernel<<<1, 1024, 0, st>>>(ws_counts, n_chunks, N_r, load, expert_offset);
+  dispatch_scan_kernel<<<(N_r + 7) / 8, 256, 0, st>>>(ws_counts, n_chunks, N_r, load);
   dispatch_scatter_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
-                                                            perm_token, inv_row);
+                                                            load, expert_offset, perm_token,
+                                                            inv_row);
   if (u && x_perm) {
     dispatch_gather_kernel<<<(T + 7) / 8, 256, 0, st>>>(
         (const uint8_t*)u, row_bytes, u_scale, scale_cols, inv_row, T, K_r,

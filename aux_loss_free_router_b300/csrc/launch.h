@@ -26,11 +26,13 @@ int device_sm_count();
 int32_t* dev_error_ptr();                        // device address of the error word
 cudaError_t read_dev_error(int32_t* code, bool clear);   // synchronises the device
 
-size_t router_simt_smem(int N_r);
-cudaError_t launch_router_simt(const void* u, const void* e, moe_dtype dt, const float* b,
-                               int d, const RouteOut& p, cudaStream_t st);
-cudaError_t launch_router_tc(const void* u, const void* e, const float* b, int d,
-                             const RouteOut& p, cudaStream_t st);
+int router_tc_splits(int T, int d);   // split-K factor of the tensor-core affinity GEMM
+cudaError_t launch_router_gemm_tc(const void* u, const void* e, int T, int d, int N_r,
+                                  float* z_part, cudaStream_t st);
+cudaError_t launch_router_gemm_simt(const void* u, const void* e, moe_dtype dt, int T, int d,
+                                    int N_r, float* z, cudaStream_t st);
+cudaError_t launch_router_select(const float* z_part, int S, const float* b, const RouteOut& p,
+                                 cudaStream_t st);
 cudaError_t launch_seq_psum(const float* sprime, const int32_t* seq_offsets, int n_seq,
                             int N_r, double* partial, float* out, cudaStream_t st);
 

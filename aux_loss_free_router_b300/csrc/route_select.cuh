@@ -122,6 +122,99 @@ __device__ __forceinline__ void route_token(const float* s_row, const float* b_s
   }
 }
 
+constexpr int kFastK = 8;    // per-thread selection keeps the 8 largest keys
+constexpr int kFastG = 16;   // and handles up to 16 groups of whole 32-column chunks
+
+// One thread takes the whole decision for its token.  c1/c2 hold the two largest keys
+// of every 32-column chunk; with the group limit a group is per/32 whole chunks and
+// keeps its K_r/M <= 2 best keys.  Candidates are visited in ascending expert index
+// and only a strictly larger key displaces a list entry, so equal keys keep the lower
+// index first, as the definition requires.
+__device__ __forceinline__ void select_row(const float* s_row, const float* b,
+                                           const float (&c1)[kMaxSlots],
+                                           const float (&c2)[kMaxSlots], int t,
+                                           const RouteOut& p) {
+  if (t >= p.T) return;
+  const int N_r = p.N_r;
+  unsigned keep = 0xffffffffu;
+  int per = N_r, n_keep = 1;
+  if (p.G > 1) {
+    per = N_r / p.G;
+    const int cpg = per / 32, kg = p.K_r / p.M;
+    float gs[kFastG];
+#pragma unroll
+    for (int g = 0; g < kFastG; ++g) {
+      float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < kMaxSlots; ++c) {
+        if (c / cpg == g && c < N_r / 32) {   // chunk c belongs to group g
+          const float lo = fminf(t1, c1[c]);
+          t1 = fmaxf(t1, c1[c]);
+          t2 = fmaxf(lo, fmaxf(t2, c2[c]));
+        }
+      }
+      gs[g] = kg == 1 ? t1 : __fadd_rn(t1, t2);   // fp32, descending order
+    }
+    keep = 0;
+    for (int m = 0; m < p.M; ++m) {
+      float best = -CUDART_INF_F;
+      int bg = 0;
+#pragma unroll
+      for (int g = kFastG - 1; g >= 0; --g)   // descending scan: ties settle on the lower g
+        if (g < p.G && !((keep >> g) & 1u) && gs[g] >= best) { best = gs[g]; bg = g; }
+      keep |= 1u << bg;
+    }
+    n_keep = p.M;
+  }
+  float lk[kFastK];
+  int li[kFastK];
+#pragma unroll
+  for (int j = 0; j < kFastK; ++j) { lk[j] = -CUDART_INF_F; li[j] = 0; }
+  for (int m = 0; m < n_keep; ++m) {
+    const int g = p.G > 1 ? (int)__fns(keep, 0, m + 1) : 0;   // m-th kept group, ascending
+    const int c0 = g * per;
+    for (int j0 = 0; j0 < per; ++j0) {
+      const int i = c0 + j0;
+      const float v = __fadd_rn(s_row[i], b[i]);
+      if (v > lk[kFastK - 1]) {
+        bool cj[kFastK];
+#pragma unroll
+        for (int j = 0; j < kFastK; ++j) cj[j] = v > lk[j];
+#pragma unroll
+        for (int j = kFastK - 1; j >= 1; --j) {
+          const float nk = cj[j - 1] ? lk[j - 1] : (cj[j] ? v : lk[j]);
+          const int ni = cj[j - 1] ? li[j - 1] : (cj[j] ? i : li[j]);
+          lk[j] = nk;
+          li[j] = ni;
+        }
+        if (cj[0]) { lk[0] = v; li[0] = i; }
+      }
+    }
+  }
+  float total = 0.f, sel[kFastK];
+#pragma unroll
+  for (int j = 0; j < kFastK; ++j) {
+    sel[j] = j < p.K_r ? s_row[li[j]] : 0.f;
+    if (j < p.K_r) total = __fadd_rn(total, sel[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < kFastK; ++j) {
+    if (j < p.K_r) {
+      p.topk_idx[(size_t)t * p.K_r + j] = li[j];
+      p.topk_gate[(size_t)t * p.K_r + j] = __fdiv_rn(sel[j], total);
+    }
+  }
+}
+
+// Whether select_row() handles the shape: K_r <= 8, and either no group limit or
+// groups made of whole 32-expert chunks (at most 16 groups) keeping <= 2 keys each.
+inline bool fast_select_ok(int N_r, int K_r, int G, int M) {
+  if (K_r > kFastK || N_r % 32 != 0) return false;
+  if (G == 1) return true;
+  const int per = N_r / G;
+  return per % 32 == 0 && G <= kFastG && K_r / M <= 2;
+}
+
 __device__ __forceinline__ float sigmoid_f32(float z) {
   return __fdiv_rn(1.f, __fadd_rn(1.f, expf(-z)));
 }

@@ -10,6 +10,9 @@ update -> sequence-wise balance statistic, all through the C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+The timed region replays a CUDA graph of exactly K captured steps (kernel launches
+through the C ABI, recorded once), so the host adds no per-kernel overhead.
+
 Prints one JSON line.  Under torchrun each rank runs an independent replica of the
 layer on its own batch (weak scaling); rank 0 prints the line with the whole-job
 throughput computed from the slowest rank's time.  ``--impl reference`` times the
@@ -205,11 +208,18 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
-def cpu_baseline(cfg, n_tokens: int) -> dict:
+def cpu_baseline(cfg, n_tokens: int, group: int = 4) -> dict:
+    """Oracle time for n_tokens tokens, taken `group` tokens at a time; each group's
+    expert weights are drawn (untimed) before it runs and dropped after, which bounds
+    host memory."""
     s = OracleSample(cfg)
-    tokens = list(range(n_tokens))
-    s.prepare(tokens)
-    dt = s.run(tokens)
+    dt = 0.0
+    for g0 in range(0, n_tokens, group):
+        tokens = list(range(g0, min(n_tokens, g0 + group)))
+        s.cache.clear()
+        s.prepare(tokens)
+        dt += s.run(tokens)
+    s.cache.clear()
     return {"value": n_tokens / dt, "unit": "tokens/s", "cores": blas_threads(),
             "kind": "oracle",
             "sample": f"{n_tokens} tokens of the {cfg.name} workload (route + all "
@@ -222,13 +232,13 @@ def run_reference(args, cfg, ws, rank):
         return
     s = OracleSample(cfg)
     tok = lambda k: [k % cfg.T]
-    for k in range(args.warmup + args.steps):
-        s.prepare(tok(k))
-    for k in range(args.warmup):
-        s.run(tok(k))
     total = 0.0
-    for k in range(args.steps):
-        total += s.run(tok(args.warmup + k))
+    for k in range(args.warmup + args.steps):
+        s.cache.clear()
+        s.prepare(tok(k))            # untimed: draws the weights this token needs
+        dt = s.run(tok(k))
+        if k >= args.warmup:
+            total += dt
     value = args.steps / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
@@ -275,22 +285,27 @@ def run_ours(args, cfg, ws, rank, local):
     if moe.device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
+    # The timed region replays one CUDA graph holding exactly K steps; per-stage
+    # events are recorded inside it.  One untimed replay first.
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+           for _ in range(K)]
+    moe.launch_counter_reset()
+    graph = layer.capture(u, off, steps=K, events=evs)
+    launches = moe.launch_counter()
+    graph.replay()
+    torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     barrier(ws)
     torch.cuda.synchronize()
-    moe.launch_counter_reset()
     t0.record(stream)
-    for k in range(K):
-        layer.step(u, off, events=evs[k])
+    graph.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
-    launches = moe.launch_counter()
     clk = clocks.stop()
     ms = max_over_ranks(ws, t0.elapsed_time(t1) / K)
     stage_names = ["route", "dispatch", "gate_up", "down", "combine_bias_stat"]
@@ -298,31 +313,41 @@ def run_ours(args, cfg, ws, rank, local):
               for i, n in enumerate(stage_names)}
     if moe.device_error() != 0:
         raise RuntimeError("device error word set during the timed steps")
+    del graph
 
-    # end to end: pinned host tokens in, layer output + loads + statistic out
+    # end to end: pinned host tokens in, layer output + loads + statistic out, every
+    # step, inside one captured graph of K steps
     u_host = u.cpu().pin_memory()
     h_host = torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory()
     load_host = torch.empty(cfg.N_r, dtype=torch.int32).pin_memory()
     stat_host = torch.empty(cfg.n_seq, dtype=torch.float32).pin_memory()
     u_dev = torch.empty_like(u)
-    for _ in range(2):
+
+    def h2d(k):
         u_dev.copy_(u_host, non_blocking=True)
-        layer.step(u_dev, off)
+
+    def d2h(k):
         h_host.copy_(layer.out, non_blocking=True)
+        load_host.copy_(layer.load, non_blocking=True)
+        stat_host.copy_(layer.stat, non_blocking=True)
+
+    g_e2e = layer.capture(u_dev, off, steps=K, pre=h2d, post=d2h)
+    g_e2e.replay()
     torch.cuda.synchronize()
     barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(K):
-        u_dev.copy_(u_host, non_blocking=True)
-        layer.step(u_dev, off)
-        h_host.copy_(layer.out, non_blocking=True)
-        load_host.copy_(layer.load, non_blocking=True)
-        stat_host.copy_(layer.stat, non_blocking=True)
+    g_e2e.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     e2e_ms = max_over_ranks(ws, e0.elapsed_time(e1) / K)
+    del g_e2e
+
+    balance = decode = None
+    if cfg.skew:
+        balance = balance_run(moe, cfg, layer, off, dev, stream)
+        decode = decode_pass(moe, cfg, x, dev, stream)
 
     if rank != 0:
         return
@@ -366,11 +391,67 @@ def run_ours(args, cfg, ws, rank, local):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if balance is not None:
+        line["balance_run"] = balance
+        line["decode"] = decode
     if ws == 1 and not args.no_cpu_baseline:
         del layer, x, w
         torch.cuda.empty_cache()
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_tokens)
     print(json.dumps(line), flush=True)
+
+
+def balance_run(moe, cfg, layer, off, dev, stream, steps: int = 200) -> dict:
+    """The skewed workload's balance run: `steps` steps of forward + load count + bias
+    update, each on fresh mixture tokens (seed 1000 + step); reports max/mean expert
+    load per step and the layer throughput over the run."""
+    us = [synth.make_inputs(cfg, device=dev, u_seed=1000 + s, with_weights=False)["u"]
+          for s in range(steps)]
+    loads = torch.empty(steps, cfg.N_r, dtype=torch.int32, device=dev)
+    u_buf = torch.empty_like(us[0])
+    u_buf.copy_(us[0])
+    g = layer.capture(u_buf, off, steps=1)
+    layer.b.zero_()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s_ in range(steps):
+        u_buf.copy_(us[s_], non_blocking=True)
+        g.replay()
+        loads[s_].copy_(layer.load, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    mean = cfg.T * cfg.K_r / cfg.N_r
+    ratio = (loads.max(dim=1).values.float() / mean).cpu().tolist()
+    return {"steps": steps, "gamma": cfg.gamma, "tokens_per_s": cfg.T / (ms / 1e3),
+            "ms_per_step": ms, "max_over_mean_load": [round(r, 4) for r in ratio],
+            "first10_mean": sum(ratio[:10]) / 10, "last10_mean": sum(ratio[-10:]) / 10,
+            "b_absmax_end": float(layer.b.abs().max())}
+
+
+def decode_pass(moe, cfg, x, dev, stream, T: int = 128, steps: int = 50) -> dict:
+    """A decode-sized batch (T tokens) through the same layer weights."""
+    w = {k: x[k] for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")}
+    lay = moe.MoELayer(T=T, d=cfg.d, N_r=cfg.N_r, K_r=cfg.K_r, N_s=cfg.N_s, I=cfg.I, G=cfg.G,
+                       M=cfg.M, e=x["e"], b=x["b"].clone(), weights=w, n_seq=1,
+                       gamma=cfg.gamma, alpha=cfg.alpha)
+    u = synth.make_inputs(cfg.replace(T=T, n_seq=1), device=dev, u_seed=7, with_weights=False)["u"]
+    off = synth.make_seq_offsets(T, 1).to(dev)
+    for _ in range(3):
+        lay.step(u, off)
+    g = lay.capture(u, off, steps=steps)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    wbytes = (cfg.N_r + cfg.N_s) * 3 * cfg.I * cfg.d * 2
+    return {"T": T, "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3),
+            "weight_GB_per_s_if_all_read": wbytes / (ms / 1e3) / 1e9}
 
 
 def main():

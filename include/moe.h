@@ -111,7 +111,10 @@ MOE_API int moe_abi_version(void);
  *   s_out [T, N_r] fp32 out or NULL: the affinities in fp32.
  *   seq_p_sum [n_seq, N_r] fp32 out or NULL: sum over tokens t of sequence j of
  *     s_{i,t} / sum_k s_{k,t} (input of moe_seq_balance_stat).
- *   workspace: moe_route_workspace(sh, n_seq) bytes (0 when seq_p_sum is NULL).
+ *   workspace: moe_route_workspace(sh, n_seq) bytes, queried with the device that
+ *     will run the call current (the affinity GEMM splits the d dimension according
+ *     to the device's SM count; the partial products live there).  Pass n_seq = 0 to
+ *     the query when seq_p_sum will be NULL.
  * The keys s+b are formed as one fp32 addition; a group's score is the fp32 sum of
  * its K_r/M largest keys in descending order. */
 MOE_API size_t moe_route_workspace(moe_shape sh, int32_t n_seq);

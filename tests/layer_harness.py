@@ -84,15 +84,20 @@ def oracle_weights(x: dict) -> dict:
     return {k: to_np(x[k]) for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")}
 
 
-def check_output_full(cfg, r, rel_tol, abs_tol=None):
+def check_output_full(cfg, r, rel_tol, abs_tol=None, abs_per_rms=False):
+    """rel L2 and max-abs of h' against the oracle.  With ``abs_per_rms`` the max-abs
+    bound scales with the reference's RMS when that exceeds 1 (inputs far from unit
+    scale, as the Gaussian-mixture tokens are)."""
     x = r["inputs"]
     ref = oracle.moe_forward(to_np(x["u"]), to_np(x["e"]), to_np(r["b0"]), oracle_weights(x),
                              cfg.K_r, cfg.G, cfg.M, cfg.N_s, s=r["s_out"])
     err = rel_l2(r["h"], ref["h"])
     assert err <= rel_tol, f"rel L2 {err}"
     if abs_tol is not None:
+        if abs_per_rms:
+            abs_tol = abs_tol * max(1.0, float(np.sqrt(np.mean(ref["h"] ** 2))))
         mx = np.abs(r["h"] - ref["h"]).max()
-        assert mx <= abs_tol, f"max abs {mx}"
+        assert mx <= abs_tol, f"max abs {mx} (bound {abs_tol})"
     return ref
 
 

@@ -162,3 +162,41 @@ def test_bias_update_moves_toward_balance_over_steps():
         np.testing.assert_array_equal(to_np(layer.b), ref)
         ratios.append(load.max().item() / (cfg.T * cfg.K_r / cfg.N_r))
     assert np.mean(ratios[-5:]) < np.mean(ratios[:5])
+
+
+def test_skewed_balance_run_200_steps():
+    """The skewed workload: 200 steps of forward + load count + bias update with
+    gamma = 0.001 on Gaussian-mixture tokens.  Every step's update equals the oracle's
+    update of that step's loads, routing is bit-exact at sampled steps, and the
+    imbalance falls."""
+    cfg = synth.config("skew")
+    x = synth.make_inputs(cfg, device="cuda")
+    w = {k: x[k] for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")}
+    layer = moe.MoELayer(T=cfg.T, d=cfg.d, N_r=cfg.N_r, K_r=cfg.K_r, N_s=cfg.N_s, I=cfg.I,
+                         G=1, M=1, e=x["e"], b=x["b"].clone(), weights=w, n_seq=cfg.n_seq,
+                         gamma=cfg.gamma, want_s=True)
+    mean = cfg.T * cfg.K_r / cfg.N_r
+    ratios = []
+    for step in range(200):
+        u = synth.make_inputs(cfg, device="cuda", u_seed=1000 + step, with_weights=False)["u"]
+        b_before = to_np(layer.b)
+        layer.step(u, x["seq_offsets"])
+        torch.cuda.synchronize()
+        load = to_np(layer.load)
+        np.testing.assert_array_equal(
+            to_np(layer.b), oracle.bias_update(b_before, load, cfg.T, cfg.K_r, cfg.gamma))
+        if step in (0, 99, 199):
+            idx = oracle.select_experts(to_np(layer.s_out), b_before, cfg.K_r)
+            np.testing.assert_array_equal(to_np(layer.topk_idx), idx)
+        ratios.append(load.max() / mean)
+    assert ratios[0] > 1.5                     # the mixture does skew the routing
+    assert np.mean(ratios[-20:]) < np.mean(ratios[:20])
+
+
+def test_decode_sized_pass():
+    # mixture tokens have ~sqrt(10) times the norm of N(0,1) tokens, and h' scales with
+    # them: the max-abs bound is taken relative to the output RMS
+    cfg = synth.config("skew", T=128, n_seq=1)
+    r = run_layer(cfg)
+    idx, _ = check_routing(cfg, r)
+    check_output_full(cfg, r, rel_tol=BF16_REL, abs_tol=BF16_ABS, abs_per_rms=True)
