@@ -18,7 +18,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "MoEError", "Shape", "load_library", "route", "dispatch", "quantize_e4m3",
+    "MoEError", "Shape", "load_library", "route", "dispatch", "dispatch_noalloc", "quantize_e4m3",
     "expert_gate_up", "expert_down", "expert_ffn", "combine", "bias_update",
     "seq_balance_stat", "device_error", "route_workspace_bytes",
     "dispatch_workspace_bytes", "expert_ffn_workspace_bytes", "MoELayer",
@@ -57,6 +57,7 @@ _SIGS = {
     "moe_route": (ctypes.c_int, [_P, _P, ctypes.c_int, _P, Shape, _P, _I32, _P, _P, _P, _P, _P, _S, _P]),
     "moe_dispatch_workspace": (_S, [Shape]),
     "moe_dispatch": (ctypes.c_int, [_P, Shape, _P, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [_P, Shape, _P, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_quantize_e4m3": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I32, _P, _P, _P]),
     "moe_expert_ffn_workspace": (_S, [Shape, ctypes.c_int]),
     "moe_expert_gate_up": (ctypes.c_int, [_P, _P, _P, _P, _P, Shape, ctypes.POINTER(_Weights), _P, _P, _P]),
@@ -87,7 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 
 # Kernels each call enqueues for a non-empty batch (the launch count of a step).
-_KERNELS = {"moe_route": 2, "moe_dispatch": 3, "moe_quantize_e4m3": 1, "moe_expert_gate_up": 1,
+_KERNELS = {"moe_route": 2, "moe_dispatch": 3, "moe_dispatch_noalloc": 3, "moe_quantize_e4m3": 1, "moe_expert_gate_up": 1,
             "moe_expert_down": 1, "moe_expert_ffn": 2, "moe_combine": 1, "moe_bias_update": 1,
             "moe_seq_balance_stat": 1}
 _launches = 0
@@ -178,6 +179,17 @@ def dispatch(topk_idx, sh: Shape, load, expert_offset, perm_token, inv_row, u=No
           _ptr(u_scale), _ptr(load), _ptr(expert_offset), _ptr(perm_token), _ptr(inv_row),
           _ptr(x_perm), _ptr(x_perm_scale), _ptr(ws), ws.numel() if ws is not None else 0,
           _stream(stream), extra_kernels=1 if x_perm is not None else 0)
+
+
+def dispatch_noalloc(topk_idx, sh: Shape, load, expert_offset, perm_token, inv_row, u=None,
+                     x_perm=None, u_scale=None, x_perm_scale=None, stream=None):
+    """``dispatch`` for callers that cannot allocate device memory: the chunk counts
+    live in the library's built-in device array (T <= 65536 at 256 experts), which all
+    calls on a device share, so calls must not overlap on the GPU."""
+    _call("moe_dispatch_noalloc", _ptr(topk_idx), sh, _ptr(u), _dt(u) if u is not None else BF16,
+          _ptr(u_scale), _ptr(load), _ptr(expert_offset), _ptr(perm_token), _ptr(inv_row),
+          _ptr(x_perm), _ptr(x_perm_scale), _stream(stream),
+          extra_kernels=1 if x_perm is not None else 0)
 
 
 def quantize_e4m3(x, block_rows: int, q, scale, stream=None):

@@ -157,6 +157,22 @@ moe_status moe_dispatch(const int32_t* topk_idx, moe_shape sh, const void* u, mo
   return cuda_status(err);
 }
 
+// For callers that cannot allocate device memory: the same dispatch, with the chunk
+// counts kept in the library's built-in device array instead of a workspace.
+moe_status moe_dispatch_noalloc(const int32_t* topk_idx, moe_shape sh, const void* u,
+                                moe_dtype u_dt, const float* u_scale, int32_t* load,
+                                int32_t* expert_offset, int32_t* perm_token, int32_t* inv_row,
+                                void* x_perm, float* x_perm_scale, void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  const size_t cap = kDispatchStaticCounts * sizeof(int32_t);
+  if (moe_dispatch_workspace(sh) > cap) return MOE_ERR_INVALID_ARG;   // beyond the built-in size
+  int32_t* counts = nullptr;
+  if (dispatch_static_counts(&counts) != cudaSuccess) return MOE_ERR_CUDA;
+  return moe_dispatch(topk_idx, sh, u, u_dt, u_scale, load, expert_offset, perm_token, inv_row,
+                      x_perm, x_perm_scale, counts, cap, stream);
+}
+
 // ------------------------------------------------------------------------- quant ----
 
 moe_status moe_quantize_e4m3(const void* x, moe_dtype x_dt, int64_t rows, int64_t cols,

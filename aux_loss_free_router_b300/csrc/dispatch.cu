@@ -13,6 +13,8 @@
 //            number of lower lanes with the same expert.  Positions therefore grow
 //            with t inside every expert: the order is deterministic and stable.
 //   gather:  one warp per token reads its row once and writes it to its K_r rows.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -194,6 +196,40 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
         (uint8_t*)x_perm, x_perm_scale);
   }
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------ built-in chunk-count scratch ---
+//
+// moe_dispatch_noalloc runs the same kernels with their per-chunk expert counts in this
+// file-scope device array instead of a caller workspace.  It is sized for
+// kDispatchStaticCounts int32 entries (2 MiB): ceil(T/32) * N_r must not exceed it,
+// e.g. T <= 65536 tokens with 256 experts.  Every GPU that loads the library keeps it
+// until the process exits.
+static __device__ __align__(256) int32_t g_dispatch_counts[kDispatchStaticCounts];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_counts_mu;
+int32_t* g_counts_addr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of g_dispatch_counts on the current device.  In host code the array's
+// name only stands in for the symbol, so it is looked up with cudaGetSymbolAddress once
+// per device, with that device current, and cached.
+cudaError_t dispatch_static_counts(int32_t** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_counts_mu);
+  if (g_counts_addr[dev] == nullptr) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_dispatch_counts);
+    if (err != cudaSuccess) return err;
+    g_counts_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_counts_addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -14,6 +14,8 @@ struct RouteOut;
 
 constexpr int kSeqSlabs = 16;       // token slabs per sequence in the P-sum reduction
 constexpr int kDispatchChunk = 32;  // tokens per warp chunk in count / scatter
+// Capacity (int32 entries) of the dispatch's built-in chunk-count array.
+constexpr size_t kDispatchStaticCounts = (size_t)1 << 19;
 
 // Segments of the expert FFN row space: routed expert i owns rows
 // [expert_offset[i], expert_offset[i+1]); shared expert s owns T rows starting at
@@ -41,6 +43,10 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
                             int scale_cols, int32_t* load, int32_t* expert_offset,
                             int32_t* perm_token, int32_t* inv_row, void* x_perm,
                             float* x_perm_scale, int32_t* ws_counts, cudaStream_t st);
+
+// Device address of the built-in chunk-count array (kDispatchStaticCounts entries) on
+// the current device; looked up on the first call per device.
+cudaError_t dispatch_static_counts(int32_t** out);
 
 cudaError_t launch_quantize_e4m3(const void* x, moe_dtype x_dt, int64_t rows, int64_t cols,
                                  int block_rows, uint8_t* q, float* scale, cudaStream_t st);

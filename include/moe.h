@@ -147,6 +147,32 @@ MOE_API moe_status moe_dispatch(const int32_t* topk_idx, moe_shape sh, const voi
                         size_t ws_bytes, void* stream);
 
 /* --------------------------------------------------------------------------------
+ * Dispatch without any allocation.  The pages have no counterpart: this exists for
+ * callers that cannot call cudaMalloc or hand out device scratch, such as code running
+ * under an allocator that owns all device memory, or a host runtime whose buffers are
+ * fixed up front.  It computes exactly what moe_dispatch computes, with the same
+ * arguments minus the workspace.
+ *
+ *   Scratch: the per-chunk expert counts live in one device array built into the
+ *   library, 2 MiB per GPU (524288 int32), held by every GPU that loads the library
+ *   until the process exits.  ceil(T/32) * N_r must fit in it (T <= 65536 tokens with
+ *   N_r = 256); a larger batch returns MOE_ERR_INVALID_ARG and launches nothing.
+ *   Allocation: none; no cudaMalloc, cudaFree or allocating library routine.
+ *   First call per device: looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current and caches it; make that first call before any stream
+ *     capture.
+ *   Sharing: every call on a device uses the same array, which keeps the last call's
+ *     contents.  Each entry a call reads is written earlier in the same call, so
+ *     nothing has to be cleared, but calls that overlap on the GPU (different streams
+ *     without ordering between them) race on it: serialise them.
+ * Returns what moe_dispatch returns; MOE_ERR_CUDA if the address lookup fails. */
+MOE_API moe_status moe_dispatch_noalloc(const int32_t* topk_idx, moe_shape sh, const void* u,
+                                moe_dtype u_dt, const float* u_scale, int32_t* load,
+                                int32_t* expert_offset, int32_t* perm_token,
+                                int32_t* inv_row, void* x_perm, float* x_perm_scale,
+                                void* stream);
+
+/* --------------------------------------------------------------------------------
  * FP8 E4M3 quantisation with fp32 block scales ([P4] Key ideas: E4M3 on all
  * tensors, activations per 1x128 tile, weights per 128x128 block; [P3] §三).
  * x [rows, cols] (dtype x_dt: MOE_F32 or MOE_BF16) -> q [rows, cols] E4M3 codes and
