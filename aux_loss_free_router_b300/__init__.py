@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "MoEError", "Shape", "load_library", "route", "dispatch", "dispatch_noalloc", "quantize_e4m3",
     "expert_gate_up", "expert_down", "expert_ffn", "combine", "bias_update",
-    "seq_balance_stat", "device_error", "route_workspace_bytes",
+    "seq_balance_stat", "device_error", "quantize_weights", "route_workspace_bytes",
     "dispatch_workspace_bytes", "expert_ffn_workspace_bytes", "MoELayer",
     "LIB_PATH", "STATUS", "launch_counter", "launch_counter_reset", "make_shape",
 ]
@@ -252,6 +252,24 @@ def device_error(clear: bool = True) -> int:
     return code.value
 
 
+def quantize_weights(weights: dict, stream=None) -> dict:
+    """E4M3 codes and per-128x128-block fp32 scales of bf16/fp32 expert weights
+    (``w_gate``/``w_up`` [E, I, d], ``w_down`` [E, d, I] and the shared ``ws_*``), via
+    moe_quantize_e4m3; returns the dict the FFN calls take for E4M3 weights."""
+    out = {}
+    for k, w in weights.items():
+        if w is None:
+            continue
+        E, R, C = w.shape
+        q = torch.empty(E, R, C, dtype=torch.uint8, device=w.device)
+        sc = torch.empty(E, R // 128, C // 128, dtype=torch.float32, device=w.device)
+        if w.numel():
+            quantize_e4m3(w.reshape(E * R, C), 128, q, sc, stream=stream)
+        out[k] = q
+        out[k + "_scale"] = sc
+    return out
+
+
 # --------------------------------------------------------------- whole layer -----
 
 @dataclasses.dataclass
@@ -277,6 +295,8 @@ class MoELayer:
     want_s: bool = False
     out_dtype: Optional[torch.dtype] = torch.float32   # h' (fp32 keeps the layer output
     # within 2e-2 max-abs: a bf16 store alone errs by up to 0.0156 once |h'| >= 4)
+    fp8: bool = False   # expert GEMMs in E4M3: weights quantised here once (128x128
+    # blocks), tokens every step (1x128 tiles); routing stays on the bf16 tokens
 
     def __post_init__(self):
         dev, dt = self.e.device, self.e.dtype
@@ -291,9 +311,22 @@ class MoELayer:
         self.expert_offset = z(N_r + 1)
         self.perm_token = z(T * K_r)
         self.inv_row = z(T, K_r)
-        self.x_perm = z(T * K_r, self.d, dtype=dt)
         R = T * K_r + self.N_s * T
-        self.h_mid = z(R, self.I, dtype=dt)
+        if self.fp8:
+            if dt != torch.bfloat16:
+                raise ValueError("the FP8 layer takes bf16 tokens and weights")
+            u8 = torch.uint8
+            self.u_q = z(T, self.d, dtype=u8)
+            self.u_scale = z(T, self.d // 128, dtype=torch.float32)
+            self.x_perm = z(T * K_r, self.d, dtype=u8)
+            self.x_perm_scale = z(T * K_r, self.d // 128, dtype=torch.float32)
+            self.h_mid = z(R, self.I, dtype=u8)
+            self.h_scale = z(R, self.I // 128, dtype=torch.float32)
+            self.ffn_weights = quantize_weights(self.weights)
+        else:
+            self.x_perm = z(T * K_r, self.d, dtype=dt)
+            self.h_mid = z(R, self.I, dtype=dt)
+            self.ffn_weights = self.weights
         self.y = z(R, self.d, dtype=dt)
         self.out = z(T, self.d, dtype=self.out_dtype or dt)
         self.stat = z(self.n_seq, dtype=torch.float32)
@@ -312,13 +345,27 @@ class MoELayer:
         route(u, self.e, self.b, sh, self.topk_idx, self.topk_gate, self.s_out, seq_offsets,
               self.n_seq, self.seq_p_sum, self.ws_route, stream)
         ev(1)
-        dispatch(self.topk_idx, sh, self.load, self.expert_offset, self.perm_token, self.inv_row,
-                 u, self.x_perm, workspace=self.ws_dispatch, stream=stream)
-        ev(2)
-        expert_gate_up(self.x_perm, u, self.expert_offset, sh, self.weights, self.h_mid,
-                       stream=stream)
-        ev(3)
-        expert_down(self.h_mid, self.expert_offset, sh, self.weights, self.y, stream=stream)
+        if self.fp8:
+            quantize_e4m3(u, 1, self.u_q, self.u_scale, stream=stream)
+            dispatch(self.topk_idx, sh, self.load, self.expert_offset, self.perm_token,
+                     self.inv_row, self.u_q, self.x_perm, self.u_scale, self.x_perm_scale,
+                     workspace=self.ws_dispatch, stream=stream)
+            ev(2)
+            expert_gate_up(self.x_perm, self.u_q, self.expert_offset, sh, self.ffn_weights,
+                           self.h_mid, self.x_perm_scale, self.u_scale, self.h_scale,
+                           stream=stream)
+            ev(3)
+            expert_down(self.h_mid, self.expert_offset, sh, self.ffn_weights, self.y,
+                        self.h_scale, stream=stream)
+        else:
+            dispatch(self.topk_idx, sh, self.load, self.expert_offset, self.perm_token,
+                     self.inv_row, u, self.x_perm, workspace=self.ws_dispatch, stream=stream)
+            ev(2)
+            expert_gate_up(self.x_perm, u, self.expert_offset, sh, self.ffn_weights, self.h_mid,
+                           stream=stream)
+            ev(3)
+            expert_down(self.h_mid, self.expert_offset, sh, self.ffn_weights, self.y,
+                        stream=stream)
         ev(4)
         combine(u, self.y, self.topk_gate, self.inv_row, sh, self.out, stream=stream)
         if update_bias:

@@ -195,7 +195,14 @@ moe_status check_weights(const moe_shape& sh, const moe_expert_weights* w) {
   if (!ok_ptr(w->gate) || !ok_ptr(w->up) || !ok_ptr(w->down)) return MOE_ERR_INVALID_ARG;
   if (sh.N_s > 0 && (!ok_ptr(w->s_gate) || !ok_ptr(w->s_up) || !ok_ptr(w->s_down)))
     return MOE_ERR_INVALID_ARG;
-  if (w->dtype == MOE_E4M3) return MOE_ERR_UNSUPPORTED;
+  if (w->dtype == MOE_E4M3) {
+    if (sh.d % 128 != 0 || sh.I % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (!ok_ptr(w->gate_scale) || !ok_ptr(w->up_scale) || !ok_ptr(w->down_scale))
+      return MOE_ERR_INVALID_ARG;
+    if (sh.N_s > 0 && (!ok_ptr(w->s_gate_scale) || !ok_ptr(w->s_up_scale) || !ok_ptr(w->s_down_scale)))
+      return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+  }
   if (!is_float_dtype(w->dtype)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -207,10 +214,16 @@ size_t h_bytes(const moe_shape& sh, moe_dtype dt) {
   return rows * sh.I * elem_bytes(dt);
 }
 
+size_t h_scale_bytes(const moe_shape& sh) {
+  const size_t rows = (size_t)sh.T * sh.K_r + (size_t)sh.N_s * sh.T;
+  return rows * (size_t)(sh.I / 128) * sizeof(float);
+}
+
 }  // namespace
 
 size_t moe_expert_ffn_workspace(moe_shape sh, moe_dtype w_dt) {
   if (sh.T <= 0) return 0;
+  if (w_dt == MOE_E4M3) return align256(h_bytes(sh, w_dt)) + align256(h_scale_bytes(sh));
   return align256(h_bytes(sh, w_dt));
 }
 
@@ -218,7 +231,6 @@ moe_status moe_expert_gate_up(const void* x_perm, const float* x_perm_scale, con
                               const float* u_scale, const int32_t* expert_offset, moe_shape sh,
                               const moe_expert_weights* w, void* h, float* h_scale,
                               void* stream) {
-  (void)x_perm_scale; (void)u_scale; (void)h_scale;
   moe_status st = check_shape(sh);
   if (st != MOE_OK) return st;
   if ((st = check_weights(sh, w)) != MOE_OK) return st;
@@ -227,7 +239,12 @@ moe_status moe_expert_gate_up(const void* x_perm, const float* x_perm_scale, con
     return MOE_ERR_INVALID_ARG;
   const FfnShape fs = ffn_shape(sh);
   cudaError_t err;
-  if (w->dtype == MOE_F32)
+  if (w->dtype == MOE_E4M3) {
+    if (!ok_ptr(x_perm_scale) || !ok_ptr(h_scale) || (sh.N_s > 0 && !ok_ptr(u_scale)))
+      return MOE_ERR_INVALID_ARG;
+    err = launch_ffn_up_fp8(fs, x_perm, x_perm_scale, u, u_scale, expert_offset, w, h, h_scale,
+                            S(stream));
+  } else if (w->dtype == MOE_F32)
     err = launch_ffn_up_simt(fs, (const float*)x_perm, (const float*)u, expert_offset, w,
                              (float*)h, S(stream));
   else
@@ -237,7 +254,6 @@ moe_status moe_expert_gate_up(const void* x_perm, const float* x_perm_scale, con
 
 moe_status moe_expert_down(const void* h, const float* h_scale, const int32_t* expert_offset,
                            moe_shape sh, const moe_expert_weights* w, void* y, void* stream) {
-  (void)h_scale;
   moe_status st = check_shape(sh);
   if (st != MOE_OK) return st;
   if ((st = check_weights(sh, w)) != MOE_OK) return st;
@@ -245,7 +261,10 @@ moe_status moe_expert_down(const void* h, const float* h_scale, const int32_t* e
   if (!ok_ptr(h) || !ok_ptr(expert_offset) || !ok_ptr(y)) return MOE_ERR_INVALID_ARG;
   const FfnShape fs = ffn_shape(sh);
   cudaError_t err;
-  if (w->dtype == MOE_F32)
+  if (w->dtype == MOE_E4M3) {
+    if (!ok_ptr(h_scale)) return MOE_ERR_INVALID_ARG;
+    err = launch_ffn_down_fp8(fs, h, h_scale, expert_offset, w, y, S(stream));
+  } else if (w->dtype == MOE_F32)
     err = launch_ffn_down_simt(fs, (const float*)h, expert_offset, w, (float*)y, S(stream));
   else
     err = launch_ffn_down_tc(fs, h, expert_offset, w, y, S(stream));
@@ -262,10 +281,13 @@ moe_status moe_expert_ffn(const void* x_perm, const float* x_perm_scale, const v
   if (sh.T == 0) return MOE_OK;
   const size_t need = moe_expert_ffn_workspace(sh, w->dtype);
   if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  float* h_scale = nullptr;
+  if (w->dtype == MOE_E4M3)
+    h_scale = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(h_bytes(sh, w->dtype)));
   st = moe_expert_gate_up(x_perm, x_perm_scale, u, u_scale, expert_offset, sh, w, workspace,
-                          nullptr, stream);
+                          h_scale, stream);
   if (st != MOE_OK) return st;
-  return moe_expert_down(workspace, nullptr, expert_offset, sh, w, y, stream);
+  return moe_expert_down(workspace, h_scale, expert_offset, sh, w, y, stream);
 }
 
 // ---------------------------------------------------------------------- combine ----

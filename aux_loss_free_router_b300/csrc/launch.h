@@ -65,6 +65,14 @@ cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h,
                                const int32_t* expert_offset, const moe_expert_weights* w,
                                void* y, cudaStream_t st);
 
+cudaError_t launch_ffn_up_fp8(const FfnShape& s, const void* x_perm, const float* x_perm_scale,
+                              const void* u, const float* u_scale, const int32_t* expert_offset,
+                              const moe_expert_weights* w, void* h, float* h_scale,
+                              cudaStream_t st);
+cudaError_t launch_ffn_down_fp8(const FfnShape& s, const void* h, const float* h_scale,
+                                const int32_t* expert_offset, const moe_expert_weights* w,
+                                void* y, cudaStream_t st);
+
 cudaError_t launch_combine(const void* u, const void* y, moe_dtype dt, const float* gate,
                            const int32_t* inv_row, int T, int d, int K_r, int N_s,
                            void* out, moe_dtype out_dt, cudaStream_t st);

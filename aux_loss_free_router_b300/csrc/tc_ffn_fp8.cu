@@ -1,0 +1,401 @@
+// Grouped SwiGLU expert GEMMs in FP8 (E4M3) on the sm_103a tensor cores, with fp32
+// block scales: tokens and the SwiGLU output per 1x128 tile, weights per 128x128
+// block (DeepSeek-V3 Technical Report reading guide, Key ideas, FP8 bullet;
+// pwwt.cn notes §三).
+//
+// The scales change every 128 elements of K, so each 128-wide K chunk is multiplied
+// on the tensor cores on its own (four kind::f8f6f4 MMAs of K=32 into a TMEM
+// buffer) and the epilogue warps promote it into fp32 registers with that chunk's
+// scales: acc += P * (scale_x[row, chunk] * scale_w[block, chunk]).  Two TMEM
+// buffers alternate, so the MMAs of chunk c+1 run while chunk c is promoted: the
+// tensor-core form of the pages' promotion to CUDA cores every 128 elements.
+//
+// One persistent CTA per SM walks the segment schedule (ffn_sched.cuh).  Warp roles:
+//   warp 0      TMA producer: A [128 rows x 128 B] and B [256 rows x 128 B] per
+//               stage, 128-byte swizzled, 4-stage ring.
+//   warp 1      allocates 512 TMEM columns, issues the MMAs (one thread).
+//   warps 2..9  epilogue: two warps per TMEM lane quarter, each holding 128 fp32
+//               accumulators of its row (one half of the tile's columns).
+//
+// gate/up (MODE 0): B = 128 rows of W_gate over the same 128 rows of W_up; the
+//   epilogue forms h = silu(gate) * up for 128 columns of a row, quantises that 1x128
+//   tile to E4M3 (the two halves exchange their amax through shared memory) and
+//   writes the codes and the scale.
+// down (MODE 1): B = 256 rows of W_down (two 128-row scale blocks); y is bf16.
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "ffn_sched.cuh"
+#include "launch.h"
+#include "tc_ptx.cuh"
+#include "tmap.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BK = 128, BN = 256, STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + EPI_WARPS * 32;
+
+struct Ctrl {
+  uint64_t full[STAGES], empty[STAGES], pfull[2], pempty[2], xbar[2], fin;
+  uint32_t tmem_base;
+  int abort_flag;
+  float amax[2][2][BM];   // [tile parity][column half][row]
+  SegTable tab;
+};
+
+constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
+
+struct Fp8Args {
+  FfnShape s;
+  const int32_t* expert_offset;
+  const float* a_scale_r;    // scales of the routed A rows (x_perm / h), [rows, K/128]
+  const float* a_scale_s;    // MODE 0: scales of u for the shared experts, [T, d/128]
+  const float* b0_scale_r;   // gate (MODE 0) or down (MODE 1) block scales, routed
+  const float* b1_scale_r;   // up block scales, routed (MODE 0)
+  const float* b0_scale_s;   // the same for the shared experts
+  const float* b1_scale_s;
+  void* out;                 // MODE 0: h codes [R, I]; MODE 1: y bf16 [R, d]
+  float* out_scale;          // MODE 0: h scales [R, I/128]
+  int32_t* err;
+};
+
+__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+
+__device__ __forceinline__ uint32_t e4m3_code(float x, float scale) {
+  return (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_ffn_fp8_kernel(const __grid_constant__ CUtensorMap mA_r,
+                      const __grid_constant__ CUtensorMap mA_s,
+                      const __grid_constant__ CUtensorMap mB0_r,
+                      const __grid_constant__ CUtensorMap mB1_r,
+                      const __grid_constant__ CUtensorMap mB0_s,
+                      const __grid_constant__ CUtensorMap mB1_s, Fp8Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_off = tc::smem_u32(smem_raw);
+  uint8_t* base = smem_raw + ((1024u - (raw_off & 1023u)) & 1023u);
+  Ctrl& C = *reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
+
+  const FfnShape s = args.s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = MODE == 0 ? s.d : s.I;
+  const int N = MODE == 0 ? s.I : s.d;
+  constexpr int BNO = MODE == 0 ? BN / 2 : BN;   // output columns per tile
+  const int n_tiles_n = (N + BNO - 1) / BNO;
+  const int nk = K / BK;                          // K is a multiple of 128
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      tc::mbar_init(&C.full[i], 1);
+      tc::mbar_init(&C.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&C.pfull[i], 1);
+      tc::mbar_init(&C.pempty[i], EPI_WARPS * 32);
+      tc::mbar_init(&C.xbar[i], EPI_WARPS * 32);
+    }
+    tc::mbar_init(&C.fin, 1);
+    C.abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&mA_r);
+    tc::tma_prefetch_desc(&mB0_r);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&C.tmem_base, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BM, n_tiles_n);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = C.tmem_base;
+  const int total = C.tab.total;
+  volatile int* abort_flag = &C.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer --
+      int it = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const TileCoord tcd = decode_tile(C.tab, tile, n_tiles_n);
+        const bool shared = tcd.seg >= s.N_r;
+        const int e = shared ? tcd.seg - s.N_r : tcd.seg;
+        const CUtensorMap* mA = (MODE == 0 && shared) ? &mA_s : &mA_r;
+        const int a_row = (MODE == 0 ? (shared ? 0 : tcd.row0) : tcd.out_row0) + tcd.m * BM;
+        const CUtensorMap* mB0 = shared ? &mB0_s : &mB0_r;
+        const CUtensorMap* mB1 = shared ? &mB1_s : &mB1_r;
+        const int b_row = e * N + tcd.n * BNO;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int st = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!tc::mbar_wait(&C.empty[st], ph ^ 1, abort_flag, args.err)) { ok = false; break; }
+          uint8_t* sa = base + st * STAGE_BYTES;
+          uint8_t* sb = sa + A_BYTES;
+          tc::mbar_arrive_expect_tx(&C.full[st], STAGE_BYTES);
+          tc::tma_load_2d(sa, mA, &C.full[st], kb * BK, a_row);
+          if (MODE == 0) {
+            tc::tma_load_2d(sb, mB0, &C.full[st], kb * BK, b_row);
+            tc::tma_load_2d(sb + B_BYTES / 2, mB1, &C.full[st], kb * BK, b_row);
+          } else {
+            tc::tma_load_2d(sb, mB0, &C.full[st], kb * BK, b_row);
+          }
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          tc::mbar_drain(&C.full[j % STAGES], (j / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer --
+      constexpr uint32_t idesc = tc::idesc_e4m3(BM, BN);
+      int it = 0, c = 0;   // stage counter, K-chunk counter (TMEM buffer = c & 1)
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total && !*abort_flag; tile += gridDim.x) {
+        for (int kb = 0; kb < nk; ++kb, ++it, ++c) {
+          const int buf = c & 1;
+          if (!tc::mbar_wait(&C.pempty[buf], ((c >> 1) & 1) ^ 1, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          const int st = it % STAGES;
+          if (!tc::mbar_wait(&C.full[st], (it / STAGES) & 1, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t a0 = tc::smem_u32(base + st * STAGE_BYTES);
+          const uint64_t ad = tc::sdesc_sw128(a0), bd = tc::sdesc_sw128(a0 + A_BYTES);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk)
+            tc::mma_e4m3(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, kk != 0);
+          tc::mma_commit(&C.empty[st]);
+          tc::mma_commit(&C.pfull[buf]);
+        }
+      }
+      tc::mma_commit(&C.fin);
+      tc::mbar_drain(&C.fin, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    const int q = warp & 3;              // TMEM lane quarter this warp can access
+    const int hh = (warp - 2) >> 2;      // column half of the tile
+    const int row_in_tile = q * 32 + lane;
+    const int nkc_out = N / 128;         // scale columns of the output (MODE 0)
+    int c = 0, tcount = 0;
+    bool alive = true;
+    for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x, ++tcount) {
+      const TileCoord tcd = decode_tile(C.tab, tile, n_tiles_n);
+      const bool shared = tcd.seg >= s.N_r;
+      const int e = shared ? tcd.seg - s.N_r : tcd.seg;
+      const int row_local = tcd.m * BM + row_in_tile;
+      const bool row_ok = row_local < tcd.rows;
+      // A-row scales: routed rows of x_perm / h, or the token rows of u (shared, MODE 0)
+      const float* a_sc;
+      size_t a_row;
+      if (MODE == 0 && shared) {
+        a_sc = args.a_scale_s;
+        a_row = (size_t)row_local;
+      } else {
+        a_sc = args.a_scale_r;
+        a_row = (size_t)(MODE == 0 ? tcd.row0 : tcd.out_row0) + row_local;
+      }
+      a_sc += a_row * nk;
+      // weight block scales for this tile's columns
+      const float* b0 = (shared ? args.b0_scale_s : args.b0_scale_r);
+      const float* b1 = (shared ? args.b1_scale_s : args.b1_scale_r);
+      const int nblk = N / 128;            // 128-row blocks per expert along N
+      int blk0;                            // block row of this thread's columns
+      bool blk_ok = true;
+      if (MODE == 0) {
+        blk0 = tcd.n;
+      } else {
+        blk0 = tcd.n * 2 + hh;
+        blk_ok = blk0 < nblk;
+      }
+      const float* b0row = b0 + ((size_t)e * nblk + (blk_ok ? blk0 : 0)) * nk;
+      const float* b1row = MODE == 0 ? b1 + ((size_t)e * nblk + blk0) * nk : nullptr;
+
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+
+      for (int kb = 0; kb < nk; ++kb, ++c) {
+        const float sa = row_ok ? __ldg(a_sc + kb) : 0.f;
+        const float sb0 = blk_ok ? __ldg(b0row + kb) : 0.f;
+        const float sb1 = MODE == 0 ? __ldg(b1row + kb) : 0.f;
+        const int buf = c & 1;
+        const bool got = tc::mbar_wait(&C.pfull[buf], (c >> 1) & 1, abort_flag, args.err);
+        if (!__all_sync(0xffffffffu, got)) { alive = false; break; }
+        tc::fence_after_sync();
+        const uint32_t t_base = tmem_base + (uint32_t)(buf * BN) + ((uint32_t)(q * 32) << 16);
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+          int col;
+          float sc;
+          if (MODE == 0) {
+            col = (part < 2 ? 0 : BN / 2) + hh * 64 + (part & 1) * 32;
+            sc = sa * (part < 2 ? sb0 : sb1);
+          } else {
+            col = hh * 128 + part * 32;
+            sc = sa * sb0;
+          }
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t p[16];
+            tc::tmem_ld16(t_base + col + half * 16, p);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int a = part * 32 + half * 16 + j;
+              acc[a] = fmaf(__uint_as_float(p[j]), sc, acc[a]);
+            }
+          }
+        }
+        tc::fence_before_sync();
+        tc::mbar_arrive(&C.pempty[buf]);
+      }
+      if (!alive) break;
+
+      const size_t out_row = (size_t)tcd.out_row0 + row_local;
+      if (MODE == 0) {
+        // h for this thread's 64 columns, then the 1x128 tile scale from both halves
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          acc[j] = silu(acc[j]) * acc[64 + j];
+          amax = fmaxf(amax, fabsf(acc[j]));
+        }
+        const int tb = tcount & 1;
+        C.amax[tb][hh][row_in_tile] = amax;
+        tc::mbar_arrive(&C.xbar[tb]);   // release: the amax store is visible after the wait
+        const bool xg = tc::mbar_wait(&C.xbar[tb], (tcount >> 1) & 1, abort_flag, args.err);
+        if (!__all_sync(0xffffffffu, xg)) break;
+        const float tile_amax = fmaxf(amax, C.amax[tb][hh ^ 1][row_in_tile]);
+        const float scale = tile_amax > 0.f ? __fdiv_rn(tile_amax, 448.f) : 1.f;
+        if (row_ok) {
+          uint8_t* hq = static_cast<uint8_t*>(args.out) + out_row * N + tcd.n * 128 + hh * 64;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const int j = v * 16 + x * 4;
+              w[x] = e4m3_code(acc[j], scale) | (e4m3_code(acc[j + 1], scale) << 8) |
+                     (e4m3_code(acc[j + 2], scale) << 16) | (e4m3_code(acc[j + 3], scale) << 24);
+            }
+            reinterpret_cast<uint4*>(hq)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          if (hh == 0) args.out_scale[out_row * nkc_out + tcd.n] = scale;
+        }
+      } else {
+        const int col0 = tcd.n * BN + hh * 128;
+        if (row_ok && col0 < N) {
+          __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(args.out) + out_row * N + col0;
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            reinterpret_cast<uint4*>(yrow)[v] =
+                make_uint4(pack_bf16(acc[8 * v + 0], acc[8 * v + 1]), pack_bf16(acc[8 * v + 2], acc[8 * v + 3]),
+                           pack_bf16(acc[8 * v + 4], acc[8 * v + 5]), pack_bf16(acc[8 * v + 6], acc[8 * v + 7]));
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int MODE>
+cudaError_t launch(const FfnShape& s, const CUtensorMap* maps, const Fp8Args& a, cudaStream_t st) {
+  const int N = MODE == 0 ? s.I : s.d;
+  const int bno = MODE == 0 ? BN / 2 : BN;
+  const long long m_ub = (long long)s.T * s.K_r / BM + s.N_r + (long long)s.N_s * ((s.T + BM - 1) / BM);
+  const long long tiles_ub = m_ub * ((N + bno - 1) / bno);
+  const int grid = (int)std::min<long long>(device_sm_count(), std::max<long long>(1, tiles_ub));
+  auto k = tc_ffn_fp8_kernel<MODE>;
+  cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  k<<<grid, THREADS, kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+  return cudaGetLastError();
+}
+
+constexpr CUtensorMapDataType kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+
+}  // namespace
+
+cudaError_t launch_ffn_up_fp8(const FfnShape& s, const void* x_perm, const float* x_perm_scale,
+                              const void* u, const float* u_scale, const int32_t* expert_offset,
+                              const moe_expert_weights* w, void* h, float* h_scale,
+                              cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  CUtensorMap m[6];
+  const uint64_t rb = (uint64_t)s.d;
+  const uint64_t routed = (uint64_t)s.T * s.K_r;
+  bool ok = make_tmap_2d(&m[0], kU8, x_perm, s.d, routed, rb, BK, BM) &&
+            make_tmap_2d(&m[1], kU8, u, s.d, s.T, rb, BK, BM) &&
+            make_tmap_2d(&m[2], kU8, w->gate, s.d, (uint64_t)s.N_r * s.I, rb, BK, BN / 2) &&
+            make_tmap_2d(&m[3], kU8, w->up, s.d, (uint64_t)s.N_r * s.I, rb, BK, BN / 2);
+  if (ok && s.N_s > 0) {
+    ok = make_tmap_2d(&m[4], kU8, w->s_gate, s.d, (uint64_t)s.N_s * s.I, rb, BK, BN / 2) &&
+         make_tmap_2d(&m[5], kU8, w->s_up, s.d, (uint64_t)s.N_s * s.I, rb, BK, BN / 2);
+  } else {
+    m[4] = m[2];
+    m[5] = m[3];
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  Fp8Args a{s, expert_offset, x_perm_scale, u_scale, w->gate_scale, w->up_scale,
+            s.N_s > 0 ? w->s_gate_scale : w->gate_scale, s.N_s > 0 ? w->s_up_scale : w->up_scale,
+            h, h_scale, dev_error_ptr()};
+  return launch<0>(s, m, a, st);
+}
+
+cudaError_t launch_ffn_down_fp8(const FfnShape& s, const void* h, const float* h_scale,
+                                const int32_t* expert_offset, const moe_expert_weights* w,
+                                void* y, cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  CUtensorMap m[6];
+  const uint64_t rb = (uint64_t)s.I;
+  const uint64_t rows = (uint64_t)s.T * s.K_r + (uint64_t)s.N_s * s.T;
+  bool ok = make_tmap_2d(&m[0], kU8, h, s.I, rows, rb, BK, BM) &&
+            make_tmap_2d(&m[2], kU8, w->down, s.I, (uint64_t)s.N_r * s.d, rb, BK, BN);
+  if (ok && s.N_s > 0)
+    ok = make_tmap_2d(&m[4], kU8, w->s_down, s.I, (uint64_t)s.N_s * s.d, rb, BK, BN);
+  else
+    m[4] = m[2];
+  if (!ok) return cudaErrorInvalidValue;
+  m[1] = m[0];
+  m[3] = m[2];
+  m[5] = m[4];
+  Fp8Args a{s, expert_offset, h_scale, nullptr, w->down_scale, nullptr,
+            s.N_s > 0 ? w->s_down_scale : w->down_scale, nullptr, y, nullptr, dev_error_ptr()};
+  return launch<1>(s, m, a, st);
+}
+
+}  // namespace moe

@@ -29,7 +29,8 @@ def run_layer(cfg: synth.MoEConfig, inputs: dict | None = None, device="cuda"):
     b0 = x["b"].clone()
     layer = moe.MoELayer(T=cfg.T, d=cfg.d, N_r=cfg.N_r, K_r=cfg.K_r, N_s=cfg.N_s, I=cfg.I,
                          G=cfg.G, M=cfg.M, e=x["e"], b=x["b"].clone(), weights=w,
-                         n_seq=cfg.n_seq, gamma=cfg.gamma, alpha=cfg.alpha, want_s=True)
+                         n_seq=cfg.n_seq, gamma=cfg.gamma, alpha=cfg.alpha, want_s=True,
+                         fp8=cfg.fp8)
     out = layer.step(x["u"], x["seq_offsets"])
     torch.cuda.synchronize()
     assert moe.device_error() == 0
@@ -90,7 +91,7 @@ def check_output_full(cfg, r, rel_tol, abs_tol=None, abs_per_rms=False):
     scale, as the Gaussian-mixture tokens are)."""
     x = r["inputs"]
     ref = oracle.moe_forward(to_np(x["u"]), to_np(x["e"]), to_np(r["b0"]), oracle_weights(x),
-                             cfg.K_r, cfg.G, cfg.M, cfg.N_s, s=r["s_out"])
+                             cfg.K_r, cfg.G, cfg.M, cfg.N_s, s=r["s_out"], fp8=cfg.fp8)
     err = rel_l2(r["h"], ref["h"])
     assert err <= rel_tol, f"rel L2 {err}"
     if abs_tol is not None:
