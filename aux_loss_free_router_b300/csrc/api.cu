@@ -59,18 +59,15 @@ namespace {
 bool router_uses_tc(const moe_shape& sh, moe_dtype dt) { return dt == MOE_BF16 && sh.N_r % 32 == 0; }
 
 struct RouteWs {
-  size_t z_bytes, sprime_bytes, partial_bytes;
-  size_t total() const { return z_bytes + sprime_bytes + partial_bytes; }
+  size_t z_bytes, pwin_bytes;
+  size_t total() const { return z_bytes + pwin_bytes; }
 };
 
 RouteWs route_ws(const moe_shape& sh, int n_seq, int S) {
-  RouteWs w{0, 0, 0};
+  RouteWs w{0, 0};
   if (sh.T <= 0) return w;
   w.z_bytes = align256((size_t)S * sh.T * sh.N_r * sizeof(float));
-  if (n_seq > 0) {
-    w.sprime_bytes = align256((size_t)sh.T * sh.N_r * sizeof(float));
-    w.partial_bytes = align256((size_t)n_seq * kSeqSlabs * sh.N_r * sizeof(double));
-  }
+  if (n_seq > 0) w.pwin_bytes = align256((size_t)sh.T * sh.N_r * sizeof(float));
   return w;
 }
 
@@ -104,14 +101,14 @@ moe_status moe_route(const void* u, const void* e, moe_dtype dt, const float* b,
   if (workspace == nullptr || !aligned16(workspace) || ws_bytes < w.total()) return MOE_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   float* z_part = reinterpret_cast<float*>(ws);
-  float* sprime = want_stat ? reinterpret_cast<float*>(ws + w.z_bytes) : nullptr;
-  double* partial = want_stat ? reinterpret_cast<double*>(ws + w.z_bytes + w.sprime_bytes) : nullptr;
-  RouteOut p{sh.T, sh.N_r, sh.K_r, sh.G, sh.M, topk_idx, topk_gate, s_out, sprime};
+  float* pwin = want_stat ? reinterpret_cast<float*>(ws + w.z_bytes) : nullptr;
+  RouteOut p{sh.T, sh.N_r, sh.K_r, sh.G, sh.M, topk_idx, topk_gate, s_out, pwin,
+             seq_offsets, want_stat ? n_seq : 0};
   cudaError_t err = tc ? launch_router_gemm_tc(u, e, sh.T, sh.d, sh.N_r, z_part, S(stream))
                        : launch_router_gemm_simt(u, e, dt, sh.T, sh.d, sh.N_r, z_part, S(stream));
   if (err == cudaSuccess) err = launch_router_select(z_part, splits, b, p, S(stream));
   if (err == cudaSuccess && want_stat)
-    err = launch_seq_psum(sprime, seq_offsets, n_seq, sh.N_r, partial, seq_p_sum, S(stream));
+    err = launch_seq_psum(pwin, seq_offsets, n_seq, sh.N_r, seq_p_sum, S(stream));
   return cuda_status(err);
 }
 

@@ -12,7 +12,6 @@ namespace moe {
 
 struct RouteOut;
 
-constexpr int kSeqSlabs = 16;       // token slabs per sequence in the P-sum reduction
 constexpr int kDispatchChunk = 32;  // tokens per warp chunk in count / scatter
 // Capacity (int32 entries) of the dispatch's built-in chunk-count array.
 constexpr size_t kDispatchStaticCounts = (size_t)1 << 19;
@@ -35,8 +34,8 @@ cudaError_t launch_router_gemm_simt(const void* u, const void* e, moe_dtype dt, 
                                     int N_r, float* z, cudaStream_t st);
 cudaError_t launch_router_select(const float* z_part, int S, const float* b, const RouteOut& p,
                                  cudaStream_t st);
-cudaError_t launch_seq_psum(const float* sprime, const int32_t* seq_offsets, int n_seq,
-                            int N_r, double* partial, float* out, cudaStream_t st);
+cudaError_t launch_seq_psum(const float* pwin, const int32_t* seq_offsets, int n_seq, int N_r,
+                            float* out, cudaStream_t st);
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
                             const void* u, size_t row_bytes, const float* u_scale,

@@ -18,13 +18,50 @@ namespace moe {
 constexpr int kMaxExperts = 256;
 constexpr int kMaxSlots = kMaxExperts / 32;
 
+// Tokens per P-sum window: the selection kernels sum s_{i,t} / sum_j s_{j,t} over the
+// tokens of each window that belong to one sequence.
+constexpr int kPWindow = 32;
+
 struct RouteOut {
   int T, N_r, K_r, G, M;
   int32_t* topk_idx;   // [T, K_r]
   float* topk_gate;    // [T, K_r]
   float* s_out;        // [T, N_r] or null
-  float* sprime;       // [T, N_r] or null: s_{i,t} / sum_j s_{j,t}
+  // [T, N_r] or null.  For every run of tokens [t, t') that lies in one kPWindow-token
+  // window and one sequence, row t receives sum_{t <= x < t'} s_{i,x} / sum_j s_{j,x};
+  // other rows are not written.
+  float* pwin;
+  const int32_t* seq_offsets;   // [n_seq + 1], used when pwin is set
+  int n_seq;
 };
+
+// Index of the sequence holding token t: the largest j with seq_offsets[j] <= t.
+__device__ __forceinline__ int seq_of(int t, const int32_t* __restrict__ off, int n_seq) {
+  int lo = 0, hi = n_seq;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(off + mid) <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Window sums of one expert column: v(r) gives s'_{i, t0+r} for the window's ntok
+// tokens, seqid[r] their sequences; each run of one sequence is written to the row of
+// its first token.
+template <typename F>
+__device__ __forceinline__ void window_runs(F v, const int* seqid, int ntok, int t0, int N_r,
+                                            int i, float* __restrict__ pwin) {
+  float acc = 0.f;
+  int start = 0;
+  for (int r = 0; r < ntok; ++r) {
+    acc = __fadd_rn(acc, v(r));
+    if (r == ntok - 1 || seqid[r + 1] != seqid[r]) {
+      pwin[(size_t)(t0 + start) * N_r + i] = acc;
+      acc = 0.f;
+      start = r + 1;
+    }
+  }
+}
 
 // s_row: the token's N_r fp32 affinities (shared memory); b_sm: biases (shared).
 // All 32 lanes of the warp must call it with the same token.
@@ -39,25 +76,6 @@ __device__ __forceinline__ void route_token(const float* s_row, const float* b_s
     const bool ok = i < N_r;
     sv[j] = ok ? s_row[i] : 0.f;
     key[j] = ok ? __fadd_rn(sv[j], b_sm[i]) : -CUDART_INF_F;   // one fp32 rounding
-  }
-  const size_t rowbase = (size_t)t * N_r;
-  if (p.s_out) {
-#pragma unroll
-    for (int j = 0; j < kMaxSlots; ++j) {
-      const int i = j * 32 + lane;
-      if (i < N_r) p.s_out[rowbase + i] = sv[j];
-    }
-  }
-  if (p.sprime) {
-    float part = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxSlots; ++j) part = __fadd_rn(part, sv[j]);
-    const float rs = warp_sum(part);   // butterfly: every lane holds the same sum
-#pragma unroll
-    for (int j = 0; j < kMaxSlots; ++j) {
-      const int i = j * 32 + lane;
-      if (i < N_r) p.sprime[rowbase + i] = __fdiv_rn(sv[j], rs);
-    }
   }
 
   if (p.G > 1) {

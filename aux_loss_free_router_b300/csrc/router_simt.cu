@@ -59,22 +59,26 @@ __global__ void __launch_bounds__(256) router_gemm_simt_kernel(const TIn* __rest
   }
 }
 
-// The routing decision for 32 tokens per block (one warp): z = the fixed-order fp32 sum
-// of the S split-K partials, s = sigmoid(z) into shared memory, then either one thread
-// per token (select_row, the common shapes) or one warp per token (route_token), and
-// coalesced writes of s and s / sum(s).
+// The routing decision for 32 tokens per block (one warp), for the shapes the
+// warp-per-token kernel below does not take: z = the fixed-order fp32 sum of the S
+// split-K partials, s = sigmoid(z) into shared memory, then either one thread per
+// token (select_row) or one warp per token (route_token); s is written out when asked
+// for, and the block's P-sum window runs.
 __global__ void __launch_bounds__(32) router_select_kernel(const float* __restrict__ z_part,
                                                            int S, const float* __restrict__ b,
                                                            RouteOut p, int fast) {
+  static_assert(kTok == kPWindow, "one block covers one P-sum window");
   __shared__ float s_tile[kTok * (kMaxExperts + 1)];
   __shared__ float b_sm[kMaxExperts];
   __shared__ float rs_sm[kTok];
+  __shared__ int seqid[kTok];
   const int lane = threadIdx.x, N_r = p.N_r, T = p.T, stride = N_r + 1;
   const int t0 = blockIdx.x * kTok;
+  const int ntok = min(kTok, T - t0);
   for (int i = lane; i < N_r; i += 32) b_sm[i] = b[i];
-  for (int r = 0; r < kTok; ++r) {
+  if (p.pwin && lane < ntok) seqid[lane] = seq_of(t0 + lane, p.seq_offsets, p.n_seq);
+  for (int r = 0; r < ntok; ++r) {
     const int t = t0 + r;
-    if (t >= T) break;
     for (int i = lane; i < N_r; i += 32) {
       float z = z_part[(size_t)t * N_r + i];
       for (int sp = 1; sp < S; ++sp) z = __fadd_rn(z, z_part[((size_t)sp * T + t) * N_r + i]);
@@ -83,84 +87,246 @@ __global__ void __launch_bounds__(32) router_select_kernel(const float* __restri
   }
   __syncwarp();
   if (!fast) {
-    for (int r = 0; r < kTok; ++r) {
-      const int t = t0 + r;
-      if (t < T) route_token(s_tile + r * stride, b_sm, t, p);
+    for (int r = 0; r < ntok; ++r) {
+      route_token(s_tile + r * stride, b_sm, t0 + r, p);
+      if (p.pwin) {
+        float part = 0.f;
+        for (int i = lane; i < N_r; i += 32) part = __fadd_rn(part, s_tile[r * stride + i]);
+        const float rs = warp_sum(part);
+        if (lane == 0) rs_sm[r] = rs;
+      }
     }
-    return;
-  }
-  const int t = t0 + lane;
-  float rowsum = 0.f;
-  if (t < T) {
-    const float* row = s_tile + lane * stride;
-    float c1[kMaxSlots], c2[kMaxSlots];
+  } else {
+    const int t = t0 + lane;
+    float rowsum = 0.f;
+    if (t < T) {
+      const float* row = s_tile + lane * stride;
+      float c1[kMaxSlots], c2[kMaxSlots];
 #pragma unroll
-    for (int c = 0; c < kMaxSlots; ++c) {
-      c1[c] = c2[c] = -CUDART_INF_F;
-      if (c < N_r / 32) {
+      for (int c = 0; c < kMaxSlots; ++c) {
+        c1[c] = c2[c] = -CUDART_INF_F;
+        if (c < N_r / 32) {
 #pragma unroll 8
-        for (int j = 0; j < 32; ++j) {
-          const int i = c * 32 + j;
-          const float sv = row[i];
-          rowsum = __fadd_rn(rowsum, sv);
-          const float k = __fadd_rn(sv, b_sm[i]);
-          c2[c] = fmaxf(c2[c], fminf(c1[c], k));
-          c1[c] = fmaxf(c1[c], k);
+          for (int j = 0; j < 32; ++j) {
+            const int i = c * 32 + j;
+            const float sv = row[i];
+            rowsum = __fadd_rn(rowsum, sv);
+            const float k = __fadd_rn(sv, b_sm[i]);
+            c2[c] = fmaxf(c2[c], fminf(c1[c], k));
+            c1[c] = fmaxf(c1[c], k);
+          }
+        }
+      }
+      select_row(row, b_sm, c1, c2, t, p);
+    }
+    rs_sm[lane] = rowsum;
+  }
+  __syncwarp();
+  if (p.s_out) {
+    for (int r = 0; r < ntok; ++r)
+      for (int i = lane; i < N_r; i += 32) p.s_out[(size_t)(t0 + r) * N_r + i] = s_tile[r * stride + i];
+  }
+  if (p.pwin) {
+    for (int i = lane; i < N_r; i += 32)
+      window_runs([&](int r) { return __fdiv_rn(s_tile[r * stride + i], rs_sm[r]); }, seqid, ntok,
+                  t0, N_r, i, p.pwin);
+  }
+}
+
+// The routing decision with one warp per token, for N_r = 32*E experts: lane l holds
+// experts [l*E, l*E + E).  With the group limit a group is 32/G whole lanes, so a
+// group's two best keys merge in log2(32/G) shuffle steps; Top-K_r takes K_r rounds
+// of a warp-wide (key, index) argmax.  A block covers one P-sum window of 32 tokens
+// (8 warps x 4 tokens); the normalised affinities go through shared memory to the
+// window's per-sequence run sums.
+// E consecutive floats (16-byte vectors when E is a multiple of 4; the rows are
+// 16-byte aligned then).
+template <int E>
+__device__ __forceinline__ void load_row(const float* __restrict__ src, float (&v)[E]) {
+  if constexpr (E % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(src) + q);
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j) v[j] = __ldg(src + j);
+  }
+}
+
+template <int E>
+__device__ __forceinline__ void store_row(float* dst, const float (&v)[E]) {
+  if constexpr (E % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q)
+      reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j) dst[j] = v[j];
+  }
+}
+
+template <int E>
+__global__ void __launch_bounds__(256, 2) router_select_warp_kernel(const float* __restrict__ z_part,
+                                                                 int S, const float* __restrict__ b,
+                                                                 RouteOut p) {
+  constexpr int WARPS = 8, TPW = kPWindow / WARPS, N = 32 * E;
+  __shared__ __align__(16) float sp_tile[kPWindow][N];
+  __shared__ int seqid[kPWindow];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = p.T, t0 = blockIdx.x * kPWindow;
+  const int ntok = min(kPWindow, T - t0);
+  const bool want_p = p.pwin != nullptr;
+  if (want_p && (int)threadIdx.x < ntok) seqid[threadIdx.x] = seq_of(t0 + threadIdx.x, p.seq_offsets, p.n_seq);
+  float bl[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) bl[j] = __ldg(b + lane * E + j);
+  const int G = p.G, lpg = 32 / G, my_group = lane / lpg;
+  const int kg = p.K_r / p.M;
+
+  for (int r = 0; r < TPW; ++r) {
+    const int tl = warp * TPW + r, t = t0 + tl;
+    if (tl >= ntok) break;                       // warp-uniform
+    float z[E];
+    const float* zp = z_part + (size_t)t * N + lane * E;
+    load_row<E>(zp, z);
+    for (int sp = 1; sp < S; ++sp) {
+      float zs[E];
+      load_row<E>(zp + (size_t)sp * T * N, zs);
+#pragma unroll
+      for (int j = 0; j < E; ++j) z[j] = __fadd_rn(z[j], zs[j]);
+    }
+    float sv[E], key[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      sv[j] = sigmoid_f32(z[j]);
+      key[j] = __fadd_rn(sv[j], bl[j]);           // one fp32 rounding
+    }
+    if (p.s_out) store_row<E>(p.s_out + (size_t)t * N + lane * E, sv);
+    if (want_p) {
+      float part = 0.f;
+#pragma unroll
+      for (int j = 0; j < E; ++j) part = __fadd_rn(part, sv[j]);
+      const float rs = warp_sum(part);
+      float spv[E];
+#pragma unroll
+      for (int j = 0; j < E; ++j) spv[j] = __fdiv_rn(sv[j], rs);
+      store_row<E>(&sp_tile[tl][lane * E], spv);
+    }
+
+    if (G > 1) {
+      // the group's kg <= 2 best keys (values only: ties do not change the sum)
+      float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const float lo = fminf(t1, key[j]);
+        t1 = fmaxf(t1, key[j]);
+        t2 = fmaxf(t2, lo);
+      }
+      for (int o = 1; o < lpg; o <<= 1) {
+        const float a1 = __shfl_xor_sync(0xffffffffu, t1, o);
+        const float a2 = __shfl_xor_sync(0xffffffffu, t2, o);
+        const float lo = fminf(t1, a1);
+        t1 = fmaxf(t1, a1);
+        t2 = fmaxf(fmaxf(t2, a2), lo);
+      }
+      const float gs = kg == 1 ? t1 : __fadd_rn(t1, t2);   // descending order
+      int rank = 0;                                          // groups ranked above mine
+      for (int g = 0; g < G; ++g) {
+        const float o = __shfl_sync(0xffffffffu, gs, g * lpg);
+        rank += (o > gs || (o == gs && g < my_group)) ? 1 : 0;
+      }
+      if (rank >= p.M) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) key[j] = -CUDART_INF_F;
+      }
+    }
+
+    // Top-K_r: the lane's best entry (lowest index among equal keys), then K_r rounds
+    // of the warp argmax; only the winning lane recomputes its best.
+    float bk = -CUDART_INF_F;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+      if (key[j] > bk) { bk = key[j]; bi = lane * E + j; }
+    int my_idx = 0;
+    for (int k = 0; k < p.K_r; ++k) {
+      float wk = bk;
+      int wi = bi;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float k2 = __shfl_xor_sync(0xffffffffu, wk, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, wi, o);
+        if (better(k2, i2, wk, wi)) { wk = k2; wi = i2; }
+      }
+      if (lane == k) my_idx = wi;
+      if (wi == bi) {                 // this lane's entry was taken
+        bk = -CUDART_INF_F;
+        bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          if (lane * E + j == wi) key[j] = -CUDART_INF_F;
+          else if (key[j] > bk) { bk = key[j]; bi = lane * E + j; }
         }
       }
     }
-    select_row(row, b_sm, c1, c2, t, p);
-  }
-  rs_sm[lane] = rowsum;
-  __syncwarp();
-  if (p.s_out || p.sprime) {
-    for (int r = 0; r < kTok; ++r) {
-      const int tr = t0 + r;
-      if (tr >= T) break;
-      const float rs = rs_sm[r];
-      for (int i = lane; i < N_r; i += 32) {
-        const float sv = s_tile[r * stride + i];
-        if (p.s_out) p.s_out[(size_t)tr * N_r + i] = sv;
-        if (p.sprime) p.sprime[(size_t)tr * N_r + i] = __fdiv_rn(sv, rs);
-      }
+    // raw s of the selected experts, gates normalised over them in selection order
+    const int owner = my_idx / E, slot = my_idx - owner * E;
+    float my_s = 0.f;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const float v = __shfl_sync(0xffffffffu, sv[j], owner);
+      if (slot == j) my_s = v;
+    }
+    float total = 0.f;
+    for (int k = 0; k < p.K_r; ++k) total = __fadd_rn(total, __shfl_sync(0xffffffffu, my_s, k));
+    if (lane < p.K_r) {
+      p.topk_idx[(size_t)t * p.K_r + lane] = my_idx;
+      p.topk_gate[(size_t)t * p.K_r + lane] = __fdiv_rn(my_s, total);
     }
   }
-}
-
-// partial[(j*Z + z)*N_r + i] = sum over slab z of sequence j of sprime[t, i] (fp64).
-__global__ void __launch_bounds__(256) seq_psum_partial_kernel(const float* __restrict__ sprime,
-                                                               const int32_t* __restrict__ seq_offsets,
-                                                               int N_r, int Z,
-                                                               double* __restrict__ partial) {
-  __shared__ double red[8][32];
-  const int j = blockIdx.x, z = blockIdx.z;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int i = blockIdx.y * 32 + lane;
-  const int a = seq_offsets[j], bnd = seq_offsets[j + 1];
-  const int len = bnd - a;
-  const int L = (len + Z - 1) / Z;
-  const int t_begin = a + z * L;
-  const int t_end = min(t_begin + L, bnd);
-  double acc = 0.0;
-  if (i < N_r)
-    for (int t = t_begin + warp; t < t_end; t += 8) acc += (double)sprime[(size_t)t * N_r + i];
-  red[warp][lane] = acc;
-  __syncthreads();
-  if (warp == 0 && i < N_r) {
-    double s = 0.0;
-    for (int w = 0; w < 8; ++w) s += red[w][lane];
-    partial[((size_t)j * Z + z) * N_r + i] = s;
+  if (want_p) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < N; i += blockDim.x)
+      window_runs([&](int r) { return sp_tile[r][i]; }, seqid, ntok, t0, N, i, p.pwin);
   }
 }
 
-__global__ void seq_psum_final_kernel(const double* __restrict__ partial, int n_seq, int N_r,
-                                      int Z, float* __restrict__ out) {
-  const int x = blockIdx.x * blockDim.x + threadIdx.x;
-  if (x >= n_seq * N_r) return;
-  const int j = x / N_r, i = x % N_r;
-  double s = 0.0;
-  for (int z = 0; z < Z; ++z) s += partial[((size_t)j * Z + z) * N_r + i];
-  out[x] = (float)s;
+// Whether router_select_warp_kernel takes the shape: 32, 64, 128 or 256 experts and,
+// with the group limit, groups of whole lanes (G divides 32) keeping K_r/M <= 2 keys.
+inline bool warp_select_ok(int N_r, int K_r, int G, int M) {
+  if (N_r != 32 && N_r != 64 && N_r != 128 && N_r != 256) return false;
+  if (G == 1) return true;
+  return 32 % G == 0 && K_r / M <= 2;
+}
+
+// out[j, i] = sum over the P-sum windows' run sums of sequence j: the run starting at
+// the sequence's first token and one at every window start inside the sequence, in
+// token order, accumulated in fp64.
+__global__ void __launch_bounds__(256) seq_psum_kernel(const float* __restrict__ pwin,
+                                                       const int32_t* __restrict__ seq_offsets,
+                                                       int N_r, float* __restrict__ out) {
+  const int j = blockIdx.x, i = blockIdx.y * blockDim.x + threadIdx.x;
+  if (i >= N_r) return;
+  const int a = seq_offsets[j], z = seq_offsets[j + 1];
+  double acc = 0.0;
+  if (a < z) {
+    acc = (double)pwin[(size_t)a * N_r + i];
+    int w = (a / kPWindow + 1) * kPWindow;
+    for (; w + 3 * kPWindow < z; w += 4 * kPWindow) {
+      const float v0 = pwin[(size_t)w * N_r + i];
+      const float v1 = pwin[(size_t)(w + kPWindow) * N_r + i];
+      const float v2 = pwin[(size_t)(w + 2 * kPWindow) * N_r + i];
+      const float v3 = pwin[(size_t)(w + 3 * kPWindow) * N_r + i];
+      acc += (double)v0;
+      acc += (double)v1;
+      acc += (double)v2;
+      acc += (double)v3;
+    }
+    for (; w < z; w += kPWindow) acc += (double)pwin[(size_t)w * N_r + i];
+  }
+  out[(size_t)j * N_r + i] = (float)acc;
 }
 
 }  // namespace
@@ -183,18 +349,26 @@ cudaError_t launch_router_gemm_simt(const void* u, const void* e, moe_dtype dt, 
 cudaError_t launch_router_select(const float* z_part, int S, const float* b, const RouteOut& p,
                                  cudaStream_t st) {
   if (p.T == 0) return cudaSuccess;
-  const int fast = fast_select_ok(p.N_r, p.K_r, p.G, p.M) ? 1 : 0;
-  router_select_kernel<<<(p.T + kTok - 1) / kTok, 32, 0, st>>>(z_part, S, b, p, fast);
+  const int blocks = (p.T + kPWindow - 1) / kPWindow;
+  if (warp_select_ok(p.N_r, p.K_r, p.G, p.M)) {
+    switch (p.N_r) {
+      case 32: router_select_warp_kernel<1><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
+      case 64: router_select_warp_kernel<2><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
+      case 128: router_select_warp_kernel<4><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
+      default: router_select_warp_kernel<8><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
+    }
+  } else {
+    const int fast = fast_select_ok(p.N_r, p.K_r, p.G, p.M) ? 1 : 0;
+    router_select_kernel<<<blocks, 32, 0, st>>>(z_part, S, b, p, fast);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_seq_psum(const float* sprime, const int32_t* seq_offsets, int n_seq,
-                            int N_r, double* partial, float* out, cudaStream_t st) {
+cudaError_t launch_seq_psum(const float* pwin, const int32_t* seq_offsets, int n_seq, int N_r,
+                            float* out, cudaStream_t st) {
   if (n_seq == 0) return cudaSuccess;
-  const dim3 grid(n_seq, (N_r + 31) / 32, kSeqSlabs);
-  seq_psum_partial_kernel<<<grid, 256, 0, st>>>(sprime, seq_offsets, N_r, kSeqSlabs, partial);
-  const int n = n_seq * N_r;
-  seq_psum_final_kernel<<<(n + 255) / 256, 256, 0, st>>>(partial, n_seq, N_r, kSeqSlabs, out);
+  const dim3 grid(n_seq, (N_r + 255) / 256);
+  seq_psum_kernel<<<grid, 256, 0, st>>>(pwin, seq_offsets, N_r, out);
   return cudaGetLastError();
 }
 

@@ -144,14 +144,15 @@ class ClockSampler:
 def work(cfg):
     T, d, N_r, K_r, N_s, I = cfg.T, cfg.d, cfg.N_r, cfg.K_r, cfg.N_s, cfg.I
     rows = T * K_r + N_s * T
+    q = 1 if cfg.fp8 else 2        # bytes per FFN operand element (E4M3 or bf16)
     return {
         "router_flop": 2.0 * T * d * N_r,
         "router_bytes": T * d * 2 + N_r * d * 2 + T * K_r * 8,
-        "gather_bytes": T * d * 2 + T * K_r * d * 2,
+        "gather_bytes": T * d * q + T * K_r * d * q,
         "gate_up_flop": 2.0 * rows * d * 2 * I,
-        "gate_up_bytes": (N_r + N_s) * 2 * I * d * 2 + rows * d * 2 + rows * I * 2,
+        "gate_up_bytes": (N_r + N_s) * 2 * I * d * q + rows * d * q + rows * I * q,
         "down_flop": 2.0 * rows * I * d,
-        "down_bytes": (N_r + N_s) * d * I * 2 + rows * I * 2 + rows * d * 2,
+        "down_bytes": (N_r + N_s) * d * I * q + rows * I * q + rows * d * 2,
         "combine_bytes": T * d * 2 + rows * d * 2 + T * d * 4 + T * K_r * 8,
         "layer_flop": 2.0 * T * d * N_r + 2.0 * rows * d * 3 * I,
     }
@@ -262,7 +263,7 @@ def config_block(cfg):
             "T": cfg.T, "d": cfg.d, "N_r": cfg.N_r, "K_r": cfg.K_r, "N_s": cfg.N_s, "I": cfg.I,
             "G": cfg.G, "M": cfg.M, "n_seq": cfg.n_seq, "parallelism": "replicas",
             "l2": "inputs larger than L2: every step reads all expert weights "
-                  f"({(cfg.N_r + cfg.N_s) * 3 * cfg.I * cfg.d * 2 / 1e9:.1f} GB)"}
+                  f"({(cfg.N_r + cfg.N_s) * 3 * cfg.I * cfg.d * (1 if cfg.fp8 else 2) / 1e9:.2f} GB)"}
 
 
 # --------------------------------------------------------------------- our arm ---
@@ -276,7 +277,7 @@ def run_ours(args, cfg, ws, rank, local):
     w = {k: x[k] for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")}
     layer = moe.MoELayer(T=cfg.T, d=cfg.d, N_r=cfg.N_r, K_r=cfg.K_r, N_s=cfg.N_s, I=cfg.I,
                          G=cfg.G, M=cfg.M, e=x["e"], b=x["b"].clone(), weights=w,
-                         n_seq=cfg.n_seq, gamma=cfg.gamma, alpha=cfg.alpha)
+                         n_seq=cfg.n_seq, gamma=cfg.gamma, alpha=cfg.alpha, fp8=cfg.fp8)
     u, off = x["u"], x["seq_offsets"]
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -356,6 +357,10 @@ def run_ours(args, cfg, ws, rank, local):
     t_gu = stages["gate_up"] / 1e3
     achieved = wk["gate_up_flop"] / t_gu / 1e12
     peak = pk["bf16_tflops_sustained"]
+    peak_source = f"{pk['source']} bf16 sustained"
+    if cfg.fp8:   # E4M3 dense rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
+        peak *= 2.0
+        peak_source += " x 2 (nominal E4M3/bf16 ratio)"
     sha = kernel_src_sha()
     traffic = NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["kernel_src_sha"] == sha else None
     tok_s = cfg.T * ws / (ms / 1e3)
@@ -370,18 +375,21 @@ def run_ours(args, cfg, ws, rank, local):
         "combine_bias_stat": {"ms": stages["combine_bias_stat"],
                               "GB/s": wk["combine_bytes"] / (stages["combine_bias_stat"] / 1e3) / 1e9},
     }
-    layer_roof_ms = 1e3 * max(wk["layer_flop"] / (pk["bf16_tflops_sustained"] * 1e12),
-                              ((cfg.N_r + cfg.N_s) * 3 * cfg.I * cfg.d * 2 + cfg.T * cfg.d * 6)
+    wq = 1 if cfg.fp8 else 2
+    layer_roof_ms = 1e3 * max(wk["layer_flop"] / (peak * 1e12),
+                              ((cfg.N_r + cfg.N_s) * 3 * cfg.I * cfg.d * wq + cfg.T * cfg.d * 6)
                               / (pk["hbm_gbs"] * 1e9))
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3" if cfg.fp8 else "bf16", "data": "synthetic",
         "config": config_block(cfg),
-        "roofline": {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU GEMM, tcgen05)",
+        "roofline": {"bound": "tensor",
+                     "kernel": "gate_up (grouped SwiGLU GEMM, tcgen05 "
+                               + ("kind::f8f6f4, E4M3)" if cfg.fp8 else "kind::f16, bf16)"),
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{pk['source']} bf16 sustained"},
+                     "peak_source": peak_source},
         "layer_roofline_frac": layer_roof_ms / ms,
         "kernels": kernels,
         "e2e": {"value": cfg.T * ws / (e2e_ms / 1e3), "unit": "tokens/s",
