@@ -14,12 +14,13 @@
 //   warp 0      TMA producer: A [128 rows x 128 B] and B [256 rows x 128 B] per
 //               stage, 128-byte swizzled, 4-stage ring.
 //   warp 1      allocates 512 TMEM columns, issues the MMAs (one thread).
-//   warps 2..9  epilogue: two warps per TMEM lane quarter, each holding 128 fp32
-//               accumulators of its row (one half of the tile's columns).
+//   warps 2..17 epilogue: four warps per TMEM lane quarter, each holding 64 fp32
+//               accumulators of its row (one quarter of the tile's columns), so
+//               four warps per scheduler hide the TMEM-load latency.
 //
 // gate/up (MODE 0): B = 128 rows of W_gate over the same 128 rows of W_up; the
 //   epilogue forms h = silu(gate) * up for 128 columns of a row, quantises that 1x128
-//   tile to E4M3 (the two halves exchange their amax through shared memory) and
+//   tile to E4M3 (the four quarters exchange their amax through shared memory) and
 //   writes the codes and the scale.
 // down (MODE 1): B = 256 rows of W_down (two 128-row scale blocks); y is bf16.
 #include <cuda_fp8.h>
@@ -41,14 +42,14 @@ constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 16;
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 
 struct Ctrl {
   uint64_t full[STAGES], empty[STAGES], pfull[2], pempty[2], xbar[2], fin;
   uint32_t tmem_base;
   int abort_flag;
-  float amax[2][2][BM];   // [tile parity][column half][row]
+  float amax[2][4][BM];   // [tile parity][column quarter][row]
   SegTable tab;
 };
 
@@ -201,51 +202,49 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue --
     const int q = warp & 3;              // TMEM lane quarter this warp can access
-    const int hh = (warp - 2) >> 2;      // column half of the tile
+    const int cq = (warp - 2) >> 2;      // column quarter of the tile
     const int row_in_tile = q * 32 + lane;
     const int nkc_out = N / 128;         // scale columns of the output (MODE 0)
+    const int nblk = N / 128;            // 128-row weight blocks per expert along N
     int c = 0, tcount = 0;
     bool alive = true;
     for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x, ++tcount) {
-      const TileCoord tcd = decode_tile(C.tab, tile, n_tiles_n);
-      const bool shared = tcd.seg >= s.N_r;
-      const int e = shared ? tcd.seg - s.N_r : tcd.seg;
-      const int row_local = tcd.m * BM + row_in_tile;
-      const bool row_ok = row_local < tcd.rows;
-      // A-row scales: routed rows of x_perm / h, or the token rows of u (shared, MODE 0)
-      const float* a_sc;
-      size_t a_row;
-      if (MODE == 0 && shared) {
-        a_sc = args.a_scale_s;
-        a_row = (size_t)row_local;
-      } else {
-        a_sc = args.a_scale_r;
-        a_row = (size_t)(MODE == 0 ? tcd.row0 : tcd.out_row0) + row_local;
+      // Only what the chunk loop needs stays live across it (the register budget is
+      // 96 per thread): the scale offsets, -1 where this thread has no valid row or
+      // block.  The tile's coordinates are decoded again for the output.
+      int a_off, b_off;
+      bool shared;
+      {
+        const TileCoord tcd = decode_tile(C.tab, tile, n_tiles_n);
+        shared = tcd.seg >= s.N_r;
+        const int e = shared ? tcd.seg - s.N_r : tcd.seg;
+        const int row_local = tcd.m * BM + row_in_tile;
+        const int a_row = (MODE == 0 && shared) ? row_local
+                          : (MODE == 0 ? tcd.row0 : tcd.out_row0) + row_local;
+        a_off = row_local < tcd.rows ? a_row * nk : -1;
+        const int blk0 = MODE == 0 ? tcd.n : tcd.n * 2 + (cq >> 1);
+        b_off = blk0 < nblk ? (e * nblk + blk0) * nk : -1;
       }
-      a_sc += a_row * nk;
-      // weight block scales for this tile's columns
-      const float* b0 = (shared ? args.b0_scale_s : args.b0_scale_r);
-      const float* b1 = (shared ? args.b1_scale_s : args.b1_scale_r);
-      const int nblk = N / 128;            // 128-row blocks per expert along N
-      int blk0;                            // block row of this thread's columns
-      bool blk_ok = true;
-      if (MODE == 0) {
-        blk0 = tcd.n;
-      } else {
-        blk0 = tcd.n * 2 + hh;
-        blk_ok = blk0 < nblk;
-      }
-      const float* b0row = b0 + ((size_t)e * nblk + (blk_ok ? blk0 : 0)) * nk;
-      const float* b1row = MODE == 0 ? b1 + ((size_t)e * nblk + blk0) * nk : nullptr;
+      const float* a_sc = (MODE == 0 && shared) ? args.a_scale_s : args.a_scale_r;
+      const float* b0 = shared ? args.b0_scale_s : args.b0_scale_r;
+      const float* b1 = shared ? args.b1_scale_s : args.b1_scale_r;   // same block layout
 
-      float acc[128];
+      float acc[64];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+      for (int j = 0; j < 64; ++j) acc[j] = 0.f;
 
+      // scales of chunk kb+1 are fetched while chunk kb is promoted
+      float sa_n = a_off >= 0 ? __ldg(a_sc + a_off) : 0.f;
+      float sb0_n = b_off >= 0 ? __ldg(b0 + b_off) : 0.f;
+      float sb1_n = (MODE == 0 && b_off >= 0) ? __ldg(b1 + b_off) : 0.f;
+#pragma unroll 1
       for (int kb = 0; kb < nk; ++kb, ++c) {
-        const float sa = row_ok ? __ldg(a_sc + kb) : 0.f;
-        const float sb0 = blk_ok ? __ldg(b0row + kb) : 0.f;
-        const float sb1 = MODE == 0 ? __ldg(b1row + kb) : 0.f;
+        const float sa = sa_n, sb0 = sb0_n, sb1 = sb1_n;
+        if (kb + 1 < nk) {
+          sa_n = a_off >= 0 ? __ldg(a_sc + a_off + kb + 1) : 0.f;
+          sb0_n = b_off >= 0 ? __ldg(b0 + b_off + kb + 1) : 0.f;
+          if (MODE == 0) sb1_n = b_off >= 0 ? __ldg(b1 + b_off + kb + 1) : 0.f;
+        }
         const int buf = c & 1;
         const bool got = tc::mbar_wait(&C.pfull[buf], (c >> 1) & 1, abort_flag, args.err);
         if (!__all_sync(0xffffffffu, got)) { alive = false; break; }
@@ -255,21 +254,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int part = 0; part < 4; ++part) {
           int col;
           float sc;
-          if (MODE == 0) {
-            col = (part < 2 ? 0 : BN / 2) + hh * 64 + (part & 1) * 32;
+          if (MODE == 0) {   // parts 0,1: gate columns; 2,3: the same up columns
+            col = (part < 2 ? 0 : BN / 2) + cq * 32 + (part & 1) * 16;
             sc = sa * (part < 2 ? sb0 : sb1);
           } else {
-            col = hh * 128 + part * 32;
+            col = cq * 64 + part * 16;
             sc = sa * sb0;
           }
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t p[16];
-            tc::tmem_ld16(t_base + col + half * 16, p);
+          for (int h8 = 0; h8 < 2; ++h8) {
+            uint32_t p[8];
+            tc::tmem_ld8(t_base + col + h8 * 8, p);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int a = part * 32 + half * 16 + j;
+            for (int j = 0; j < 8; ++j) {
+              const int a = part * 16 + h8 * 8 + j;
               acc[a] = fmaf(__uint_as_float(p[j]), sc, acc[a]);
             }
           }
@@ -279,26 +278,31 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!alive) break;
 
+      const TileCoord tcd = decode_tile(C.tab, tile, n_tiles_n);
+      const int row_local = tcd.m * BM + row_in_tile;
+      const bool row_ok = row_local < tcd.rows;
       const size_t out_row = (size_t)tcd.out_row0 + row_local;
       if (MODE == 0) {
-        // h for this thread's 64 columns, then the 1x128 tile scale from both halves
+        // h for this thread's 32 columns, then the 1x128 tile scale from all four quarters
         float amax = 0.f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          acc[j] = silu(acc[j]) * acc[64 + j];
+        for (int j = 0; j < 32; ++j) {
+          acc[j] = silu(acc[j]) * acc[32 + j];
           amax = fmaxf(amax, fabsf(acc[j]));
         }
         const int tb = tcount & 1;
-        C.amax[tb][hh][row_in_tile] = amax;
+        C.amax[tb][cq][row_in_tile] = amax;
         tc::mbar_arrive(&C.xbar[tb]);   // release: the amax store is visible after the wait
         const bool xg = tc::mbar_wait(&C.xbar[tb], (tcount >> 1) & 1, abort_flag, args.err);
         if (!__all_sync(0xffffffffu, xg)) break;
-        const float tile_amax = fmaxf(amax, C.amax[tb][hh ^ 1][row_in_tile]);
+        float tile_amax = 0.f;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) tile_amax = fmaxf(tile_amax, C.amax[tb][x][row_in_tile]);
         const float scale = tile_amax > 0.f ? __fdiv_rn(tile_amax, 448.f) : 1.f;
         if (row_ok) {
-          uint8_t* hq = static_cast<uint8_t*>(args.out) + out_row * N + tcd.n * 128 + hh * 64;
+          uint8_t* hq = static_cast<uint8_t*>(args.out) + out_row * N + tcd.n * 128 + cq * 32;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
+          for (int v = 0; v < 2; ++v) {
             uint32_t w[4];
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
@@ -308,14 +312,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             reinterpret_cast<uint4*>(hq)[v] = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          if (hh == 0) args.out_scale[out_row * nkc_out + tcd.n] = scale;
+          if (cq == 0) args.out_scale[out_row * nkc_out + tcd.n] = scale;
         }
       } else {
-        const int col0 = tcd.n * BN + hh * 128;
+        const int col0 = tcd.n * BN + cq * 64;
         if (row_ok && col0 < N) {
           __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(args.out) + out_row * N + col0;
 #pragma unroll
-          for (int v = 0; v < 16; ++v)
+          for (int v = 0; v < 8; ++v)
             reinterpret_cast<uint4*>(yrow)[v] =
                 make_uint4(pack_bf16(acc[8 * v + 0], acc[8 * v + 1]), pack_bf16(acc[8 * v + 2], acc[8 * v + 3]),
                            pack_bf16(acc[8 * v + 4], acc[8 * v + 5]), pack_bf16(acc[8 * v + 6], acc[8 * v + 7]));
