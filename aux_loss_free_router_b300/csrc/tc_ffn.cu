@@ -1,31 +1,41 @@
-// Grouped SwiGLU expert GEMMs on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+// Grouped SwiGLU expert GEMMs on the sm_103a tensor cores: tcgen05 pair MMAs over
+// TMEM, fed by TMA.
 //
-// Weights on the M side, tokens on the N side: each MMA computes a [128 features x
-// n tokens] block of the transposed output, D^T = W X^T.  The MMA's N (tokens) goes
-// down to 16 in steps of 16, so the last tile of an expert's segment is sized to the
-// tokens it has (at most 15 padding tokens), where a token-major M tile would pad up
-// to 127 rows: on the DeepSeek-V3 layer that is about a fifth of the routed work.
+// Weights on the M side, tokens on the N side: each MMA computes a block of the
+// transposed output, D^T = W X^T.  The MMA's N (tokens) goes down to 16 in steps of
+// 16, so the last tile of an expert's segment is sized to the tokens it has (at most
+// 15 padding tokens), where a token-major M tile would pad up to 127 rows.
 //
-// One persistent CTA per SM walks the tiles of the segment schedule (ffn_sched.cuh):
-// segment-major, then feature tile, then token tile, so CTAs running at the same time
-// share an expert's weight tile through L2.  Warp roles:
-//   warp 0      TMA producer into a 4-stage shared-memory ring (48 KB per stage).
-//   warp 1      allocates 512 TMEM columns and issues the MMAs (one thread) into one
-//               of two 256-column fp32 accumulators, so the epilogue of tile i
-//               overlaps the MMAs of tile i+1.
-//   warps 2..5  epilogue: TMEM lane = feature, column = token; each warp transposes
+// Two CTAs on two SMs form a pair (a cluster of two) and issue M=256 MMAs together
+// (cta_group::2): each CTA holds 128 of the 256 weight rows and half of the token rows
+// of a K step, and receives its 128 rows of the accumulator in its own TMEM.  Per SM
+// a K step of 64 moves 32 KB (16 KB of weights, 16 KB of tokens) for 128 x 256 x 64
+// MACs, two thirds of what a single-SM M=128 x N=256 MMA needs; the TMA ingest of an
+// SM, not the tensor pipe, is what bounds these GEMMs.
+//
+// One persistent pair per two SMs walks the tiles of the segment schedule
+// (ffn_sched.cuh): segment-major, then feature tile, then token tile of 256.  Warp
+// roles in each CTA:
+//   warp 0      TMA producer: this CTA's weight and token rows into a 6-stage ring
+//               (32 KB per stage); completion is counted on the even CTA's barrier.
+//   warp 1      allocates 512 TMEM columns (with the peer); in the even CTA one thread
+//               issues the pair MMAs into one of two 256-column accumulators, so the
+//               epilogue of tile i overlaps the MMAs of tile i+1.
+//   warps 2..5  epilogue: TMEM lane = feature row, column = token; each warp transposes
 //               32 features x 16 tokens through its own shared-memory scratch and
 //               writes 16-byte pieces of token rows.
 //
-// gate/up (MODE 0): a stage holds W_gate and W_up [128 features x 64 K] and X [128
-//   tokens x 64 K]; two MMAs per K step give gate (columns 0..127) and up (128..255)
-//   of the same features; the epilogue writes h = silu(gate) * up.
-// down (MODE 1): a stage holds W_down [128 features x 64 K] and H [256 tokens x 64 K];
-//   the epilogue writes y.
+// gate/up (MODE 0): a pair tile is 128 columns of h.  Each CTA's 128 weight rows are
+//   64 rows of W_gate over the same 64 rows of W_up, so TMEM lanes 0..63 hold gate and
+//   lanes 64..127 up of the same features; per 16 tokens the four epilogue warps stage
+//   their raw values in shared memory and each thread forms 8 features of
+//   h = silu(gate) * up for one token.
+// down (MODE 1): a pair tile is 256 columns of y, 128 W_down rows per CTA.
 // Tokens past the end of a tile's segment are loaded (or zero-filled past the tensor
-// end) but sit beyond the MMA's N or are not stored; features past the end of the
-// output width are computed from the next expert's rows (or zeros) and not stored.
+// end) but sit beyond the MMA's N or are not stored; features past the output width
+// are computed from the next expert's rows (or zeros) and not stored.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "ffn_sched.cuh"
@@ -37,25 +47,28 @@ namespace moe {
 
 namespace {
 
-constexpr int BF = 128, BK = 64, STAGES = 4;
-constexpr int W_BYTES = BF * BK * 2;          // one weight tile
-constexpr int STAGE_BYTES = 3 * W_BYTES;      // MODE 0: Wg, Wu, X[128]; MODE 1: Wd, H[256]
+constexpr int BK = 64, STAGES = 6, BT = 256;
+constexpr int A_BYTES = 128 * BK * 2;           // this CTA's 128 weight rows
+constexpr int B_BYTES = (BT / 2) * BK * 2;      // this CTA's half of the token rows
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
 constexpr int TMEM_COLS = 512, ACC_COLS = 256;
 constexpr int THREADS = 192;
-constexpr int SCRATCH = 16 * 32 * 2;          // per epilogue warp: 16 tokens x 32 features bf16
+constexpr int SCRATCH = 16 * 32 * 2;            // per epilogue warp: 16 tokens x 32 features bf16
+constexpr int XCH = 2 * 16 * 128 * 4;           // gate/up: raw values [2 buffers][16 tokens][128 rows]
 
-template <int MODE> struct Tiles {
-  static constexpr int BT = MODE == 0 ? 128 : 256;   // tokens per tile (MMA N at most)
+template <int MODE> struct Pair {
+  static constexpr int FEAT = MODE == 0 ? 128 : 256;   // output columns per pair tile
 };
 
 struct Ctrl {
-  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], fin;
+  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], xfull[2], xempty[2], fin;
   uint32_t tmem_base;
   int abort_flag;
   SegTable tab;
 };
 
-constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + 4 * SCRATCH + sizeof(Ctrl) + 1024;
+constexpr size_t kSmemBytes =
+    (size_t)STAGES * STAGE_BYTES + 4 * SCRATCH + XCH + sizeof(Ctrl) + 1024;
 
 struct TcArgs {
   FfnShape s;
@@ -64,7 +77,37 @@ struct TcArgs {
   int32_t* err;
 };
 
-__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+// silu(g) * u = g * u / (1 + e^-g), with the fast reciprocal division (the result is
+// rounded to bf16).
+__device__ __forceinline__ float swiglu(float g, float u) {
+  return __fdividef(g * u, 1.f + __expf(-g));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 16 tokens x 32 features of one warp (lane = feature, v[j] = token j) to token rows:
+// through the warp's scratch, then 16-byte pieces of 8 features.
+__device__ __forceinline__ void store_transposed(__nv_bfloat16* scr, const float (&v)[16], int lane,
+                                                 __nv_bfloat16* out, size_t row0, int j0, int n_tok,
+                                                 int f0, int N) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) scr[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int item = i * 32 + lane;      // 16 tokens x 4 pieces of 8 features
+    const int tok = item >> 2, piece = item & 3;
+    const int f = f0 + piece * 8;
+    if (j0 + tok < n_tok && f < N) {
+      const uint4 val = *reinterpret_cast<const uint4*>(scr + tok * 32 + piece * 8);
+      *reinterpret_cast<uint4*>(out + (row0 + j0 + tok) * N + f) = val;
+    }
+  }
+  __syncwarp();
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -72,18 +115,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                   const __grid_constant__ CUtensorMap mW0_r, const __grid_constant__ CUtensorMap mW1_r,
                   const __grid_constant__ CUtensorMap mW0_s, const __grid_constant__ CUtensorMap mW1_s,
                   TcArgs args) {
-  constexpr int BT = Tiles<MODE>::BT;
+  constexpr int FEAT = Pair<MODE>::FEAT;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_off = tc::smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_off & 1023u)) & 1023u);
   uint8_t* scratch = base + STAGES * STAGE_BYTES;
-  Ctrl& C = *reinterpret_cast<Ctrl*>(scratch + 4 * SCRATCH);
+  float* xch = reinterpret_cast<float*>(scratch + 4 * SCRATCH);
+  Ctrl& C = *reinterpret_cast<Ctrl*>(scratch + 4 * SCRATCH + XCH);
 
   const FfnShape s = args.s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = tc::cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
   const int K = MODE == 0 ? s.d : s.I;
-  const int N = MODE == 0 ? s.I : s.d;            // output width (features)
-  const int n_ft = (N + BF - 1) / BF;             // feature tiles per expert
+  const int N = MODE == 0 ? s.I : s.d;            // output width
+  const int n_ft = (N + FEAT - 1) / FEAT;         // feature tiles per expert
   const int nk = (K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -93,7 +140,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&C.tfull[i], 1);
-      tc::mbar_init(&C.tempty[i], 128);
+      tc::mbar_init(&C.tempty[i], 8);      // one arrival per epilogue warp of both CTAs
+      tc::mbar_init(&C.xfull[i], 128);
+      tc::mbar_init(&C.xempty[i], 128);
     }
     tc::mbar_init(&C.fin, 1);
     C.abort_flag = 0;
@@ -104,13 +153,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tma_prefetch_desc(&mW0_r);
   }
   if (warp == 1) {
-    tc::tmem_alloc(&C.tmem_base, TMEM_COLS);
-    tc::tmem_relinquish();
+    tc::tmem_alloc_pair(&C.tmem_base, TMEM_COLS);
+    tc::tmem_relinquish_pair();
   }
   build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BT, n_ft);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  tc::cluster_sync();   // both CTAs' barriers exist before any remote arrive or copy
   const uint32_t tmem_base = C.tmem_base;
   const int total = C.tab.total;
   volatile int* abort_flag = &C.abort_flag;
@@ -119,46 +169,45 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ producer --
       int it = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+      for (int tile = pair; tile < total && !*abort_flag; tile += n_pairs) {
         const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
         const bool shared = tcd.seg >= s.N_r;
         const int e = shared ? tcd.seg - s.N_r : tcd.seg;
+        const int n_tok = min(BT, tcd.rows - tcd.m * BT);
+        const int half = ((n_tok + 15) & ~15) >> 1;     // token rows per CTA
         const CUtensorMap* mX = (MODE == 0 && shared) ? &mX_s : &mX_r;
-        const int x_row = (MODE == 0 ? (shared ? 0 : tcd.row0) : tcd.out_row0) + tcd.m * BT;
+        const int x_row = (MODE == 0 ? (shared ? 0 : tcd.row0) : tcd.out_row0) + tcd.m * BT +
+                          (int)rank * half;
         const CUtensorMap* mW0 = shared ? &mW0_s : &mW0_r;
         const CUtensorMap* mW1 = shared ? &mW1_s : &mW1_r;
-        const int w_row = e * N + tcd.n * BF;
+        const int w_row = e * N + tcd.n * FEAT + (int)rank * (FEAT / 2);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int st = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!tc::mbar_wait(&C.empty[st], ph ^ 1, abort_flag, args.err)) { ok = false; break; }
-          uint8_t* sw = base + st * STAGE_BYTES;
-          tc::mbar_arrive_expect_tx(&C.full[st], STAGE_BYTES);
-          tc::tma_load_2d(sw, mW0, &C.full[st], kb * BK, w_row);
+          const uint32_t bar = tc::cluster_addr(&C.full[st], 0);   // the even CTA's barrier
+          if (leader) tc::mbar_arrive_expect_tx(&C.full[st], 2 * STAGE_BYTES);
+          uint8_t* sa = base + st * STAGE_BYTES;
           if (MODE == 0) {
-            tc::tma_load_2d(sw + W_BYTES, mW1, &C.full[st], kb * BK, w_row);
-            tc::tma_load_2d(sw + 2 * W_BYTES, mX, &C.full[st], kb * BK, x_row);
+            tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);                 // 64 gate rows
+            tc::tma_load_2d_pair(sa + A_BYTES / 2, mW1, bar, kb * BK, w_row);   // 64 up rows
           } else {
-            tc::tma_load_2d(sw + W_BYTES, mX, &C.full[st], kb * BK, x_row);
+            tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);                 // 128 down rows
           }
+          tc::tma_load_2d_pair(sa + A_BYTES, mX, bar, kb * BK, x_row);
         }
         if (!ok) break;
       }
-      if (*abort_flag) {
-        // let the copies already issued land before the CTA exits
-        for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-          tc::mbar_drain(&C.full[j % STAGES], (j / STAGES) & 1);
-      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer --
       int it = 0, tcount = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++tcount) {
+      for (int tile = pair; tile < total && !*abort_flag; tile += n_pairs, ++tcount) {
         const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
         const int n_tok = min(BT, tcd.rows - tcd.m * BT);
-        const uint32_t idesc = tc::idesc_bf16(BF, (n_tok + 15) & ~15);
+        const uint32_t idesc = tc::idesc_bf16(256, (n_tok + 15) & ~15);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (!tc::mbar_wait(&C.tempty[acc], aph ^ 1, abort_flag, args.err)) break;
@@ -171,35 +220,26 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!tc::mbar_wait(&C.full[st], ph, abort_flag, args.err)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t s0 = tc::smem_u32(base + st * STAGE_BYTES);
-          const uint64_t w0 = tc::sdesc_sw128(s0);
-          if (MODE == 0) {
-            const uint64_t w1 = tc::sdesc_sw128(s0 + W_BYTES), x = tc::sdesc_sw128(s0 + 2 * W_BYTES);
+          const uint64_t a = tc::sdesc_sw128(s0), b = tc::sdesc_sw128(s0 + A_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              tc::mma_bf16(d_tmem, w0 + 2 * kk, x + 2 * kk, idesc, (kb | kk) != 0);        // gate
-              tc::mma_bf16(d_tmem + BT, w1 + 2 * kk, x + 2 * kk, idesc, (kb | kk) != 0);   // up
-            }
-          } else {
-            const uint64_t x = tc::sdesc_sw128(s0 + W_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              tc::mma_bf16(d_tmem, w0 + 2 * kk, x + 2 * kk, idesc, (kb | kk) != 0);
-          }
-          tc::mma_commit(&C.empty[st]);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_bf16_pair(d_tmem, a + 2 * kk, b + 2 * kk, idesc, (kb | kk) != 0);
+          tc::mma_commit_pair(&C.empty[st]);
         }
         if (!ok) break;
-        tc::mma_commit(&C.tfull[acc]);
+        tc::mma_commit_pair(&C.tfull[acc]);
       }
-      // every MMA issued by this thread has finished once `fin` flips
-      tc::mma_commit(&C.fin);
-      tc::mbar_drain(&C.fin, 0);
+      // every pair MMA has finished once `fin` flips (in both CTAs)
+      tc::mma_commit_pair(&C.fin);
     }
   } else {
     // ------------------------------------------------------------ epilogue --
-    const int q = warp & 3;   // TMEM lane quarter this warp can access: features q*32..
+    const int q = warp & 3;   // TMEM lane quarter this warp can access
     __nv_bfloat16* scr = reinterpret_cast<__nv_bfloat16*>(scratch + q * SCRATCH);  // [16][32]
-    int tcount = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
+    const uint32_t tempty0 = tc::cluster_addr(&C.tempty[0], 0);
+    const uint32_t tempty1 = tc::cluster_addr(&C.tempty[1], 0);
+    int tcount = 0, cc = 0;
+    for (int tile = pair; tile < total; tile += n_pairs, ++tcount) {
       // warp-uniform decisions: the TMEM loads below are warp-collective
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
@@ -210,67 +250,125 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc::fence_after_sync();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(q * 32) << 16);
-      const int f0 = tcd.n * BF + q * 32;                 // first feature of this warp
       const size_t row0 = (size_t)tcd.out_row0 + (size_t)tcd.m * BT;
+      bool alive = true;
+      if (MODE == 1) {
+        const int f0 = tcd.n * FEAT + (int)rank * 128 + q * 32;
 #pragma unroll 1
-      for (int j0 = 0; j0 < n_tok; j0 += 16) {
-        uint32_t a[16];
-        float v[16];
-        if (MODE == 0) {
-          uint32_t b[16];
-          tc::tmem_ld16(t_base + j0, a);
-          tc::tmem_ld16(t_base + BT + j0, b);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = silu(__uint_as_float(a[j])) * __uint_as_float(b[j]);
-        } else {
+        for (int j0 = 0; j0 < n_tok; j0 += 16) {
+          uint32_t a[16];
+          float v[16];
           tc::tmem_ld16(t_base + j0, a);
           tc::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(a[j]);
+          store_transposed(scr, v, lane, args.out, row0, j0, n_tok, f0, N);
         }
-        // transpose: lane = feature -> 16-byte pieces of 8 features of one token
+      } else {
+        // lanes 0..63: gate rows, 64..127: up rows of the same 64 features.  Per 16
+        // tokens all four warps put their raw values in shared memory, then each
+        // thread forms 8 features of h for one token and writes them as 16 bytes.
+        const int t = q * 32 + lane;                 // this thread's piece: token t/8,
+        const int tok = t >> 3, piece = t & 7;       // features 8*piece .. 8*piece+7
+        const int f = tcd.n * FEAT + (int)rank * 64 + piece * 8;
+#pragma unroll 1
+        for (int j0 = 0; j0 < n_tok; j0 += 16, ++cc) {
+          const int xb = cc & 1;
+          const uint32_t xph = (cc >> 1) & 1;
+          float* S = xch + xb * (16 * 128);                   // [16 tokens][128 rows]
+          uint32_t a[16];
+          tc::tmem_ld16(t_base + j0, a);
+          tc::tmem_ld_wait();
+          bool ok = tc::mbar_wait(&C.xempty[xb], xph ^ 1, abort_flag, args.err);
+          if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) scr[j * 32 + lane] = __float2bfloat16_rn(v[j]);
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int item = i * 32 + lane;      // 16 tokens x 4 pieces of 8 features
-          const int tok = item >> 2, piece = item & 3;
-          const int f = f0 + piece * 8;
+          for (int j = 0; j < 16; ++j) S[j * 128 + q * 32 + lane] = __uint_as_float(a[j]);
+          tc::mbar_arrive(&C.xfull[xb]);   // release: the stores are visible after the wait
+          ok = tc::mbar_wait(&C.xfull[xb], xph, abort_flag, args.err);
+          if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+          const float4* g4 = reinterpret_cast<const float4*>(S + tok * 128 + piece * 8);
+          const float4* u4 = reinterpret_cast<const float4*>(S + tok * 128 + 64 + piece * 8);
+          const float4 g0 = g4[0], g1 = g4[1], u0 = u4[0], u1 = u4[1];
+          tc::mbar_arrive(&C.xempty[xb]);
           if (j0 + tok < n_tok && f < N) {
-            const uint4 val = *reinterpret_cast<const uint4*>(scr + tok * 32 + piece * 8);
-            *reinterpret_cast<uint4*>(args.out + (row0 + j0 + tok) * N + f) = val;
+            const uint4 hv = make_uint4(pack_bf16(swiglu(g0.x, u0.x), swiglu(g0.y, u0.y)),
+                                        pack_bf16(swiglu(g0.z, u0.z), swiglu(g0.w, u0.w)),
+                                        pack_bf16(swiglu(g1.x, u1.x), swiglu(g1.y, u1.y)),
+                                        pack_bf16(swiglu(g1.z, u1.z), swiglu(g1.w, u1.w)));
+            *reinterpret_cast<uint4*>(args.out + (row0 + j0 + tok) * N + f) = hv;
           }
         }
-        __syncwarp();
       }
+      if (!alive) break;
       tc::fence_before_sync();
-      tc::mbar_arrive(&C.tempty[acc]);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_cluster(acc ? tempty1 : tempty0);
     }
   }
+
   tc::fence_before_sync();
   __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // copies this CTA issued report to the even CTA's barriers: give them time to land
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 10000000ull) {
+    }
+  }
+  if (warp == 1 && lane == 0) tc::mbar_drain(&C.fin, 0);
+  __syncthreads();
+  tc::cluster_sync();   // neither CTA leaves while its peer may still touch it
   if (warp == 1) {
     __syncwarp();
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem_base, TMEM_COLS);
+    tc::tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
+}
+
+// Pairs that fit on the device at once (cluster occupancy), cached per device.
+template <int MODE>
+int max_pairs(cudaLaunchConfig_t cfg) {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_ffn_kernel<MODE>, &cfg) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 template <int MODE>
 cudaError_t launch(const FfnShape& s, const CUtensorMap* maps, const int32_t* off, void* out,
                    cudaStream_t st) {
-  constexpr int BT = Tiles<MODE>::BT;
+  constexpr int FEAT = Pair<MODE>::FEAT;
   const int N = MODE == 0 ? s.I : s.d;
   const long long t_ub = (long long)s.T * s.K_r / BT + s.N_r + (long long)s.N_s * ((s.T + BT - 1) / BT);
-  const long long tiles_ub = t_ub * ((N + BF - 1) / BF);
-  const int grid = (int)std::min<long long>(device_sm_count(), std::max<long long>(1, tiles_ub));
+  const long long tiles_ub = t_ub * ((N + FEAT - 1) / FEAT);
   auto k = tc_ffn_kernel<MODE>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int fit = max_pairs<MODE>(cfg);
+  if (fit < 1) return cudaErrorInvalidConfiguration;
+  const int pairs = (int)std::min<long long>(fit, std::max<long long>(1, tiles_ub));
+  cfg.gridDim = dim3(2 * pairs);
   TcArgs a{s, off, static_cast<__nv_bfloat16*>(out), dev_error_ptr()};
-  k<<<grid, THREADS, kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+  err = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -282,17 +380,17 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
                              const int32_t* expert_offset, const moe_expert_weights* w, void* h,
                              cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
-  constexpr int BT = Tiles<0>::BT;
   CUtensorMap m[6];
   const uint64_t rb = (uint64_t)s.d * 2;
   const uint64_t routed = (uint64_t)s.T * s.K_r;
-  bool ok = make_tmap_2d(&m[0], kBF16, x_perm, s.d, routed, rb, BK, BT) &&
-            make_tmap_2d(&m[1], kBF16, u, s.d, s.T, rb, BK, BT) &&
-            make_tmap_2d(&m[2], kBF16, w->gate, s.d, (uint64_t)s.N_r * s.I, rb, BK, BF) &&
-            make_tmap_2d(&m[3], kBF16, w->up, s.d, (uint64_t)s.N_r * s.I, rb, BK, BF);
+  // tokens: 128-row boxes (a CTA's half of a 256-token tile); weights: 64-row boxes
+  bool ok = make_tmap_2d(&m[0], kBF16, x_perm, s.d, routed, rb, BK, BT / 2) &&
+            make_tmap_2d(&m[1], kBF16, u, s.d, s.T, rb, BK, BT / 2) &&
+            make_tmap_2d(&m[2], kBF16, w->gate, s.d, (uint64_t)s.N_r * s.I, rb, BK, 64) &&
+            make_tmap_2d(&m[3], kBF16, w->up, s.d, (uint64_t)s.N_r * s.I, rb, BK, 64);
   if (ok && s.N_s > 0) {
-    ok = make_tmap_2d(&m[4], kBF16, w->s_gate, s.d, (uint64_t)s.N_s * s.I, rb, BK, BF) &&
-         make_tmap_2d(&m[5], kBF16, w->s_up, s.d, (uint64_t)s.N_s * s.I, rb, BK, BF);
+    ok = make_tmap_2d(&m[4], kBF16, w->s_gate, s.d, (uint64_t)s.N_s * s.I, rb, BK, 64) &&
+         make_tmap_2d(&m[5], kBF16, w->s_up, s.d, (uint64_t)s.N_s * s.I, rb, BK, 64);
   } else {
     m[4] = m[2];
     m[5] = m[3];
@@ -304,14 +402,13 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
 cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h, const int32_t* expert_offset,
                                const moe_expert_weights* w, void* y, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
-  constexpr int BT = Tiles<1>::BT;
   CUtensorMap m[6];
   const uint64_t rb = (uint64_t)s.I * 2;
   const uint64_t rows = (uint64_t)s.T * s.K_r + (uint64_t)s.N_s * s.T;
-  bool ok = make_tmap_2d(&m[0], kBF16, h, s.I, rows, rb, BK, BT) &&
-            make_tmap_2d(&m[2], kBF16, w->down, s.I, (uint64_t)s.N_r * s.d, rb, BK, BF);
+  bool ok = make_tmap_2d(&m[0], kBF16, h, s.I, rows, rb, BK, BT / 2) &&
+            make_tmap_2d(&m[2], kBF16, w->down, s.I, (uint64_t)s.N_r * s.d, rb, BK, 128);
   if (ok && s.N_s > 0)
-    ok = make_tmap_2d(&m[4], kBF16, w->s_down, s.I, (uint64_t)s.N_s * s.d, rb, BK, BF);
+    ok = make_tmap_2d(&m[4], kBF16, w->s_down, s.I, (uint64_t)s.N_s * s.d, rb, BK, 128);
   else
     m[4] = m[2];
   if (!ok) return cudaErrorInvalidValue;
