@@ -335,11 +335,14 @@ class MoELayer:
         self.ws_dispatch = _workspace(dispatch_workspace_bytes(self.shape), dev)
 
     def step(self, u: torch.Tensor, seq_offsets: torch.Tensor, update_bias: bool = True,
-             events: Optional[list] = None, stream=None) -> torch.Tensor:
+             events: Optional[list] = None, stream=None,
+             out: Optional[torch.Tensor] = None) -> torch.Tensor:
         """Forward pass h' for the tokens u; then b <- b + gamma*sign(mean - load) and the
         per-sequence statistic.  ``events`` (optional list of 6 CUDA events) are recorded
-        between the stages for per-stage timing (6 events)."""
+        between the stages for per-stage timing (6 events).  h' goes to ``out`` (same
+        shape and dtype as ``self.out``) when given, else to ``self.out``."""
         sh = self.shape
+        out = self.out if out is None else out
         ev = (lambda i: events[i].record(stream)) if events else (lambda i: None)
         ev(0)
         route(u, self.e, self.b, sh, self.topk_idx, self.topk_gate, self.s_out, seq_offsets,
@@ -367,13 +370,59 @@ class MoELayer:
             expert_down(self.h_mid, self.expert_offset, sh, self.ffn_weights, self.y,
                         stream=stream)
         ev(4)
-        combine(u, self.y, self.topk_gate, self.inv_row, sh, self.out, stream=stream)
+        combine(u, self.y, self.topk_gate, self.inv_row, sh, out, stream=stream)
         if update_bias:
             bias_update(self.b, self.load, sh, self.gamma, stream=stream)
         seq_balance_stat(self.seq_p_sum, self.topk_idx, seq_offsets, self.n_seq, sh, self.alpha,
                          self.stat, self.stat_mean, stream=stream)
         ev(5)
-        return self.out
+        return out
+
+    def pipeline(self, u_host: list, out_host: list, seq_offsets: torch.Tensor,
+                 load_host: Optional[list] = None, stat_host: Optional[list] = None) -> None:
+        """Run one step per host batch: u_host[k] (pinned, [T, d]) in, h' to out_host[k]
+        (pinned, like ``self.out``), optionally the loads and per-sequence statistics to
+        load_host[k] / stat_host[k].  Three streams overlap the copy-in of batch k+1 and
+        the copy-out of batch k-1 with the compute of batch k; the device holds two
+        input and two output buffers.  Enqueues everything on the current stream and
+        two side streams and returns; the current stream waits for the last copy-out,
+        so synchronising it (or the device) completes the run."""
+        comp = torch.cuda.current_stream()
+        dev = self.e.device
+        if not hasattr(self, "_pipe"):
+            self._pipe = dict(
+                s_in=torch.cuda.Stream(device=dev), s_out=torch.cuda.Stream(device=dev),
+                u=[torch.empty(u_host[0].shape, dtype=u_host[0].dtype, device=dev)
+                   for _ in range(2)],
+                out=[self.out, torch.empty_like(self.out)])
+        P = self._pipe
+        s_in, s_out = P["s_in"], P["s_out"]
+        ev = lambda: torch.cuda.Event()
+        in_ready, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        s_in.wait_stream(comp)
+        s_out.wait_stream(comp)
+        for k in range(len(u_host)):
+            slot = k & 1
+            with torch.cuda.stream(s_in):
+                if k >= 2:   # the compute of batch k-2 has finished reading this buffer
+                    s_in.wait_event(comp_done[slot])
+                P["u"][slot].copy_(u_host[k], non_blocking=True)
+                in_ready[slot].record(s_in)
+            comp.wait_event(in_ready[slot])
+            if k >= 2:       # the copy-out of batch k-2 has finished reading this buffer
+                comp.wait_event(out_done[slot])
+            self.step(P["u"][slot], seq_offsets, out=P["out"][slot], stream=comp)
+            if load_host is not None:
+                load_host[k].copy_(self.load, non_blocking=True)
+            if stat_host is not None:
+                stat_host[k].copy_(self.stat, non_blocking=True)
+            comp_done[slot].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[slot])
+                out_host[k].copy_(P["out"][slot], non_blocking=True)
+                out_done[slot].record(s_out)
+        comp.wait_stream(s_out)
+        comp.wait_stream(s_in)
 
     def capture(self, u: torch.Tensor, seq_offsets: torch.Tensor, steps: int = 1,
                 events: Optional[list] = None, pre=None, post=None) -> "torch.cuda.CUDAGraph":

@@ -22,26 +22,33 @@ __global__ void bias_update_kernel(float* __restrict__ b, const int32_t* __restr
   b[i] = __fadd_rn(b[i], step);
 }
 
-// alpha * sum_i f_i P_i per sequence (pwwt.cn notes §1.2), one block per sequence: an
-// integer histogram of the experts selected in the sequence, then a fixed-order fp64
-// tree sum.  f_i = N_r/(K_r*T_j) * count_i, P_i = seq_p_sum[j, i] / T_j.
-__global__ void __launch_bounds__(256) seq_stat_kernel(const float* __restrict__ seq_p_sum,
-                                                       const int32_t* __restrict__ topk_idx,
-                                                       const int32_t* __restrict__ seq_offsets,
-                                                       int N_r, int K_r, float alpha,
-                                                       float* __restrict__ stat_per_seq) {
+// alpha * sum_i f_i P_i per sequence (pwwt.cn notes §1.2), one block of 1024 threads
+// per sequence: an integer histogram of the experts selected in the sequence (lanes
+// holding the same expert add once, by match_any), then a fixed-order fp64 tree sum.
+// f_i = N_r/(K_r*T_j) * count_i, P_i = seq_p_sum[j, i] / T_j.
+__global__ void __launch_bounds__(1024) seq_stat_kernel(const float* __restrict__ seq_p_sum,
+                                                        const int32_t* __restrict__ topk_idx,
+                                                        const int32_t* __restrict__ seq_offsets,
+                                                        int N_r, int K_r, float alpha,
+                                                        float* __restrict__ stat_per_seq) {
   __shared__ int32_t cnt[256];
   __shared__ double term[256];
-  const int j = blockIdx.x;
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) cnt[i] = 0;
+  const int j = blockIdx.x, lane = threadIdx.x & 31;
+  if (threadIdx.x < 256) cnt[threadIdx.x] = 0;
   __syncthreads();
   const int a = seq_offsets[j], z = seq_offsets[j + 1];
   const long long n_ent = (long long)(z - a) * K_r;
   const int32_t* src = topk_idx + (size_t)a * K_r;
-  for (long long x = threadIdx.x; x < n_ent; x += blockDim.x) atomicAdd(&cnt[src[x]], 1);
+  for (long long x0 = 0; x0 < n_ent; x0 += blockDim.x) {   // every lane runs every round
+    const long long x = x0 + threadIdx.x;
+    const int ex = x < n_ent ? __ldg(src + x) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, ex);
+    if (ex >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[ex], __popc(peers));
+  }
   __syncthreads();
   const int T_j = z - a;
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+  if (threadIdx.x < 256) {
+    const int i = threadIdx.x;
     double v = 0.0;
     if (i < N_r && T_j > 0) {
       const double f = (double)N_r / ((double)K_r * T_j) * (double)cnt[i];
@@ -95,7 +102,7 @@ cudaError_t launch_seq_stat(const float* seq_p_sum, const int32_t* topk_idx,
                             const int32_t* seq_offsets, int n_seq, int N_r, int K_r,
                             float alpha, float* stat_per_seq, float* stat_mean,
                             cudaStream_t st) {
-  seq_stat_kernel<<<n_seq, 256, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, N_r, K_r, alpha,
+  seq_stat_kernel<<<n_seq, 1024, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, N_r, K_r, alpha,
                                          stat_per_seq);
   if (stat_mean) seq_mean_kernel<<<1, 1, 0, st>>>(stat_per_seq, n_seq, stat_mean);
   return cudaGetLastError();

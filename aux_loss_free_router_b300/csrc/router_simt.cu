@@ -302,31 +302,34 @@ inline bool warp_select_ok(int N_r, int K_r, int G, int M) {
 }
 
 // out[j, i] = sum over the P-sum windows' run sums of sequence j: the run starting at
-// the sequence's first token and one at every window start inside the sequence, in
-// token order, accumulated in fp64.
+// the sequence's first token and one at every window start inside the sequence.  A
+// block takes one sequence and 32 experts (lane = expert); its 8 warps take every 8th
+// run, accumulate in fp64, and the 8 partial sums are added in warp order.
 __global__ void __launch_bounds__(256) seq_psum_kernel(const float* __restrict__ pwin,
                                                        const int32_t* __restrict__ seq_offsets,
                                                        int N_r, float* __restrict__ out) {
-  const int j = blockIdx.x, i = blockIdx.y * blockDim.x + threadIdx.x;
-  if (i >= N_r) return;
+  __shared__ double part[8][32];
+  const int j = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.y * 32 + lane;
   const int a = seq_offsets[j], z = seq_offsets[j + 1];
   double acc = 0.0;
-  if (a < z) {
-    acc = (double)pwin[(size_t)a * N_r + i];
-    int w = (a / kPWindow + 1) * kPWindow;
-    for (; w + 3 * kPWindow < z; w += 4 * kPWindow) {
-      const float v0 = pwin[(size_t)w * N_r + i];
-      const float v1 = pwin[(size_t)(w + kPWindow) * N_r + i];
-      const float v2 = pwin[(size_t)(w + 2 * kPWindow) * N_r + i];
-      const float v3 = pwin[(size_t)(w + 3 * kPWindow) * N_r + i];
-      acc += (double)v0;
-      acc += (double)v1;
-      acc += (double)v2;
-      acc += (double)v3;
+  if (i < N_r && a < z) {
+    // run r = 0 starts at a; run r >= 1 at the r-th window start after a
+    const int w1 = (a / kPWindow + 1) * kPWindow;
+    const int n_runs = 1 + (z > w1 ? (z - w1 + kPWindow - 1) / kPWindow : 0);
+    for (int r = warp; r < n_runs; r += 8) {
+      const int t = r == 0 ? a : w1 + (r - 1) * kPWindow;
+      acc += (double)__ldg(pwin + (size_t)t * N_r + i);
     }
-    for (; w < z; w += kPWindow) acc += (double)pwin[(size_t)w * N_r + i];
   }
-  out[(size_t)j * N_r + i] = (float)acc;
+  part[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && i < N_r) {
+    double s = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += part[w][lane];
+    out[(size_t)j * N_r + i] = (float)s;
+  }
 }
 
 }  // namespace
@@ -367,7 +370,7 @@ cudaError_t launch_router_select(const float* z_part, int S, const float* b, con
 cudaError_t launch_seq_psum(const float* pwin, const int32_t* seq_offsets, int n_seq, int N_r,
                             float* out, cudaStream_t st) {
   if (n_seq == 0) return cudaSuccess;
-  const dim3 grid(n_seq, (N_r + 255) / 256);
+  const dim3 grid(n_seq, (N_r + 31) / 32);
   seq_psum_kernel<<<grid, 256, 0, st>>>(pwin, seq_offsets, N_r, out);
   return cudaGetLastError();
 }

@@ -200,3 +200,34 @@ def test_decode_sized_pass():
     r = run_layer(cfg)
     idx, _ = check_routing(cfg, r)
     check_output_full(cfg, r, rel_tol=BF16_REL, abs_tol=BF16_ABS, abs_per_rms=True)
+
+
+def test_pipelined_host_batches_match_steps():
+    """MoELayer.pipeline (copies overlapped with compute on three streams) gives, batch
+    by batch, exactly what step() gives on the same batches in the same order."""
+    cfg = synth.config("mid", T=512, n_seq=2)
+    x = synth.make_inputs(cfg, device="cuda")
+    w = {k: x[k] for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")}
+    batches = [synth.make_inputs(cfg, device="cuda", u_seed=50 + k, with_weights=False)["u"]
+               for k in range(5)]
+
+    def layer():
+        return moe.MoELayer(T=cfg.T, d=cfg.d, N_r=cfg.N_r, K_r=cfg.K_r, N_s=cfg.N_s, I=cfg.I,
+                            G=cfg.G, M=cfg.M, e=x["e"], b=x["b"].clone(), weights=w,
+                            n_seq=cfg.n_seq, gamma=0.01)
+
+    ref = layer()
+    want, want_load = [], []
+    for u in batches:
+        want.append(ref.step(u, x["seq_offsets"]).clone())
+        want_load.append(ref.load.clone())
+    lay = layer()
+    u_host = [u.cpu().pin_memory() for u in batches]
+    out_host = [torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory() for _ in batches]
+    load_host = [torch.empty(cfg.N_r, dtype=torch.int32).pin_memory() for _ in batches]
+    lay.pipeline(u_host, out_host, x["seq_offsets"], load_host)
+    torch.cuda.synchronize()
+    for k in range(len(batches)):
+        assert torch.equal(out_host[k], want[k].cpu()), k
+        assert torch.equal(load_host[k], want_load[k].cpu()), k
+    assert torch.equal(lay.b, ref.b)
