@@ -87,3 +87,42 @@ def test_combine_v3_shape_sampled():
         for k in range(K_r):
             ref = ref + float(gate[t, k]) * to_np(y[int(inv[t, k])]).astype(np.float64)
         np.testing.assert_allclose(to_np(out[t]), ref, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("N_r,K_r,G,M,T,d,n_seq", [
+    (64, 4, 2, 2, 700, 256, 7),      # two groups of 32, top-2 per group; 100-token sequences
+    (128, 8, 4, 4, 333, 512, 3),     # four groups of 32
+    (128, 6, 4, 3, 257, 256, 1),
+    (256, 8, 8, 8, 129, 384, 3),     # eight groups, one key each
+    (256, 8, 1, 1, 96, 256, 3),      # no group limit; sequences of one window
+    (64, 1, 1, 1, 50, 128, 5),       # K_r = 1; sequences shorter than a window
+])
+def test_router_shapes_bit_exact(N_r, K_r, G, M, T, d, n_seq):
+    cfg = synth.MoEConfig("route", T=T, d=d, N_r=N_r, K_r=K_r, N_s=0, I=128, G=G, M=M,
+                          dtype="bf16", bias="uniform", seed=N_r + T, n_seq=n_seq)
+    x = synth.make_inputs(cfg, device="cuda", with_weights=False)
+    sh, idx, gate, s, psum = _route(cfg, x)
+    s_np, b = to_np(s), to_np(x["b"])
+    idx_ref = oracle.select_experts(s_np, b, K_r, G, M)
+    np.testing.assert_array_equal(to_np(idx), idx_ref)
+    np.testing.assert_allclose(to_np(gate), oracle.gate_values(s_np, idx_ref), rtol=1e-6)
+    np.testing.assert_allclose(to_np(psum), oracle.seq_p_sums(s_np, to_np(x["seq_offsets"])),
+                               rtol=1e-5)
+
+
+@pytest.mark.parametrize("N_r,K_r,G,M", [(256, 8, 8, 4), (64, 6, 1, 1), (128, 8, 4, 2)])
+def test_router_exact_ties_go_to_lower_index(N_r, K_r, G, M):
+    """Zero centroids give s = 0.5 for every expert, and biases repeat in steps of three,
+    so most keys (and group scores) tie exactly: the lower index must win each tie."""
+    T, d = 200, 256
+    cfg = synth.MoEConfig("ties", T=T, d=d, N_r=N_r, K_r=K_r, N_s=0, I=128, G=G, M=M,
+                          dtype="bf16", bias="zero", seed=1, n_seq=1)
+    x = synth.make_inputs(cfg, device="cuda", with_weights=False)
+    x["e"].zero_()
+    x["b"].copy_(torch.tensor([(i % 3) * 0.25 for i in range(N_r)], device="cuda"))
+    sh, idx, gate, s, psum = _route(cfg, x)
+    s_np, b = to_np(s), to_np(x["b"])
+    assert (s_np == 0.5).all()
+    idx_ref = oracle.select_experts(s_np, b, K_r, G, M)
+    np.testing.assert_array_equal(to_np(idx), idx_ref)
+    np.testing.assert_allclose(to_np(gate), np.full((T, K_r), 1.0 / K_r), rtol=1e-6)
