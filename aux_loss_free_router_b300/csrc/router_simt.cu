@@ -410,11 +410,11 @@ __global__ void __launch_bounds__(256, 2) router_select_oct_kernel(const float* 
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, o));
     if (valid) {
+      const float inv = __frcp_rn(rs);
 #pragma unroll
       for (int q = 0; q < Q; ++q)
         *reinterpret_cast<float4*>(&sp_tile[tl][32 * q + 4 * part]) =
-            make_float4(__fdiv_rn(sv[q][0], rs), __fdiv_rn(sv[q][1], rs), __fdiv_rn(sv[q][2], rs),
-                        __fdiv_rn(sv[q][3], rs));
+            make_float4(sv[q][0] * inv, sv[q][1] * inv, sv[q][2] * inv, sv[q][3] * inv);
     }
   }
 
