@@ -41,9 +41,10 @@ import synth  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s at d=7168, 256e top-8; tensor-pipe & HBM % of peak"
 
-# ncu DRAM traffic (read + write bytes) of one gate/up GEMM launch at this workload,
-# valid only for the kernel source with this hash (null otherwise).
-NCU_TRAFFIC = {"kernel_src_sha": None, "bytes": None}
+# ncu DRAM traffic (read + write bytes) of one gate/up GEMM launch at the V3-shaped
+# workload (dram__bytes_read.sum 20.32 GB + dram__bytes_write.sum 0.30 GB, one-pass
+# capture of the full-size bench), valid only for the kernel source with this hash.
+NCU_TRAFFIC = {"kernel_src_sha": "7c13ab41a5dd790a", "bytes": 20.32e9 + 0.3014e9}
 
 
 def log(*a):
@@ -355,7 +356,8 @@ def run_ours(args, cfg, ws, rank, local):
         peak *= 2.0
         peak_source += " x 2 (nominal E4M3/bf16 ratio)"
     sha = kernel_src_sha()
-    traffic = NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["kernel_src_sha"] == sha else None
+    traffic = (NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["kernel_src_sha"] == sha and cfg.name == "v3"
+               and not cfg.fp8 else None)
     tok_s = cfg.T * ws / (ms / 1e3)
     kernels = {
         "route": {"ms": stages["route"], "GB/s": wk["router_bytes"] / (stages["route"] / 1e3) / 1e9,
