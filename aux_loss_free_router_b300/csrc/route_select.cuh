@@ -233,10 +233,10 @@ inline bool fast_select_ok(int N_r, int K_r, int G, int M) {
   return per % 32 == 0 && G <= kFastG && K_r / M <= 2;
 }
 
-// 1 / (1 + e^-z) from the fast exponential and the correctly rounded reciprocal
-// (absolute error about 1e-7, well inside the affinity tolerances).
+// 1 / (1 + e^-z) from the fast exponential and the fast reciprocal (absolute error
+// about 1e-7, well inside the affinity tolerances).
 __device__ __forceinline__ float sigmoid_f32(float z) {
-  return __frcp_rn(__fadd_rn(1.f, __expf(-z)));
+  return __fdividef(1.f, __fadd_rn(1.f, __expf(-z)));
 }
 
 }  // namespace moe

@@ -418,10 +418,12 @@ __global__ void __launch_bounds__(256, 2) router_select_oct_kernel(const float* 
     }
   }
 
-  // group limit: bit q of `keep` marks an eligible 32-expert block
+  // group limit: bit q of `keep` marks an eligible 32-expert block (G divides Q and both
+// are powers of two)
   unsigned keep = (1u << Q) - 1u;
   if (p.G > 1) {
-    const int G = p.G, bq = Q / G, kg = p.K_r / p.M;
+    const int G = p.G, kg = p.K_r / p.M;
+    const int gsh = __ffs(Q / G) - 1;   // blocks per group = Q/G, a power of two: shift, not divide
     float b1[Q], b2[Q];                 // each block's two best keys over the token
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(256, 2) router_select_oct_kernel(const float* 
         float t1 = -CUDART_INF_F, t2 = -CUDART_INF_F;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-          if (q / bq == g) {
+          if ((q >> gsh) == g) {
             const float lo = fminf(t1, b1[q]);
             t1 = fmaxf(t1, b1[q]);
             t2 = fmaxf(fmaxf(t2, b2[q]), lo);
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(256, 2) router_select_oct_kernel(const float* 
     keep = 0;
 #pragma unroll
     for (int q = 0; q < Q; ++q)
-      if ((gkeep >> (q / bq)) & 1u) keep |= 1u << q;
+      if ((gkeep >> (q >> gsh)) & 1u) keep |= 1u << q;
   }
 
   Top8 L;
