@@ -43,6 +43,7 @@ constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 16;
+constexpr int kLoadGroup = 8;   // TMEM columns loaded per wait in the promotion
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 
 struct Ctrl {
@@ -250,27 +251,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!__all_sync(0xffffffffu, got)) { alive = false; break; }
         tc::fence_after_sync();
         const uint32_t t_base = tmem_base + (uint32_t)(buf * BN) + ((uint32_t)(q * 32) << 16);
+        // this thread's 64 columns: MODE 0 gate cq*32.. and up 128+cq*32.., MODE 1
+        // cq*64..; loaded kLoadGroup at a time per wait
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          int col;
-          float sc;
-          if (MODE == 0) {   // parts 0,1: gate columns; 2,3: the same up columns
-            col = (part < 2 ? 0 : BN / 2) + cq * 32 + (part & 1) * 16;
-            sc = sa * (part < 2 ? sb0 : sb1);
-          } else {
-            col = cq * 64 + part * 16;
-            sc = sa * sb0;
+        for (int g0 = 0; g0 < 64; g0 += kLoadGroup) {
+          uint32_t pv[kLoadGroup];
+#pragma unroll
+          for (int x = 0; x < kLoadGroup; x += 8) {
+            const int c = g0 + x;
+            const int col = MODE == 0 ? (c < 32 ? cq * 32 + c : BN / 2 + cq * 32 + (c - 32))
+                                      : cq * 64 + c;
+            tc::tmem_ld8(t_base + col, *reinterpret_cast<uint32_t(*)[8]>(&pv[x]));
           }
+          tc::tmem_ld_wait();
 #pragma unroll
-          for (int h8 = 0; h8 < 2; ++h8) {
-            uint32_t p[8];
-            tc::tmem_ld8(t_base + col + h8 * 8, p);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int a = part * 16 + h8 * 8 + j;
-              acc[a] = fmaf(__uint_as_float(p[j]), sc, acc[a]);
-            }
+          for (int j = 0; j < kLoadGroup; ++j) {
+            const int c = g0 + j;
+            const float sc = sa * (MODE == 0 && c >= 32 ? sb1 : sb0);
+            acc[c] = fmaf(__uint_as_float(pv[j]), sc, acc[c]);
           }
         }
         tc::fence_before_sync();

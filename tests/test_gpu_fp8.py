@@ -95,3 +95,31 @@ def test_fp8_layer_is_deterministic():
     r1 = run_layer(cfg, {k: v.clone() for k, v in x.items()})
     r2 = run_layer(cfg, {k: v.clone() for k, v in x.items()})
     np.testing.assert_array_equal(r1["h"], r2["h"])
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_expert_ffn_call_equals_the_two_step_calls(fp8):
+    """moe_expert_ffn (h in its workspace; for E4M3 also h's scales) gives the same y as
+    moe_expert_gate_up followed by moe_expert_down."""
+    cfg = synth.config("fp8" if fp8 else "mid", T=512, n_seq=1)
+    r = run_layer(cfg)
+    lay, x = r["layer"], r["inputs"]
+    xin = lay.u_q if fp8 else x["u"]
+    kw = dict(x_perm_scale=lay.x_perm_scale, u_scale=lay.u_scale) if fp8 else {}
+    y = torch.empty_like(lay.y)
+    moe.expert_ffn(lay.x_perm, xin, lay.expert_offset, lay.shape, lay.ffn_weights, y, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y, lay.y)
+
+
+def test_quantize_fp32_input_bit_exact():
+    g = torch.Generator(device="cuda").manual_seed(13)
+    x = torch.randn(64, 384, device="cuda", generator=g) * 10.0
+    q = torch.empty(64, 384, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(64, 3, dtype=torch.float32, device="cuda")
+    moe.quantize_e4m3(x, 1, q, sc)
+    torch.cuda.synchronize()
+    ref_q, ref_sc = ofp8.quantize_1x128(to_np(x))
+    np.testing.assert_array_equal(to_np(sc), ref_sc)
+    np.testing.assert_array_equal(_codes_to_values(q), ref_q)
+

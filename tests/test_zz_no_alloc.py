@@ -19,6 +19,7 @@ import torch
 import synth
 import aux_loss_free_router_b300 as moe
 from aux_loss_free_router_b300 import build as moe_build
+from tests.layer_harness import run_layer
 
 
 def _routing(rng, T, N_r, K_r, conc):
@@ -68,3 +69,28 @@ def test_noalloc_dispatch_rejects_batches_beyond_its_scratch():
     code = lib.moe_dispatch_noalloc(fake, sh, None, moe.BF16, None, fake, fake, fake, fake,
                                     None, None, None)
     assert code == 1
+
+
+@pytest.mark.gpu
+def test_noalloc_dispatch_gathers_e4m3_rows_and_scales():
+    """The allocation-free dispatch on E4M3 tokens: codes and their 1x128 scales are
+    gathered exactly like the workspace dispatch does."""
+    cfg = synth.config("fp8", T=1024, n_seq=1)
+    r = run_layer(cfg)
+    lay = r["layer"]
+    dev = "cuda"
+    sh = lay.shape
+    out = []
+    for fn in (moe.dispatch, moe.dispatch_noalloc):
+        load = torch.empty(cfg.N_r, dtype=torch.int32, device=dev)
+        off = torch.empty(cfg.N_r + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(cfg.T * cfg.K_r, dtype=torch.int32, device=dev)
+        inv = torch.empty(cfg.T, cfg.K_r, dtype=torch.int32, device=dev)
+        xp = torch.empty_like(lay.x_perm)
+        xs = torch.empty_like(lay.x_perm_scale)
+        fn(lay.topk_idx, sh, load, off, perm, inv, lay.u_q, xp, lay.u_scale, xs)
+        torch.cuda.synchronize()
+        out.append((load, off, perm, inv, xp, xs))
+    for a, b in zip(*out):
+        assert torch.equal(a, b)
+    assert torch.equal(out[0][4], lay.x_perm) and torch.equal(out[0][5], lay.x_perm_scale)
