@@ -48,6 +48,7 @@ namespace moe {
 namespace {
 
 constexpr int BK = 64, STAGES = 6, BT = 256;
+constexpr int SMALL_ROWS = 32;                  // token box of tiles with <= 64 tokens
 constexpr int A_BYTES = 128 * BK * 2;           // this CTA's 128 weight rows
 constexpr int B_BYTES = (BT / 2) * BK * 2;      // this CTA's half of the token rows
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_ffn_kernel(const __grid_constant__ CUtensorMap mX_r, const __grid_constant__ CUtensorMap mX_s,
                   const __grid_constant__ CUtensorMap mW0_r, const __grid_constant__ CUtensorMap mW1_r,
                   const __grid_constant__ CUtensorMap mW0_s, const __grid_constant__ CUtensorMap mW1_s,
+                  const __grid_constant__ CUtensorMap mXs_r, const __grid_constant__ CUtensorMap mXs_s,
                   TcArgs args) {
   constexpr int FEAT = Pair<MODE>::FEAT;
   extern __shared__ uint8_t smem_raw[];
@@ -175,7 +177,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int e = shared ? tcd.seg - s.N_r : tcd.seg;
         const int n_tok = min(BT, tcd.rows - tcd.m * BT);
         const int half = ((n_tok + 15) & ~15) >> 1;     // token rows per CTA
-        const CUtensorMap* mX = (MODE == 0 && shared) ? &mX_s : &mX_r;
+        // a tile of <= 64 tokens loads 32-row token boxes (decode-sized batches)
+        const bool small = half <= SMALL_ROWS;
+        const CUtensorMap* mX = (MODE == 0 && shared) ? (small ? &mXs_s : &mX_s)
+                                                      : (small ? &mXs_r : &mX_r);
+        const uint32_t stage_tx = (uint32_t)(A_BYTES + (small ? SMALL_ROWS : BT / 2) * BK * 2);
         const int x_row = (MODE == 0 ? (shared ? 0 : tcd.row0) : tcd.out_row0) + tcd.m * BT +
                           (int)rank * half;
         const CUtensorMap* mW0 = shared ? &mW0_s : &mW0_r;
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t ph = (it / STAGES) & 1;
           if (!tc::mbar_wait(&C.empty[st], ph ^ 1, abort_flag, args.err)) { ok = false; break; }
           const uint32_t bar = tc::cluster_addr(&C.full[st], 0);   // the even CTA's barrier
-          if (leader) tc::mbar_arrive_expect_tx(&C.full[st], 2 * STAGE_BYTES);
+          if (leader) tc::mbar_arrive_expect_tx(&C.full[st], 2 * stage_tx);
           uint8_t* sa = base + st * STAGE_BYTES;
           if (MODE == 0) {
             tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);                 // 64 gate rows
@@ -367,7 +373,8 @@ cudaError_t launch(const FfnShape& s, const CUtensorMap* maps, const int32_t* of
   const int pairs = (int)std::min<long long>(fit, std::max<long long>(1, tiles_ub));
   cfg.gridDim = dim3(2 * pairs);
   TcArgs a{s, off, static_cast<__nv_bfloat16*>(out), dev_error_ptr()};
-  err = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+  err = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
+                           maps[7], a);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -380,12 +387,15 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
                              const int32_t* expert_offset, const moe_expert_weights* w, void* h,
                              cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
-  CUtensorMap m[6];
+  CUtensorMap m[8];
   const uint64_t rb = (uint64_t)s.d * 2;
   const uint64_t routed = (uint64_t)s.T * s.K_r;
-  // tokens: 128-row boxes (a CTA's half of a 256-token tile); weights: 64-row boxes
+  // tokens: 128-row boxes (a CTA's half of a 256-token tile) and 32-row boxes (tiles of
+  // <= 64 tokens); weights: 64-row boxes
   bool ok = make_tmap_2d(&m[0], kBF16, x_perm, s.d, routed, rb, BK, BT / 2) &&
             make_tmap_2d(&m[1], kBF16, u, s.d, s.T, rb, BK, BT / 2) &&
+            make_tmap_2d(&m[6], kBF16, x_perm, s.d, routed, rb, BK, SMALL_ROWS) &&
+            make_tmap_2d(&m[7], kBF16, u, s.d, s.T, rb, BK, SMALL_ROWS) &&
             make_tmap_2d(&m[2], kBF16, w->gate, s.d, (uint64_t)s.N_r * s.I, rb, BK, 64) &&
             make_tmap_2d(&m[3], kBF16, w->up, s.d, (uint64_t)s.N_r * s.I, rb, BK, 64);
   if (ok && s.N_s > 0) {
@@ -402,10 +412,11 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
 cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h, const int32_t* expert_offset,
                                const moe_expert_weights* w, void* y, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
-  CUtensorMap m[6];
+  CUtensorMap m[8];
   const uint64_t rb = (uint64_t)s.I * 2;
   const uint64_t rows = (uint64_t)s.T * s.K_r + (uint64_t)s.N_s * s.T;
   bool ok = make_tmap_2d(&m[0], kBF16, h, s.I, rows, rb, BK, BT / 2) &&
+            make_tmap_2d(&m[6], kBF16, h, s.I, rows, rb, BK, SMALL_ROWS) &&
             make_tmap_2d(&m[2], kBF16, w->down, s.I, (uint64_t)s.N_r * s.d, rb, BK, 128);
   if (ok && s.N_s > 0)
     ok = make_tmap_2d(&m[4], kBF16, w->s_down, s.I, (uint64_t)s.N_s * s.d, rb, BK, 128);
@@ -415,6 +426,7 @@ cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h, const int32_t* 
   m[1] = m[0];
   m[3] = m[2];
   m[5] = m[4];
+  m[7] = m[6];
   return launch<1>(s, m, expert_offset, y, st);
 }
 
