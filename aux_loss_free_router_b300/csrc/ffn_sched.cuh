@@ -18,6 +18,7 @@ struct SegTable {
   int row0[kMaxSegs];        // first input row of the segment
   int rows[kMaxSegs];        // rows in the segment (0..T)
   int mt[kMaxSegs];          // m-tiles in the segment
+  int q[kMaxSegs];           // rows per m-tile (the last one may have fewer)
 };
 
 struct TileCoord {
@@ -25,12 +26,17 @@ struct TileCoord {
   int row0;      // first input row (x_perm row for routed, u row 0 for shared)
   int rows;      // rows in the segment
   int out_row0;  // first row in the FFN row space [T*K_r + N_s*T]
+  int tok0;      // first row of this tile within the segment (m * q)
+  int n_tok;     // rows of this tile
 };
 
-// All threads of the block call this; the caller synchronises afterwards.
+// All threads of the block call this; the caller synchronises afterwards.  With
+// `balanced` a segment's rows are cut into ceil(rows/BM) tiles of equal size rounded up
+// to 16 (at most BM), so that the tiles of one segment take the same time; otherwise
+// into tiles of exactly BM rows.
 __device__ __forceinline__ void build_seg_table(SegTable& tab, const int32_t* __restrict__ off,
                                                 int T, int K_r, int N_r, int N_s, int BM,
-                                                int n_tiles_n) {
+                                                int n_tiles_n, bool balanced = false) {
   const int nseg = N_r + N_s;
   for (int i = threadIdx.x; i < nseg; i += blockDim.x) {
     int r0 = 0, rows = T;
@@ -40,7 +46,9 @@ __device__ __forceinline__ void build_seg_table(SegTable& tab, const int32_t* __
     }
     tab.row0[i] = r0;
     tab.rows[i] = rows;
-    tab.mt[i] = (rows + BM - 1) / BM;
+    const int mt = (rows + BM - 1) / BM;
+    tab.mt[i] = mt;
+    tab.q[i] = (balanced && mt > 0) ? min(BM, (((rows + mt - 1) / mt) + 15) & ~15) : BM;
   }
   __syncthreads();
   if (threadIdx.x < 32) {
@@ -92,6 +100,8 @@ __device__ __forceinline__ TileCoord decode_tile(const SegTable& tab, int tile, 
   c.row0 = tab.row0[lo];
   c.rows = tab.rows[lo];
   c.out_row0 = lo < tab.N_r ? c.row0 : tab.T * tab.K_r + (lo - tab.N_r) * tab.T;
+  c.tok0 = c.m * tab.q[lo];
+  c.n_tok = min(tab.q[lo], c.rows - c.tok0);
   return c;
 }
 

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tmem_alloc_pair(&C.tmem_base, TMEM_COLS);
     tc::tmem_relinquish_pair();
   }
-  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BT, n_ft);
+  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BT, n_ft, true);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -175,14 +175,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
         const bool shared = tcd.seg >= s.N_r;
         const int e = shared ? tcd.seg - s.N_r : tcd.seg;
-        const int n_tok = min(BT, tcd.rows - tcd.m * BT);
+        const int n_tok = tcd.n_tok;
         const int half = ((n_tok + 15) & ~15) >> 1;     // token rows per CTA
         // a tile of <= 64 tokens loads 32-row token boxes (decode-sized batches)
         const bool small = half <= SMALL_ROWS;
         const CUtensorMap* mX = (MODE == 0 && shared) ? (small ? &mXs_s : &mX_s)
                                                       : (small ? &mXs_r : &mX_r);
         const uint32_t stage_tx = (uint32_t)(A_BYTES + (small ? SMALL_ROWS : BT / 2) * BK * 2);
-        const int x_row = (MODE == 0 ? (shared ? 0 : tcd.row0) : tcd.out_row0) + tcd.m * BT +
+        const int x_row = (MODE == 0 ? (shared ? 0 : tcd.row0) : tcd.out_row0) + tcd.tok0 +
                           (int)rank * half;
         const CUtensorMap* mW0 = shared ? &mW0_s : &mW0_r;
         const CUtensorMap* mW1 = shared ? &mW1_s : &mW1_r;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int it = 0, tcount = 0;
       for (int tile = pair; tile < total && !*abort_flag; tile += n_pairs, ++tcount) {
         const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
-        const int n_tok = min(BT, tcd.rows - tcd.m * BT);
+        const int n_tok = tcd.n_tok;
         const uint32_t idesc = tc::idesc_bf16(256, (n_tok + 15) & ~15);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
@@ -249,14 +249,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       // warp-uniform decisions: the TMEM loads below are warp-collective
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
-      const int n_tok = min(BT, tcd.rows - tcd.m * BT);
+      const int n_tok = tcd.n_tok;
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       const bool got = tc::mbar_wait(&C.tfull[acc], aph, abort_flag, args.err);
       if (!__all_sync(0xffffffffu, got)) break;
       tc::fence_after_sync();
       const uint32_t t_base = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(q * 32) << 16);
-      const size_t row0 = (size_t)tcd.out_row0 + (size_t)tcd.m * BT;
+      const size_t row0 = (size_t)tcd.out_row0 + (size_t)tcd.tok0;
       bool alive = true;
       if (MODE == 1) {
         const int f0 = tcd.n * FEAT + (int)rank * 128 + q * 32;
