@@ -1,8 +1,9 @@
 // Tile schedule over the variable-size expert segments, built on the device from
 // expert_offset (no host round trip).  Segment i < N_r is routed expert i with
 // rows [expert_offset[i], expert_offset[i+1]); segment N_r + s is shared expert s
-// over all T tokens.  Tiles are numbered segment-major, then n-tile, then m-tile,
-// so CTAs running at the same time share an expert's weight tile through L2.
+// over all T tokens.  Tiles are numbered segment-major, then m-tile (token rows),
+// then n-tile (weight rows), so CTAs running at the same time share a token tile
+// through L2, and a segment's few m-tiles reuse its weight tiles soon after.
 #pragma once
 
 #include "common.cuh"
@@ -94,9 +95,8 @@ __device__ __forceinline__ TileCoord decode_tile(const SegTable& tab, int tile, 
   TileCoord c;
   c.seg = lo;
   const int within = tile - tab.prefix[lo];
-  const int mt = tab.mt[lo];
-  c.n = within / mt;
-  c.m = within - c.n * mt;
+  c.m = within / n_tiles_n;
+  c.n = within - c.m * n_tiles_n;
   c.row0 = tab.row0[lo];
   c.rows = tab.rows[lo];
   c.out_row0 = lo < tab.N_r ? c.row0 : tab.T * tab.K_r + (lo - tab.N_r) * tab.T;

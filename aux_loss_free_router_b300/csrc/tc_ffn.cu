@@ -14,7 +14,7 @@
 // SM, not the tensor pipe, is what bounds these GEMMs.
 //
 // One persistent pair per two SMs walks the tiles of the segment schedule
-// (ffn_sched.cuh): segment-major, then feature tile, then token tile of 256.  Warp
+// (ffn_sched.cuh): segment-major, then token tile (up to 256), then feature tile.  Warp
 // roles in each CTA:
 //   warp 0      TMA producer: this CTA's weight and token rows into a 6-stage ring
 //               (32 KB per stage); completion is counted on the even CTA's barrier.
