@@ -1,6 +1,10 @@
 // End-of-step state: the bias update and the sequence-wise balance statistic.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "launch.h"
+
+namespace cg = cooperative_groups;
 
 namespace moe {
 
@@ -22,48 +26,51 @@ __global__ void bias_update_kernel(float* __restrict__ b, const int32_t* __restr
   b[i] = __fadd_rn(b[i], step);
 }
 
-// alpha * sum_i f_i P_i per sequence (pwwt.cn notes §1.2), one block of 1024 threads
-// per sequence: an integer histogram of the experts selected in the sequence (lanes
-// holding the same expert add once, by match_any), then a fixed-order fp64 tree sum.
-// f_i = N_r/(K_r*T_j) * count_i, P_i = seq_p_sum[j, i] / T_j.
-__global__ void __launch_bounds__(1024) seq_stat_kernel(const float* __restrict__ seq_p_sum,
-                                                        const int32_t* __restrict__ topk_idx,
-                                                        const int32_t* __restrict__ seq_offsets,
-                                                        int N_r, int K_r, float alpha,
-                                                        float* __restrict__ stat_per_seq) {
+// alpha * sum_i f_i P_i per sequence (pwwt.cn notes §1.2).  A cluster of kStatSplit CTAs
+// per sequence: each builds the integer histogram of the experts selected in its slab
+// of the sequence's (token, slot) entries; CTA 0 of the cluster adds the histograms
+// (integers: exact in any order) through distributed shared memory, then forms
+// f_i = N_r/(K_r*T_j) * count_i and P_i = seq_p_sum[j, i] / T_j and sums f_i P_i by a
+// fixed-order fp64 tree.
+constexpr int kStatSplit = 8;
+
+__global__ void __cluster_dims__(kStatSplit, 1, 1) __launch_bounds__(256)
+    seq_stat_kernel(const float* __restrict__ seq_p_sum, const int32_t* __restrict__ topk_idx,
+                    const int32_t* __restrict__ seq_offsets, int N_r, int K_r, float alpha,
+                    float* __restrict__ stat_per_seq) {
   __shared__ int32_t cnt[256];
   __shared__ double term[256];
-  const int j = blockIdx.x, lane = threadIdx.x & 31;
-  if (threadIdx.x < 256) cnt[threadIdx.x] = 0;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int j = blockIdx.x / kStatSplit;
+  cnt[threadIdx.x] = 0;
   __syncthreads();
   const int a = seq_offsets[j], z = seq_offsets[j + 1];
   const long long n_ent = (long long)(z - a) * K_r;
+  const long long slab = (n_ent + kStatSplit - 1) / kStatSplit;
+  const long long x0 = rank * slab, x1 = min(n_ent, x0 + slab);
   const int32_t* src = topk_idx + (size_t)a * K_r;
-  for (long long x0 = 0; x0 < n_ent; x0 += blockDim.x) {   // every lane runs every round
-    const long long x = x0 + threadIdx.x;
-    const int ex = x < n_ent ? __ldg(src + x) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, ex);
-    if (ex >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[ex], __popc(peers));
-  }
-  __syncthreads();
-  const int T_j = z - a;
-  if (threadIdx.x < 256) {
+  for (long long x = x0 + threadIdx.x; x < x1; x += blockDim.x) atomicAdd(&cnt[__ldg(src + x)], 1);
+  cluster.sync();   // every CTA's histogram is complete and visible to the cluster
+  if (rank == 0) {
     const int i = threadIdx.x;
+    int c = 0;
+    for (int r = 0; r < kStatSplit; ++r) c += cluster.map_shared_rank(cnt, r)[i];
+    const int T_j = z - a;
     double v = 0.0;
     if (i < N_r && T_j > 0) {
-      const double f = (double)N_r / ((double)K_r * T_j) * (double)cnt[i];
+      const double f = (double)N_r / ((double)K_r * T_j) * (double)c;
       v = f * ((double)seq_p_sum[(size_t)j * N_r + i] / (double)T_j);
     }
     term[i] = v;
-  }
-  __syncthreads();
-  for (int h = 128; h > 0; h >>= 1) {   // fixed pairing: deterministic
-    if (threadIdx.x < h) term[threadIdx.x] += term[threadIdx.x + h];
     __syncthreads();
+    for (int h = 128; h > 0; h >>= 1) {   // fixed pairing: deterministic
+      if (threadIdx.x < h) term[threadIdx.x] += term[threadIdx.x + h];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) stat_per_seq[j] = (float)((double)alpha * term[0]);
   }
-  if (threadIdx.x == 0) {
-    stat_per_seq[j] = (float)((double)alpha * term[0]);
-  }
+  cluster.sync();   // the peers' histograms stay in place until CTA 0 has read them
 }
 
 // Mean over sequences, summed in order in fp64 (one thread: n_seq is small).
@@ -102,8 +109,8 @@ cudaError_t launch_seq_stat(const float* seq_p_sum, const int32_t* topk_idx,
                             const int32_t* seq_offsets, int n_seq, int N_r, int K_r,
                             float alpha, float* stat_per_seq, float* stat_mean,
                             cudaStream_t st) {
-  seq_stat_kernel<<<n_seq, 1024, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, N_r, K_r, alpha,
-                                         stat_per_seq);
+  seq_stat_kernel<<<n_seq * kStatSplit, 256, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, N_r, K_r,
+                                                      alpha, stat_per_seq);
   if (stat_mean) seq_mean_kernel<<<1, 1, 0, st>>>(stat_per_seq, n_seq, stat_mean);
   return cudaGetLastError();
 }

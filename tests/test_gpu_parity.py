@@ -231,3 +231,11 @@ def test_pipelined_host_batches_match_steps():
         assert torch.equal(out_host[k], want[k].cpu()), k
         assert torch.equal(load_host[k], want_load[k].cpu()), k
     assert torch.equal(lay.b, ref.b)
+
+
+def test_sequence_statistic_with_many_short_sequences():
+    """64 sequences of 16 tokens (shorter than a P-sum window, many per window)."""
+    cfg = synth.config("mid", T=1024, n_seq=64)
+    r = run_layer(cfg)
+    idx, _ = check_routing(cfg, r)
+    check_seq_stat(cfg, r, idx)
