@@ -13,9 +13,11 @@
 // MACs, two thirds of what a single-SM M=128 x N=256 MMA needs; the TMA ingest of an
 // SM, not the tensor pipe, is what bounds these GEMMs.
 //
-// One persistent pair per two SMs walks the tiles of the segment schedule
-// (ffn_sched.cuh): segment-major, then token tile (up to 256), then feature tile.  Warp
-// roles in each CTA:
+// Persistent pairs (as many as fit) take the tiles of the segment schedule
+// (ffn_sched.cuh: segment-major, then token tile of up to 256, then feature tile) in
+// order from a per-launch device counter, so the pairs running at one time always work
+// on neighbouring tiles and share their token and weight tiles through L2.  Warp roles
+// in each CTA:
 //   warp 0      TMA producer: this CTA's weight and token rows into a 6-stage ring
 //               (32 KB per stage); completion is counted on the even CTA's barrier.
 //   warp 1      allocates 512 TMEM columns (with the peer); in the even CTA one thread
@@ -61,8 +63,13 @@ template <int MODE> struct Pair {
   static constexpr int FEAT = MODE == 0 ? 128 : 256;   // output columns per pair tile
 };
 
+constexpr int TQ = 4;                           // tile-index ring
+constexpr int kTileCounters = 64;               // counter slots handed out per launch
+
 struct Ctrl {
   uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], xfull[2], xempty[2], fin;
+  uint64_t tq_full[TQ], tq_empty[TQ];
+  int tq[TQ];
   uint32_t tmem_base;
   int abort_flag;
   SegTable tab;
@@ -76,6 +83,7 @@ struct TcArgs {
   const int32_t* expert_offset;
   __nv_bfloat16* out;
   int32_t* err;
+  int* tile_ctr;     // zeroed before the launch; pairs claim tiles from it in order
 };
 
 // silu(g) * u = g * u / (1 + e^-g), with the fast reciprocal division (the result is
@@ -129,7 +137,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_rank();
   const bool leader = rank == 0;
-  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
   const int K = MODE == 0 ? s.d : s.I;
   const int N = MODE == 0 ? s.I : s.d;            // output width
   const int n_ft = (N + FEAT - 1) / FEAT;         // feature tiles per expert
@@ -145,6 +152,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_init(&C.tempty[i], 8);      // one arrival per epilogue warp of both CTAs
       tc::mbar_init(&C.xfull[i], 128);
       tc::mbar_init(&C.xempty[i], 128);
+    }
+    for (int i = 0; i < TQ; ++i) {
+      tc::mbar_init(&C.tq_full[i], 1);
+      // readers of a tile index: the even CTA's MMA thread, the four epilogue warps of
+      // each CTA and the odd CTA's producer
+      tc::mbar_init(&C.tq_empty[i], 10);
     }
     tc::mbar_init(&C.fin, 1);
     C.abort_flag = 0;
@@ -167,11 +180,44 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int total = C.tab.total;
   volatile int* abort_flag = &C.abort_flag;
 
+  // Tiles are claimed in order from a device counter by the even CTA's producer, so
+  // pairs that start together work on neighbouring tiles (which share token and weight
+  // tiles through L2) however long their earlier tiles took.  The claimed index goes
+  // to every role of both CTAs through the TQ-slot ring tq; -1 ends the run.
+  auto next_tile = [&](int k) -> int {          // a reader's k-th tile index
+    const int slot = k % TQ;
+    const bool got = tc::mbar_wait(&C.tq_full[slot], (k / TQ) & 1, abort_flag, args.err);
+    const int t = got ? *reinterpret_cast<volatile int*>(&C.tq[slot]) : -1;
+    return t;
+  };
+  auto release_tile = [&](int k) {              // done reading slot k % TQ
+    tc::mbar_arrive_cluster(tc::cluster_addr(&C.tq_empty[k % TQ], 0));
+  };
+  auto claim_tile = [&](int k) -> int {         // even CTA's producer: publish tile k
+    const int slot = k % TQ;
+    if (!tc::mbar_wait(&C.tq_empty[slot], ((k / TQ) & 1) ^ 1, abort_flag, args.err)) return -2;
+    int t = atomicAdd(args.tile_ctr, 1);
+    if (t >= total) t = -1;
+    C.tq[slot] = t;
+    tc::st_cluster_s32(tc::cluster_addr(&C.tq[slot], 1), t);
+    tc::mbar_arrive(&C.tq_full[slot]);
+    tc::mbar_arrive_cluster(tc::cluster_addr(&C.tq_full[slot], 1));
+    return t;
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer --
       int it = 0;
-      for (int tile = pair; tile < total && !*abort_flag; tile += n_pairs) {
+      int tile = leader ? claim_tile(0) : next_tile(0);
+      for (int k = 0; tile >= 0 && !*abort_flag; ++k) {
+        int next = -1;
+        if (leader) {
+          next = claim_tile(k + 1);                     // one tile ahead of the loads
+          if (next == -2) break;
+        } else {
+          release_tile(k);
+        }
         const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
         const bool shared = tcd.seg >= s.N_r;
         const int e = shared ? tcd.seg - s.N_r : tcd.seg;
@@ -204,13 +250,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc::tma_load_2d_pair(sa + A_BYTES, mX, bar, kb * BK, x_row);
         }
         if (!ok) break;
+        tile = leader ? next : next_tile(k + 1);
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer --
       int it = 0, tcount = 0;
-      for (int tile = pair; tile < total && !*abort_flag; tile += n_pairs, ++tcount) {
+      for (;; ++tcount) {
+        const int tile = next_tile(tcount);
+        if (tile < 0 || *abort_flag) break;
+        release_tile(tcount);
         const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
         const int n_tok = tcd.n_tok;
         const uint32_t idesc = tc::idesc_bf16(256, (n_tok + 15) & ~15);
@@ -245,9 +295,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tempty0 = tc::cluster_addr(&C.tempty[0], 0);
     const uint32_t tempty1 = tc::cluster_addr(&C.tempty[1], 0);
     int tcount = 0, cc = 0;
-    for (int tile = pair; tile < total; tile += n_pairs, ++tcount) {
+    for (;; ++tcount) {
       // warp-uniform decisions: the TMEM loads below are warp-collective
-      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const int tile = __shfl_sync(0xffffffffu, next_tile(tcount), 0);
+      if (tile < 0 || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      __syncwarp();
+      if (lane == 0) release_tile(tcount);
       const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
       const int n_tok = tcd.n_tok;
       const int acc = tcount & 1;
@@ -330,6 +383,28 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// Tile counters: one slot per launch, taken round-robin from kTileCounters, so that
+// launches in flight at the same time (up to kTileCounters of them) count separately.
+__device__ int g_tile_ctr[kTileCounters];
+
+int* tile_counter(cudaError_t* err) {
+  static std::mutex mu;
+  static int* base[64] = {};
+  static unsigned next_slot = 0;
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) { *err = cudaErrorInvalidDevice; return nullptr; }
+  std::lock_guard<std::mutex> lock(mu);
+  if (base[dev] == nullptr) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_tile_ctr);
+    if (*err != cudaSuccess) return nullptr;
+    base[dev] = static_cast<int*>(p);
+  }
+  return base[dev] + (next_slot++ % kTileCounters);
+}
+
 // Pairs that fit on the device at once (cluster occupancy), cached per device.
 template <int MODE>
 int max_pairs(cudaLaunchConfig_t cfg) {
@@ -372,7 +447,11 @@ cudaError_t launch(const FfnShape& s, const CUtensorMap* maps, const int32_t* of
   if (fit < 1) return cudaErrorInvalidConfiguration;
   const int pairs = (int)std::min<long long>(fit, std::max<long long>(1, tiles_ub));
   cfg.gridDim = dim3(2 * pairs);
-  TcArgs a{s, off, static_cast<__nv_bfloat16*>(out), dev_error_ptr()};
+  int* ctr = tile_counter(&err);
+  if (ctr == nullptr) return err;
+  err = cudaMemsetAsync(ctr, 0, sizeof(int), st);
+  if (err != cudaSuccess) return err;
+  TcArgs a{s, off, static_cast<__nv_bfloat16*>(out), dev_error_ptr(), ctr};
   err = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
                            maps[7], a);
   if (err != cudaSuccess) return err;

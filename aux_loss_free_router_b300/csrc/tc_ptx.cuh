@@ -238,6 +238,11 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
   return r;
 }
 
+// Store to a 32-bit variable in the shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_cluster_s32(uint32_t cluster_addr_, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr_), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
                : "memory");

@@ -42,9 +42,9 @@ import synth  # noqa: E402
 METRIC = "MoE-layer fwd tokens/s at d=7168, 256e top-8; tensor-pipe & HBM % of peak"
 
 # ncu DRAM traffic (read + write bytes) of one gate/up GEMM launch at the V3-shaped
-# workload (dram__bytes_read.sum 19.67 GB + dram__bytes_write.sum 0.30 GB, one-pass
-# capture of the full-size bench), valid only for the kernel source with this hash.
-NCU_TRAFFIC = {"kernel_src_sha": "f7b841d582f296ed", "bytes": 19.67e9 + 0.2992e9}
+# workload (dram__bytes_read.sum 18.03 GB + dram__bytes_write.sum 0.30 GB, one-pass
+# capture of a layer step), valid only for the kernel source with this hash.
+NCU_TRAFFIC = {"kernel_src_sha": "402c6ad5a658b33e", "bytes": 18.03e9 + 0.30e9}
 
 
 def log(*a):

@@ -197,7 +197,10 @@ MOE_API moe_status moe_quantize_e4m3(const void* x, moe_dtype x_dt, int64_t rows
  *   1x128 scales h_scale [R, I/128].
  * moe_expert_down: y [R, d] = h W_down^T (y bf16 for bf16/E4M3, fp32 for f32).
  * moe_expert_ffn: both, with h in the workspace (moe_expert_ffn_workspace bytes).
- * expert_offset [N_r+1] comes from moe_dispatch. */
+ * expert_offset [N_r+1] comes from moe_dispatch.
+ * The bf16 GEMMs hand out their tiles from one of 64 device counters built into the
+ * library, taken round-robin per call and zeroed on the call's stream before its kernel;
+ * so at most 64 bf16 gate/up or down calls may be in flight on a device at one time. */
 MOE_API size_t moe_expert_ffn_workspace(moe_shape sh, moe_dtype w_dt);
 MOE_API moe_status moe_expert_gate_up(const void* x_perm, const float* x_perm_scale,
                               const void* u, const float* u_scale,
