@@ -377,7 +377,8 @@ def run_ours(args, cfg, ws, rank, local):
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3" if cfg.fp8 else "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3" if cfg.fp8 else ("f32" if cfg.dtype == "f32" else "bf16"),
+        "data": "synthetic",
         "config": config_block(cfg),
         "roofline": {"bound": "tensor",
                      "kernel": "gate_up (grouped SwiGLU GEMM, tcgen05 "
