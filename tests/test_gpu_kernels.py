@@ -126,3 +126,41 @@ def test_router_exact_ties_go_to_lower_index(N_r, K_r, G, M):
     idx_ref = oracle.select_experts(s_np, b, K_r, G, M)
     np.testing.assert_array_equal(to_np(idx), idx_ref)
     np.testing.assert_allclose(to_np(gate), np.full((T, K_r), 1.0 / K_r), rtol=1e-6)
+
+
+def test_expert_gemms_every_token_tile_size():
+    """The bf16 gate/up and down GEMMs on hand-made expert segments of 0 to 700 rows:
+    token tiles of every height from 1 to 256 rows (so every token-row box the
+    kernels load, 16 to 128 rows a CTA), segments cut into two or three tiles, empty
+    segments, and an output width (d = 320) that ends inside a 256-column tile.  Each
+    segment's y rows are compared with the oracle's expert FFN of the same rows."""
+    counts = [0, 1, 8, 15, 16, 17, 31, 32, 33, 47, 64, 65, 80, 100, 127, 128, 129, 150,
+              176, 200, 239, 241, 255, 256, 257, 300, 400, 511, 513, 700, 0, 3]
+    N_r, K_r, N_s, d, I = len(counts), 4, 1, 320, 384
+    counts[-1] += -sum(counts) % K_r
+    T = sum(counts) // K_r
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(21)
+    rnd = lambda *shape, std=1.0: (torch.randn(*shape, device=dev, generator=g) * std).bfloat16()
+    x_perm, u = rnd(T * K_r, d), rnd(T, d)
+    w = {"w_gate": rnd(N_r, I, d, std=d ** -0.5), "w_up": rnd(N_r, I, d, std=d ** -0.5),
+         "w_down": rnd(N_r, d, I, std=I ** -0.5), "ws_gate": rnd(N_s, I, d, std=d ** -0.5),
+         "ws_up": rnd(N_s, I, d, std=d ** -0.5), "ws_down": rnd(N_s, d, I, std=I ** -0.5)}
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device=dev)
+    sh = moe.make_shape(T, d, N_r, K_r, N_s, I)
+    h = torch.empty(T * K_r + N_s * T, I, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(T * K_r + N_s * T, d, dtype=torch.bfloat16, device=dev)
+    moe.expert_gate_up(x_perm, u, off, sh, w, h)
+    moe.expert_down(h, off, sh, w, y)
+    torch.cuda.synchronize()
+    assert moe.device_error() == 0
+    yg, xn, un = to_np(y), to_np(x_perm), to_np(u)
+    wn = {k: to_np(v) for k, v in w.items()}
+    segs = [(xn[a:a + c], wn["w_gate"][i], wn["w_up"][i], wn["w_down"][i], a)
+            for i, (a, c) in enumerate(zip(np.cumsum([0] + counts[:-1]), counts)) if c]
+    segs.append((un, wn["ws_gate"][0], wn["ws_up"][0], wn["ws_down"][0], T * K_r))
+    for xs, wg, wu, wd, r0 in segs:
+        ref = oracle.expert_ffn(xs, wg, wu, wd)
+        got = yg[r0:r0 + len(xs)].astype(np.float64)
+        assert np.abs(got - ref).max() <= 2e-2, (r0, len(xs))
+        assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref), (r0, len(xs))
