@@ -445,7 +445,9 @@ def decode_pass(moe, cfg, x, dev, stream, T: int = 128, steps: int = 50) -> dict
     off = synth.make_seq_offsets(T, 1).to(dev)
     for _ in range(3):
         lay.step(u, off)
-    g = lay.capture(u, off, steps=steps)
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+           for _ in range(steps)]
+    g = lay.capture(u, off, steps=steps, events=evs)
     g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -454,9 +456,13 @@ def decode_pass(moe, cfg, x, dev, stream, T: int = 128, steps: int = 50) -> dict
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    stage_names = ["route", "dispatch", "gate_up", "down", "combine_bias_stat"]
+    stages = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(steps))
+              for i, n in enumerate(stage_names)}
     wbytes = (cfg.N_r + cfg.N_s) * 3 * cfg.I * cfg.d * 2
     return {"T": T, "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3),
-            "weight_GB_per_s_if_all_read": wbytes / (ms / 1e3) / 1e9}
+            "weight_GB_per_s_if_all_read": wbytes / (ms / 1e3) / 1e9,
+            "stages_ms": stages}
 
 
 def main():
