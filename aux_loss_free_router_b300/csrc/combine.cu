@@ -2,15 +2,22 @@
 // (DeepSeek-V3 Technical Report reading guide, Method §2, equation for h'_t;
 // pwwt.cn notes §四: the gate-weighted sum of the experts' outputs back at the token).
 //
-// One warp per token; each lane owns 16-byte column vectors, so every row read is a
-// fully coalesced 512-byte warp access.  The fp32 accumulation order is fixed: u,
-// shared experts ascending, routed slots k ascending (deterministic).
+// One warp per token and column chunk; each lane owns 16-byte column vectors, so every
+// row read is a fully coalesced 512-byte warp access.  Small batches (decode) split each
+// row into column chunks over gridDim.y so that enough warps have loads in flight.  The
+// fp32 accumulation order of every element is fixed: u, shared experts ascending,
+// routed slots k ascending (deterministic, and independent of the chunking).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
 namespace moe {
 
 namespace {
+
+// Below this many token warps a row is split into column chunks.
+constexpr int kTargetWarps = 2048;
 
 template <typename TIn> struct Vec;
 template <> struct Vec<float> {
@@ -62,18 +69,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
                                                       const float* __restrict__ gate,
                                                       const int32_t* __restrict__ inv_row,
                                                       int T, int d, int K_r, int N_s,
+                                                      int pass_per_chunk,
                                                       TOut* __restrict__ out) {
   constexpr int V = Vec<TIn>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
+  const int c_begin = blockIdx.y * pass_per_chunk * 64 * V;
+  const int c_end = min(d, c_begin + pass_per_chunk * 64 * V);
   const float my_g = lane < K_r ? gate[(size_t)t * K_r + lane] : 0.f;
   const int my_r = lane < K_r ? inv_row[(size_t)t * K_r + lane] : 0;
   const size_t routed_rows = (size_t)T * K_r;
   // two 16-byte column vectors per lane per pass: twice the loads in flight
-  for (int c0 = 0; c0 < d; c0 += 64 * V) {
+  for (int c0 = c_begin; c0 < c_end; c0 += 64 * V) {
     const int ca = c0 + lane * V, cb = ca + 32 * V;
-    const bool oka = ca < d, okb = cb < d;
+    const bool oka = ca < c_end, okb = cb < c_end;
     float acc[2][V], tmp[2][V];
 #pragma unroll
     for (int q = 0; q < V; ++q) acc[0][q] = acc[1][q] = 0.f;
@@ -110,8 +120,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
 template <typename TIn, typename TOut>
 cudaError_t run(const void* u, const void* y, const float* gate, const int32_t* inv_row, int T,
                 int d, int K_r, int N_s, void* out, cudaStream_t st) {
-  combine_kernel<TIn, TOut><<<(T + 7) / 8, 256, 0, st>>>(
-      (const TIn*)u, (const TIn*)y, gate, inv_row, T, d, K_r, N_s, (TOut*)out);
+  constexpr int kCols = 64 * Vec<TIn>::N;              // columns of one pass of a warp
+  const int passes = (d + kCols - 1) / kCols;
+  const int chunks = std::min(passes, std::max(1, kTargetWarps / T));
+  const int ppc = (passes + chunks - 1) / chunks;
+  const dim3 grid((T + 7) / 8, (passes + ppc - 1) / ppc);
+  combine_kernel<TIn, TOut><<<grid, 256, 0, st>>>(
+      (const TIn*)u, (const TIn*)y, gate, inv_row, T, d, K_r, N_s, ppc, (TOut*)out);
   return cudaGetLastError();
 }
 

@@ -12,7 +12,9 @@
 //            __match_any_sync groups equal experts, the rank inside a group is the
 //            number of lower lanes with the same expert.  Positions therefore grow
 //            with t inside every expert: the order is deterministic and stable.
-//   gather:  one warp per token reads its row once and writes it to its K_r rows.
+//   gather:  one warp per token (per column chunk in small batches) reads its row once
+//            and writes it to its K_r rows.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -23,6 +25,8 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 4;
+// Below this many token warps the gather splits each row into column chunks.
+constexpr int kGatherTargetWarps = 2048;
 
 __global__ void __launch_bounds__(kWarps * 32) dispatch_count_kernel(
     const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r, int32_t* __restrict__ counts) {
@@ -135,10 +139,12 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_scatter_kernel(
   }
 }
 
-// 16-byte vector copy of each token's row to its K_r destination rows.
+// 16-byte vector copy of each token's row to its K_r destination rows: one warp per
+// token and column chunk (small batches split each row over gridDim.y so that enough
+// warps have loads in flight); the chunk of blockIdx.y == 0 also copies the scales.
 __global__ void __launch_bounds__(256) dispatch_gather_kernel(
     const uint8_t* __restrict__ u, size_t row_bytes, const float* __restrict__ u_scale,
-    int scale_cols, const int32_t* __restrict__ inv_row, int T, int K_r,
+    int scale_cols, const int32_t* __restrict__ inv_row, int T, int K_r, int pass_per_chunk,
     uint8_t* __restrict__ x_perm, float* __restrict__ x_perm_scale) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -146,10 +152,13 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(
   const int my_row = lane < K_r ? inv_row[(size_t)t * K_r + lane] : 0;
   const uint4* src = reinterpret_cast<const uint4*>(u + (size_t)t * row_bytes);
   const size_t nvec = row_bytes / 16;
+  const size_t v_begin = (size_t)blockIdx.y * pass_per_chunk * 32;
+  const size_t v_stop = v_begin + (size_t)pass_per_chunk * 32;
+  const size_t v_end = v_stop < nvec ? v_stop : nvec;
   // Every lane runs every iteration so that the shuffles below see the full warp.
-  for (size_t v0 = 0; v0 < nvec; v0 += 32) {
+  for (size_t v0 = v_begin; v0 < v_end; v0 += 32) {
     const size_t v = v0 + lane;
-    const bool ok = v < nvec;
+    const bool ok = v < v_end;
     uint4 val = make_uint4(0, 0, 0, 0);
     if (ok) val = __ldg(src + v);
     for (int k = 0; k < K_r; ++k) {
@@ -157,7 +166,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(
       if (ok) reinterpret_cast<uint4*>(x_perm + (size_t)r * row_bytes)[v] = val;
     }
   }
-  if (u_scale) {
+  if (u_scale && blockIdx.y == 0) {
     for (int c0 = 0; c0 < scale_cols; c0 += 32) {
       const int c = c0 + lane;
       const bool ok = c < scale_cols;
@@ -191,8 +200,12 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
                                                             load, expert_offset, perm_token,
                                                             inv_row);
   if (u && x_perm) {
-    dispatch_gather_kernel<<<(T + 7) / 8, 256, 0, st>>>(
-        (const uint8_t*)u, row_bytes, u_scale, scale_cols, inv_row, T, K_r,
+    const int passes = (int)((row_bytes / 16 + 31) / 32);   // 512-byte passes of a warp
+    const int chunks = std::min(passes, std::max(1, kGatherTargetWarps / T));
+    const int ppc = (passes + chunks - 1) / chunks;
+    const dim3 grid((T + 7) / 8, (passes + ppc - 1) / ppc);
+    dispatch_gather_kernel<<<grid, 256, 0, st>>>(
+        (const uint8_t*)u, row_bytes, u_scale, scale_cols, inv_row, T, K_r, ppc,
         (uint8_t*)x_perm, x_perm_scale);
   }
   return cudaGetLastError();

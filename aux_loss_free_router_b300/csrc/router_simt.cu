@@ -378,22 +378,41 @@ __global__ void __launch_bounds__(256, 2) router_select_oct_kernel(const float* 
     seqid[threadIdx.x] = seq_of(t0 + threadIdx.x, p.seq_offsets, p.n_seq);
 
   float sv[Q][4], bv[Q][4];
+  // z = the split-K partials added in split order; the loads of PB splits (8 float4 per
+  // thread) are issued before their adds, so a small batch with many splits waits for
+  // a few load round trips, not one per split
+  constexpr int PB = Q >= 8 ? 1 : 8 / Q;
+  float4 z[Q];
+  const float* zp = z_part + (size_t)t * N + 4 * part;
+  const size_t split_stride = (size_t)T * N;
+#pragma unroll
+  for (int q = 0; q < Q; ++q)
+    z[q] = valid ? __ldg(reinterpret_cast<const float4*>(zp + 32 * q)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (valid) {
+    for (int sp0 = 1; sp0 < S; sp0 += PB) {
+      float4 w[PB][Q];
+#pragma unroll
+      for (int j = 0; j < PB; ++j)
+#pragma unroll
+        for (int q = 0; q < Q; ++q)
+          if (sp0 + j < S)
+            w[j][q] = __ldg(reinterpret_cast<const float4*>(zp + (size_t)(sp0 + j) * split_stride + 32 * q));
+#pragma unroll
+      for (int j = 0; j < PB; ++j)
+#pragma unroll
+        for (int q = 0; q < Q; ++q)
+          if (sp0 + j < S) {
+            z[q].x = __fadd_rn(z[q].x, w[j][q].x); z[q].y = __fadd_rn(z[q].y, w[j][q].y);
+            z[q].z = __fadd_rn(z[q].z, w[j][q].z); z[q].w = __fadd_rn(z[q].w, w[j][q].w);
+          }
+    }
+  }
 #pragma unroll
   for (int q = 0; q < Q; ++q) {
     const float4 bb = __ldg(reinterpret_cast<const float4*>(b + 32 * q + 4 * part));
     bv[q][0] = bb.x; bv[q][1] = bb.y; bv[q][2] = bb.z; bv[q][3] = bb.w;
-    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) {
-      const float* zp = z_part + (size_t)t * N + 32 * q + 4 * part;
-      z = __ldg(reinterpret_cast<const float4*>(zp));
-      for (int sp = 1; sp < S; ++sp) {
-        const float4 w = __ldg(reinterpret_cast<const float4*>(zp + (size_t)sp * T * N));
-        z.x = __fadd_rn(z.x, w.x); z.y = __fadd_rn(z.y, w.y);
-        z.z = __fadd_rn(z.z, w.z); z.w = __fadd_rn(z.w, w.w);
-      }
-    }
-    sv[q][0] = sigmoid_f32(z.x); sv[q][1] = sigmoid_f32(z.y);
-    sv[q][2] = sigmoid_f32(z.z); sv[q][3] = sigmoid_f32(z.w);
+    sv[q][0] = sigmoid_f32(z[q].x); sv[q][1] = sigmoid_f32(z[q].y);
+    sv[q][2] = sigmoid_f32(z[q].z); sv[q][3] = sigmoid_f32(z[q].w);
   }
   if (valid && p.s_out) {
 #pragma unroll
