@@ -12,7 +12,8 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 64, BN = 64, BK = 16;
+constexpr int BM = 64, BN = 64, BK = 32;
+constexpr int kLd = BM * BK / 256;   // elements of each operand a thread loads per K step
 
 __device__ __forceinline__ float silu_f32(float z) { return __fdiv_rn(z, __fadd_rn(1.f, expf(-z))); }
 
@@ -28,9 +29,9 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(FfnShape s, const float* 
                                                        const float* __restrict__ ws1,
                                                        float* __restrict__ out) {
   __shared__ SegTable tab;
-  __shared__ float As[BK][BM + 4];
-  __shared__ float B0[BK][BN + 4];
-  __shared__ float B1[BK][BN + 4];
+  __shared__ float As[BK][BM + 1];   // +1: the transposing stores hit 32 banks
+  __shared__ float B0[BK][BN + 1];
+  __shared__ float B1[BK][BN + 1];
   const int K = MODE == 0 ? s.d : s.I;
   const int N = MODE == 0 ? s.I : s.d;
   const int n_tiles_n = (N + BN - 1) / BN;
@@ -54,20 +55,31 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(FfnShape s, const float* 
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc0[i][j] = acc1[i][j] = 0.f;
-    for (int k0 = 0; k0 < K; k0 += BK) {
-      for (int x = threadIdx.x; x < BM * BK; x += 256) {
-        const int r = x / BK, c = x % BK;
-        const int gr = m0 + r, gk = k0 + c;
-        As[c][r] = (gr < tc.rows && gk < K) ? A[(size_t)gr * K + gk] : 0.f;
+    // the next K step's operands are loaded into registers while this one computes
+    float ra[kLd], rb0[kLd], rb1[kLd];
+    auto load_step = [&](int k0) {
+#pragma unroll
+      for (int q = 0; q < kLd; ++q) {
+        const int x = threadIdx.x + 256 * q;
+        const int r = x / BK, c = x % BK, gk = k0 + c;
+        ra[q] = (m0 + r < tc.rows && gk < K) ? A[(size_t)(m0 + r) * K + gk] : 0.f;
+        const bool ok = n0 + r < N && gk < K;
+        rb0[q] = ok ? W0[(size_t)(n0 + r) * K + gk] : 0.f;
+        if (MODE == 0) rb1[q] = ok ? W1[(size_t)(n0 + r) * K + gk] : 0.f;
       }
-      for (int x = threadIdx.x; x < BN * BK; x += 256) {
+    };
+    load_step(0);
+    for (int k0 = 0; k0 < K; k0 += BK) {
+#pragma unroll
+      for (int q = 0; q < kLd; ++q) {
+        const int x = threadIdx.x + 256 * q;
         const int r = x / BK, c = x % BK;
-        const int gn = n0 + r, gk = k0 + c;
-        const bool ok = gn < N && gk < K;
-        B0[c][r] = ok ? W0[(size_t)gn * K + gk] : 0.f;
-        if (MODE == 0) B1[c][r] = ok ? W1[(size_t)gn * K + gk] : 0.f;
+        As[c][r] = ra[q];
+        B0[c][r] = rb0[q];
+        if (MODE == 0) B1[c][r] = rb1[q];
       }
       __syncthreads();
+      if (k0 + BK < K) load_step(k0 + BK);
 #pragma unroll
       for (int c = 0; c < BK; ++c) {
         float av[4], bv0[4], bv1[4];

@@ -13,8 +13,9 @@ constexpr int kTok = 32;   // tokens per block
 constexpr int kKc = 32;    // reduction chunk
 
 // z = u e^T on CUDA cores (fp32 layers, or shapes the tensor-core GEMM does not
-// take): 32 tokens x N_r centroids per block, fp32 FMA over 32-wide chunks of d.
-template <typename TIn>
+// take): 32 tokens x N_r centroids per block, fp32 FMA over 32-wide chunks of d.  Thread
+// (ty, tx) owns token ty and centroids tx + 8j, j < JN (JN >= N_r / 8).
+template <typename TIn, int JN>
 __global__ void __launch_bounds__(256) router_gemm_simt_kernel(const TIn* __restrict__ u,
                                                                const TIn* __restrict__ e,
                                                                int T, int d, int N_r,
@@ -25,9 +26,9 @@ __global__ void __launch_bounds__(256) router_gemm_simt_kernel(const TIn* __rest
   const int tid = threadIdx.x;
   const int t0 = blockIdx.x * kTok;
   const int ty = tid >> 3, tx = tid & 7;
-  float acc[kMaxExperts / 8];
+  float acc[JN];
 #pragma unroll
-  for (int j = 0; j < kMaxExperts / 8; ++j) acc[j] = 0.f;
+  for (int j = 0; j < JN; ++j) acc[j] = 0.f;
   for (int k0 = 0; k0 < d; k0 += kKc) {
     for (int x = tid; x < kTok * kKc; x += blockDim.x) {
       const int r = x / kKc, c = x % kKc, t = t0 + r, k = k0 + c;
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(256) router_gemm_simt_kernel(const TIn* __rest
     for (int c = 0; c < kKc; ++c) {
       const float uv = u_tile[ty * (kKc + 1) + c];
 #pragma unroll
-      for (int j = 0; j < kMaxExperts / 8; ++j) {
+      for (int j = 0; j < JN; ++j) {
         const int i = tx + 8 * j;
         if (i < N_r) acc[j] = fmaf(uv, e_tile[i * (kKc + 1) + c], acc[j]);
       }
@@ -52,42 +53,43 @@ __global__ void __launch_bounds__(256) router_gemm_simt_kernel(const TIn* __rest
   const int t = t0 + ty;
   if (t < T) {
 #pragma unroll
-    for (int j = 0; j < kMaxExperts / 8; ++j) {
+    for (int j = 0; j < JN; ++j) {
       const int i = tx + 8 * j;
       if (i < N_r) z[(size_t)t * N_r + i] = acc[j];
     }
   }
 }
 
-// The routing decision for 32 tokens per block (one warp), for the shapes the
+// The routing decision for 32 tokens per block (eight warps), for the shapes the
 // warp-per-token kernel below does not take: z = the fixed-order fp32 sum of the S
-// split-K partials, s = sigmoid(z) into shared memory, then either one thread per
-// token (select_row) or one warp per token (route_token); s is written out when asked
-// for, and the block's P-sum window runs.
-__global__ void __launch_bounds__(32) router_select_kernel(const float* __restrict__ z_part,
-                                                           int S, const float* __restrict__ b,
-                                                           RouteOut p, int fast) {
+// split-K partials, s = sigmoid(z) into shared memory (the block's 256 threads over
+// the tile's token x expert entries), then either one thread per token (select_row,
+// warp 0) or one warp per token (route_token, warp w takes tokens w, w+8, ...); s is
+// written out when asked for, and the block's P-sum window runs.
+constexpr int kSelWarps = 8;
+__global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(
+    const float* __restrict__ z_part, int S, const float* __restrict__ b, RouteOut p, int fast) {
   static_assert(kTok == kPWindow, "one block covers one P-sum window");
   __shared__ float s_tile[kTok * (kMaxExperts + 1)];
   __shared__ float b_sm[kMaxExperts];
   __shared__ float rs_sm[kTok];
   __shared__ int seqid[kTok];
-  const int lane = threadIdx.x, N_r = p.N_r, T = p.T, stride = N_r + 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int N_r = p.N_r, T = p.T, stride = N_r + 1;
   const int t0 = blockIdx.x * kTok;
   const int ntok = min(kTok, T - t0);
-  for (int i = lane; i < N_r; i += 32) b_sm[i] = b[i];
-  if (p.pwin && lane < ntok) seqid[lane] = seq_of(t0 + lane, p.seq_offsets, p.n_seq);
-  for (int r = 0; r < ntok; ++r) {
-    const int t = t0 + r;
-    for (int i = lane; i < N_r; i += 32) {
-      float z = z_part[(size_t)t * N_r + i];
-      for (int sp = 1; sp < S; ++sp) z = __fadd_rn(z, z_part[((size_t)sp * T + t) * N_r + i]);
-      s_tile[r * stride + i] = sigmoid_f32(z);
-    }
+  for (int i = threadIdx.x; i < N_r; i += blockDim.x) b_sm[i] = b[i];
+  if (p.pwin && (int)threadIdx.x < ntok)
+    seqid[threadIdx.x] = seq_of(t0 + threadIdx.x, p.seq_offsets, p.n_seq);
+  for (int x = threadIdx.x; x < ntok * N_r; x += blockDim.x) {
+    const int r = x / N_r, i = x - r * N_r, t = t0 + r;
+    float z = z_part[(size_t)t * N_r + i];
+    for (int sp = 1; sp < S; ++sp) z = __fadd_rn(z, z_part[((size_t)sp * T + t) * N_r + i]);
+    s_tile[r * stride + i] = sigmoid_f32(z);
   }
-  __syncwarp();
+  __syncthreads();
   if (!fast) {
-    for (int r = 0; r < ntok; ++r) {
+    for (int r = warp; r < ntok; r += kSelWarps) {
       route_token(s_tile + r * stride, b_sm, t0 + r, p);
       if (p.pwin) {
         float part = 0.f;
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(32) router_select_kernel(const float* __restri
         if (lane == 0) rs_sm[r] = rs;
       }
     }
-  } else {
+  } else if (warp == 0) {
     const int t = t0 + lane;
     float rowsum = 0.f;
     if (t < T) {
@@ -121,13 +123,15 @@ __global__ void __launch_bounds__(32) router_select_kernel(const float* __restri
     }
     rs_sm[lane] = rowsum;
   }
-  __syncwarp();
+  __syncthreads();
   if (p.s_out) {
-    for (int r = 0; r < ntok; ++r)
-      for (int i = lane; i < N_r; i += 32) p.s_out[(size_t)(t0 + r) * N_r + i] = s_tile[r * stride + i];
+    for (int x = threadIdx.x; x < ntok * N_r; x += blockDim.x) {
+      const int r = x / N_r, i = x - r * N_r;
+      p.s_out[(size_t)(t0 + r) * N_r + i] = s_tile[r * stride + i];
+    }
   }
   if (p.pwin) {
-    for (int i = lane; i < N_r; i += 32)
+    for (int i = threadIdx.x; i < N_r; i += blockDim.x)
       window_runs([&](int r) { return __fdiv_rn(s_tile[r * stride + i], rs_sm[r]); }, seqid, ntok,
                   t0, N_r, i, p.pwin);
   }
@@ -585,12 +589,29 @@ cudaError_t launch_router_gemm_simt(const void* u, const void* e, moe_dtype dt, 
   if (T == 0) return cudaSuccess;
   const size_t smem = sizeof(float) * ((size_t)kTok * (kKc + 1) + (size_t)N_r * (kKc + 1));
   const dim3 grid((T + kTok - 1) / kTok);
+  // accumulators per thread: N_r / 8 rounded up to a power of two
+  int jn = 1;
+  while (jn * 8 < N_r) jn <<= 1;
   if (dt == MOE_F32) {
-    router_gemm_simt_kernel<float><<<grid, 256, smem, st>>>((const float*)u, (const float*)e, T,
-                                                            d, N_r, z);
+    const float *pu = (const float*)u, *pe = (const float*)e;
+    switch (jn) {
+      case 1: router_gemm_simt_kernel<float, 1><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 2: router_gemm_simt_kernel<float, 2><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 4: router_gemm_simt_kernel<float, 4><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 8: router_gemm_simt_kernel<float, 8><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 16: router_gemm_simt_kernel<float, 16><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      default: router_gemm_simt_kernel<float, 32><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+    }
   } else {
-    router_gemm_simt_kernel<__nv_bfloat16><<<grid, 256, smem, st>>>(
-        (const __nv_bfloat16*)u, (const __nv_bfloat16*)e, T, d, N_r, z);
+    const __nv_bfloat16 *pu = (const __nv_bfloat16*)u, *pe = (const __nv_bfloat16*)e;
+    switch (jn) {
+      case 1: router_gemm_simt_kernel<__nv_bfloat16, 1><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 2: router_gemm_simt_kernel<__nv_bfloat16, 2><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 4: router_gemm_simt_kernel<__nv_bfloat16, 4><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 8: router_gemm_simt_kernel<__nv_bfloat16, 8><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 16: router_gemm_simt_kernel<__nv_bfloat16, 16><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      default: router_gemm_simt_kernel<__nv_bfloat16, 32><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+    }
   }
   return cudaGetLastError();
 }
@@ -614,7 +635,7 @@ cudaError_t launch_router_select(const float* z_part, int S, const float* b, con
     }
   } else {
     const int fast = fast_select_ok(p.N_r, p.K_r, p.G, p.M) ? 1 : 0;
-    router_select_kernel<<<blocks, 32, 0, st>>>(z_part, S, b, p, fast);
+    router_select_kernel<<<blocks, kSelWarps * 32, 0, st>>>(z_part, S, b, p, fast);
   }
   return cudaGetLastError();
 }

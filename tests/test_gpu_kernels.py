@@ -96,6 +96,11 @@ def test_combine_v3_shape_sampled():
     (256, 8, 8, 8, 129, 384, 3),     # eight groups, one key each
     (256, 8, 1, 1, 96, 256, 3),      # no group limit; sequences of one window
     (64, 1, 1, 1, 50, 128, 5),       # K_r = 1; sequences shorter than a window
+    # shapes outside the one-warp and eight-thread kernels: the general selection kernel
+    (16, 2, 1, 1, 100, 256, 2),      # 16 experts: one warp per token
+    (48, 5, 3, 1, 130, 128, 2),      # three groups of 16, the best group keeps all five
+    (96, 6, 3, 3, 164, 256, 4),      # three groups of 32: one thread per token
+    (200, 10, 1, 1, 77, 256, 1),     # ten of 200 experts
 ])
 def test_router_shapes_bit_exact(N_r, K_r, G, M, T, d, n_seq):
     cfg = synth.MoEConfig("route", T=T, d=d, N_r=N_r, K_r=K_r, N_s=0, I=128, G=G, M=M,

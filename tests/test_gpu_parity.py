@@ -91,6 +91,19 @@ def test_ragged_bf16_layers(T, d, I, N_r, K_r, G, M, N_s):
     check_output_full(cfg, r, rel_tol=BF16_REL, abs_tol=BF16_ABS)
 
 
+@pytest.mark.parametrize("T,d,I,N_r,K_r,N_s", [
+    (150, 264, 200, 16, 3, 1),   # K steps and output tiles that end part-way
+    (77, 136, 72, 24, 4, 2),
+])
+def test_ragged_fp32_layers(T, d, I, N_r, K_r, N_s):
+    cfg = synth.MoEConfig("ragged-f32", T=T, d=d, N_r=N_r, K_r=K_r, N_s=N_s, I=I, G=1, M=1,
+                          dtype="f32", bias="uniform", seed=T + 2)
+    r = run_layer(cfg)
+    idx, _ = check_routing(cfg, r)
+    check_seq_stat(cfg, r, idx)
+    check_output_full(cfg, r, rel_tol=1e-5)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_empty_and_concentrated_experts(dtype):
     # a bias of +1 on experts 0..K_r-1 sends every token there: the other experts get
