@@ -10,12 +10,14 @@ namespace moe {
 namespace {
 
 constexpr int kTok = 32;   // tokens per block
-constexpr int kKc = 32;    // reduction chunk
+// Reduction chunk of the SIMT affinity GEMM for JN accumulators per thread: wide
+// chunks (fewer load round trips) while the centroid tile stays small.
+template <int JN> constexpr int simt_kc() { return JN <= 4 ? 128 : (JN <= 8 ? 64 : 32); }
 
 // z = u e^T on CUDA cores (fp32 layers, or shapes the tensor-core GEMM does not
-// take): 32 tokens x N_r centroids per block, fp32 FMA over 32-wide chunks of d.  Thread
+// take): 32 tokens x N_r centroids per block, fp32 FMA over chunks of d.  Thread
 // (ty, tx) owns token ty and centroids tx + 8j, j < JN (JN >= N_r / 8).
-template <typename TIn, int JN>
+template <typename TIn, int JN, int kKc = simt_kc<JN>()>
 __global__ void __launch_bounds__(256) router_gemm_simt_kernel(const TIn* __restrict__ u,
                                                                const TIn* __restrict__ e,
                                                                int T, int d, int N_r,
@@ -29,14 +31,30 @@ __global__ void __launch_bounds__(256) router_gemm_simt_kernel(const TIn* __rest
   float acc[JN];
 #pragma unroll
   for (int j = 0; j < JN; ++j) acc[j] = 0.f;
+  // per chunk a thread loads UL token and up to EL centroid elements, all of them into
+  // registers before any shared-memory store, so the loads are in flight together
+  constexpr int UL = kTok * kKc / 256, EL = 8 * JN * kKc / 256;
   for (int k0 = 0; k0 < d; k0 += kKc) {
-    for (int x = tid; x < kTok * kKc; x += blockDim.x) {
-      const int r = x / kKc, c = x % kKc, t = t0 + r, k = k0 + c;
-      u_tile[r * (kKc + 1) + c] = (t < T && k < d) ? to_f32(u[(size_t)t * d + k]) : 0.f;
+    float ru[UL], re[EL];
+#pragma unroll
+    for (int q = 0; q < UL; ++q) {
+      const int x = tid + 256 * q, r = x / kKc, c = x % kKc, t = t0 + r, k = k0 + c;
+      ru[q] = (t < T && k < d) ? to_f32(u[(size_t)t * d + k]) : 0.f;
     }
-    for (int x = tid; x < N_r * kKc; x += blockDim.x) {
-      const int r = x / kKc, c = x % kKc, k = k0 + c;
-      e_tile[r * (kKc + 1) + c] = (k < d) ? to_f32(e[(size_t)r * d + k]) : 0.f;
+#pragma unroll
+    for (int q = 0; q < EL; ++q) {
+      const int x = tid + 256 * q, r = x / kKc, c = x % kKc, k = k0 + c;
+      re[q] = (r < N_r && k < d) ? to_f32(e[(size_t)r * d + k]) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < UL; ++q) {
+      const int x = tid + 256 * q;
+      u_tile[(x / kKc) * (kKc + 1) + x % kKc] = ru[q];
+    }
+#pragma unroll
+    for (int q = 0; q < EL; ++q) {
+      const int x = tid + 256 * q;
+      if (x / kKc < N_r) e_tile[(x / kKc) * (kKc + 1) + x % kKc] = re[q];
     }
     __syncthreads();
 #pragma unroll 4
@@ -587,32 +605,34 @@ __global__ void __launch_bounds__(256) seq_psum_kernel(const float* __restrict__
 cudaError_t launch_router_gemm_simt(const void* u, const void* e, moe_dtype dt, int T, int d,
                                     int N_r, float* z, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  const size_t smem = sizeof(float) * ((size_t)kTok * (kKc + 1) + (size_t)N_r * (kKc + 1));
   const dim3 grid((T + kTok - 1) / kTok);
   // accumulators per thread: N_r / 8 rounded up to a power of two
   int jn = 1;
   while (jn * 8 < N_r) jn <<= 1;
+  auto smem = [&](int kc) { return sizeof(float) * (size_t)(kTok + N_r) * (kc + 1); };
+#define MOE_SIMT_GEMM(TIN, JN)                                                              \
+  router_gemm_simt_kernel<TIN, JN><<<grid, 256, smem(simt_kc<JN>()), st>>>(                 \
+      (const TIN*)u, (const TIN*)e, T, d, N_r, z)
   if (dt == MOE_F32) {
-    const float *pu = (const float*)u, *pe = (const float*)e;
     switch (jn) {
-      case 1: router_gemm_simt_kernel<float, 1><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      case 2: router_gemm_simt_kernel<float, 2><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      case 4: router_gemm_simt_kernel<float, 4><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      case 8: router_gemm_simt_kernel<float, 8><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      case 16: router_gemm_simt_kernel<float, 16><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      default: router_gemm_simt_kernel<float, 32><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 1: MOE_SIMT_GEMM(float, 1); break;
+      case 2: MOE_SIMT_GEMM(float, 2); break;
+      case 4: MOE_SIMT_GEMM(float, 4); break;
+      case 8: MOE_SIMT_GEMM(float, 8); break;
+      case 16: MOE_SIMT_GEMM(float, 16); break;
+      default: MOE_SIMT_GEMM(float, 32); break;
     }
   } else {
-    const __nv_bfloat16 *pu = (const __nv_bfloat16*)u, *pe = (const __nv_bfloat16*)e;
     switch (jn) {
-      case 1: router_gemm_simt_kernel<__nv_bfloat16, 1><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      case 2: router_gemm_simt_kernel<__nv_bfloat16, 2><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      case 4: router_gemm_simt_kernel<__nv_bfloat16, 4><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      case 8: router_gemm_simt_kernel<__nv_bfloat16, 8><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      case 16: router_gemm_simt_kernel<__nv_bfloat16, 16><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
-      default: router_gemm_simt_kernel<__nv_bfloat16, 32><<<grid, 256, smem, st>>>(pu, pe, T, d, N_r, z); break;
+      case 1: MOE_SIMT_GEMM(__nv_bfloat16, 1); break;
+      case 2: MOE_SIMT_GEMM(__nv_bfloat16, 2); break;
+      case 4: MOE_SIMT_GEMM(__nv_bfloat16, 4); break;
+      case 8: MOE_SIMT_GEMM(__nv_bfloat16, 8); break;
+      case 16: MOE_SIMT_GEMM(__nv_bfloat16, 16); break;
+      default: MOE_SIMT_GEMM(__nv_bfloat16, 32); break;
     }
   }
+#undef MOE_SIMT_GEMM
   return cudaGetLastError();
 }
 
