@@ -16,7 +16,9 @@
  * Conventions shared by every call
  *   - All tensor arguments are DEVICE pointers owned by the caller, row-major, and
  *     16-byte aligned.  The library allocates no device memory and keeps no state
- *     between calls, except one device-resident error word (see moe_device_error).
+ *     between calls, except device arrays built into it: one error word (see
+ *     moe_device_error), the bf16 expert GEMMs' tile counters (see
+ *     moe_expert_gate_up) and the scratch of moe_dispatch_noalloc.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call only
  *     enqueues work on it and returns; no call synchronises with the device.
  *   - Arguments are validated before anything is launched: on an invalid argument a
