@@ -91,6 +91,20 @@ def test_ragged_bf16_layers(T, d, I, N_r, K_r, G, M, N_s):
     check_output_full(cfg, r, rel_tol=BF16_REL, abs_tol=BF16_ABS)
 
 
+@pytest.mark.parametrize("T,d,I,N_r,K_r,G,M,N_s", [
+    (100, 64, 64, 1, 1, 1, 1, 1),         # one routed expert: every token picks it
+    (96, 128, 64, 256, 32, 1, 1, 0),      # the largest K_r: 32 of 256 experts
+    (64, 128, 64, 256, 32, 32, 32, 1),    # 32 groups of 8 experts, all kept, one key each
+])
+def test_extreme_bf16_shapes(T, d, I, N_r, K_r, G, M, N_s):
+    cfg = synth.MoEConfig("extreme", T=T, d=d, N_r=N_r, K_r=K_r, N_s=N_s, I=I, G=G, M=M,
+                          dtype="bf16", bias="uniform", seed=T + N_r)
+    r = run_layer(cfg)
+    idx, _ = check_routing(cfg, r)
+    check_seq_stat(cfg, r, idx)
+    check_output_full(cfg, r, rel_tol=BF16_REL, abs_tol=BF16_ABS)
+
+
 @pytest.mark.parametrize("T,d,I,N_r,K_r,N_s", [
     (150, 264, 200, 16, 3, 1),   # K steps and output tiles that end part-way
     (77, 136, 72, 24, 4, 2),
