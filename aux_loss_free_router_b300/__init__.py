@@ -73,7 +73,7 @@ _lib = None
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libmoe.so (once).  Raises MoEError-free ``OSError`` if it is missing:
+    """Load libmoe.so (once).  Raises ``OSError`` if it is missing:
     build it with ``python -m aux_loss_free_router_b300.build``."""
     global _lib
     if _lib is None:

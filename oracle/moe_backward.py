@@ -8,7 +8,7 @@ Sources: the same pages as ``moe_oracle`` — [P4/P5] Method §2 (h'_t, s_{i,t},
 g'_{i,t}), [P3] §1.1.2–§1.1.3 (the bias only decides the selection and is moved by
 the sign rule after each step) and §1.2 (the sequence-wise balance loss).
 
-What is differentiated (readings; each is listed in DESIGN.md):
+What is differentiated (readings taken where the pages are silent):
 
 * the selection (Top-K_r of fp32(s + b) under the group limit) is piecewise
   constant in the inputs and passes no gradient; the bias b enters only the
@@ -27,8 +27,6 @@ taken from ``moe_oracle.route``), so that finite differences of it, at a frozen
 selection, measure exactly the function whose gradient ``layer_backward`` returns.
 """
 from __future__ import annotations
-
-from typing import Optional
 
 import numpy as np
 

@@ -17,7 +17,7 @@ title and section):
   Method §2: the equations for h'_t, s_{i,t} and g'_{i,t}, and gamma = 0.001,
   alpha = 0.0001.
 
-Readings taken where the pages are silent or garbled (each is listed in the design doc):
+Readings taken where the pages are silent or garbled:
 
 * gates are g = g' / sum_j g'_j over the selected experts ([P3] §一 "normalise all
   selected affinity scores"; [P4] Method §2 "normalising g'");
