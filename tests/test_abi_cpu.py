@@ -108,3 +108,36 @@ def test_quant_combine_balance_reject_bad_args(lib):
     assert lib.moe_bias_update(FAKE, FAKE, sh, -1.0, None) == 1
     assert lib.moe_seq_balance_stat(FAKE, FAKE, FAKE, 0, sh, 1e-4, FAKE, FAKE, None) == 1
     assert lib.moe_device_error(None, 0) == 1
+
+
+def test_expert_calls_check_weights_and_empty_batches(lib):
+    """E4M3 weights need their block scales and d, I multiples of 128; an unknown
+    weight dtype is unsupported; an empty batch is accepted and enqueues nothing."""
+    sh = shape()
+    w = moe._Weights(moe.E4M3, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, FAKE, None, None, None)
+    assert lib.moe_expert_gate_up(FAKE, FAKE, FAKE, FAKE, FAKE, sh, ctypes.byref(w), FAKE, FAKE, None) == 1
+    w.gate_scale = w.up_scale = w.down_scale = FAKE
+    w.s_gate_scale = w.s_up_scale = w.s_down_scale = FAKE
+    assert lib.moe_expert_down(FAKE, FAKE, FAKE, shape(I=200), ctypes.byref(w), FAKE, None) == 1
+    assert lib.moe_expert_down(FAKE, FAKE, FAKE, shape(d=264), ctypes.byref(w), FAKE, None) == 1
+    w.dtype = 7
+    assert lib.moe_expert_down(FAKE, None, FAKE, sh, ctypes.byref(w), FAKE, None) == 2
+    w.dtype = moe.BF16
+    assert lib.moe_expert_down(FAKE, None, FAKE, sh, ctypes.byref(w), None, None) == 1
+    assert lib.moe_expert_down(FAKE, None, FAKE, sh, ctypes.byref(w), FAKE + 8, None) == 1
+    empty = shape(T=0)
+    assert lib.moe_expert_gate_up(None, None, None, None, None, empty, ctypes.byref(w), None, None, None) == 0
+    assert lib.moe_expert_ffn(None, None, None, None, None, empty, ctypes.byref(w), None, None, 0, None) == 0
+    assert lib.moe_combine(None, None, moe.BF16, None, None, empty, None, moe.F32, None) == 0
+
+
+def test_combine_route_and_statistic_argument_checks(lib):
+    sh = shape()
+    assert lib.moe_combine(FAKE, FAKE, moe.BF16, FAKE, FAKE, sh, FAKE, moe.E4M3, None) == 2
+    assert lib.moe_combine(FAKE, FAKE, moe.BF16, FAKE, FAKE, sh, FAKE + 4, moe.F32, None) == 1
+    assert lib.moe_route(FAKE, FAKE, moe.BF16, FAKE, sh, FAKE, -1, FAKE, FAKE, None, None, None, 0, None) == 1
+    assert lib.moe_route(FAKE, FAKE, moe.BF16, FAKE, sh, None, 0, FAKE, FAKE, FAKE + 4, None, None, 0, None) == 1
+    assert lib.moe_seq_balance_stat(None, FAKE, FAKE, 2, sh, 1e-4, FAKE, FAKE, None) == 1
+    assert lib.moe_seq_balance_stat(FAKE, None, FAKE, 2, sh, 1e-4, FAKE, FAKE, None) == 1
+    assert lib.moe_seq_balance_stat(FAKE, FAKE, FAKE, 2, sh, 1e-4, FAKE, FAKE + 4, None) == 1
+    assert lib.moe_bias_update(FAKE, FAKE, shape(G=3), 0.001, None) == 1
