@@ -123,3 +123,26 @@ def test_quantize_fp32_input_bit_exact():
     np.testing.assert_array_equal(to_np(sc), ref_sc)
     np.testing.assert_array_equal(_codes_to_values(q), ref_q)
 
+
+def test_fp8_layer_on_the_hand_worked_token():
+    """The FP8 kernels on the hand-worked single token of
+    tests/golden/fp8_layer_single_token.json: routing on the unquantised u picks
+    expert 0 (the dequantised token would pick expert 1), and h' equals the worked
+    value up to the bf16 rounding of the experts' outputs y (|dh'| <= 2^-8 of the
+    largest |y| that enters it)."""
+    from tests.test_oracle_pins import fp8_golden_case
+    g, u, e, b, w, h_ref = fp8_golden_case()
+    cfg = synth.MoEConfig("fp8-golden", T=g["T"], d=g["d"], N_r=g["N_r"], K_r=g["K_r"],
+                          N_s=g["N_s"], I=g["I"], dtype="bf16", bias="zero", fp8=True)
+    dev = "cuda"
+    x = {"u": torch.from_numpy(u).to(dev).bfloat16(), "e": torch.from_numpy(e).to(dev).bfloat16(),
+         "b": torch.from_numpy(b).to(dev), "seq_offsets": synth.make_seq_offsets(1, 1).to(dev)}
+    for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down"):
+        x[k] = torch.from_numpy(w[k]).to(dev).bfloat16()
+    r = run_layer(cfg, x)
+    assert r["topk_idx"].tolist() == g["idx"]
+    np.testing.assert_array_equal(r["topk_gate"], np.array(g["gate"], np.float32))
+    np.testing.assert_allclose(r["s_out"], g["s"], rtol=2e-6)
+    err = np.abs(r["h"].astype(np.float64) - h_ref)
+    assert err.max() <= 2.0 ** -8 * 29.0, err.max()          # |y| <= 29 in this case
+    assert err[:, 2:].max() == 0.0

@@ -98,3 +98,35 @@ def test_e4m3_round_half_away_is_caught(monkeypatch):
     monkeypatch.setattr(fp8, "e4m3_round", bad)
     monkeypatch.setattr(pins.ofp8, "e4m3_round", bad)
     _fails(pins.test_e4m3_matches_torch_cast_in_range)
+
+
+# --------------------------------------------------- the FP8 layer's composition --
+
+def test_fp8_routing_on_dequantised_tokens_is_caught(monkeypatch):
+    from oracle import fp8
+    orig = mo.route
+
+    def bad(u, e, b, K_r, G=1, M=1, s=None):
+        q, sc = fp8.quantize_1x128(np.asarray(u, np.float32))
+        return orig(fp8.dequantize_1x128(q, sc).astype(np.float32), e, b, K_r, G, M, s=s)
+    monkeypatch.setattr(mo, "route", bad)
+    _fails(pins.test_golden_fp8_layer_single_token)
+
+
+def test_fp8_skipped_h_quantisation_is_caught(monkeypatch):
+    orig = mo.expert_ffn
+    monkeypatch.setattr(mo, "expert_ffn",
+                        lambda x, wg, wu, wd, h_quant=False: orig(x, wg, wu, wd, False))
+    _fails(pins.test_golden_fp8_layer_single_token)
+
+
+def test_fp8_shared_expert_on_unquantised_tokens_is_caught(monkeypatch):
+    orig = mo.layer_output
+
+    def bad(u, idx, gate, routed, shared, x=None, h_quant=False):
+        h = orig(u, idx, gate, routed, [], x=x, h_quant=h_quant)
+        for (wg, wu, wd) in shared:
+            h += mo.expert_ffn(u, wg, wu, wd, h_quant)
+        return h
+    monkeypatch.setattr(mo, "layer_output", bad)
+    _fails(pins.test_golden_fp8_layer_single_token)

@@ -369,3 +369,38 @@ def test_quantize_128x128_blocks():
     blk = w[1, 128:, :]
     assert sc[1, 1, 0] == np.float32(np.abs(blk).max() / np.float32(448))
     np.testing.assert_array_equal(q[1, 128:, :], ofp8.e4m3_round((blk / sc[1, 1, 0]).astype(np.float32)))
+
+
+# ----------------------------------------------------- the FP8 layer composed ----
+
+def _sparse(entries, shape):
+    a = np.zeros(shape, np.float32)
+    for *ix, v in entries:
+        a[tuple(ix)] = v
+    return a
+
+
+def fp8_golden_case():
+    g = golden("fp8_layer_single_token.json")
+    T, d, I, N_r, N_s = g["T"], g["d"], g["I"], g["N_r"], g["N_s"]
+    w = {"w_gate": _sparse(g["w_gate"], (N_r, I, d)), "w_up": _sparse(g["w_up"], (N_r, I, d)),
+         "w_down": _sparse(g["w_down"], (N_r, d, I)), "ws_gate": _sparse(g["ws_gate"], (N_s, I, d)),
+         "ws_up": _sparse(g["ws_up"], (N_s, I, d)), "ws_down": _sparse(g["ws_down"], (N_s, d, I))}
+    u = _sparse(g["u"], (T, d))
+    e = _sparse(g["e"], (N_r, d))
+    h = _sparse(g["h_nonzero"], (T, d)).astype(np.float64)
+    h[0, 0], h[0, 1] = g["h_nonzero"][0][2], g["h_nonzero"][1][2]   # exact float64 values
+    return g, u, e, np.array(g["b"], np.float32), w, h
+
+
+def test_golden_fp8_layer_single_token():
+    """The FP8 composition worked by hand: 1x128 token scales, 128x128 weight scales,
+    routing on the unquantised u, the dequantised tokens into both the routed and the
+    shared expert, and the SwiGLU output re-quantised 1x128 before the down
+    projection (xyznot.com reading guide, Key ideas FP8 bullet; Method §2)."""
+    g, u, e, b, w, h = fp8_golden_case()
+    out = oracle.moe_forward(u, e, b, w, g["K_r"], 1, 1, g["N_s"], fp8=True)
+    assert out["idx"].tolist() == g["idx"]
+    np.testing.assert_allclose(out["gate"], g["gate"], rtol=0)
+    np.testing.assert_allclose(out["s"], g["s"], rtol=1e-7)
+    np.testing.assert_allclose(out["h"], h, rtol=1e-12, atol=1e-12)
