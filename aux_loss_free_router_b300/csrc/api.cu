@@ -108,7 +108,7 @@ moe_status moe_route(const void* u, const void* e, moe_dtype dt, const float* b,
                        : launch_router_gemm_simt(u, e, dt, sh.T, sh.d, sh.N_r, z_part, S(stream));
   if (err == cudaSuccess) err = launch_router_select(z_part, splits, b, p, S(stream));
   if (err == cudaSuccess && want_stat)
-    err = launch_seq_psum(pwin, seq_offsets, n_seq, sh.N_r, seq_p_sum, S(stream));
+    err = launch_seq_psum(pwin, seq_offsets, n_seq, sh.T, sh.N_r, seq_p_sum, S(stream));
   return cuda_status(err);
 }
 
@@ -324,7 +324,7 @@ moe_status moe_seq_balance_stat(const float* seq_p_sum, const int32_t* topk_idx,
       !ok_opt(stat_mean))
     return MOE_ERR_INVALID_ARG;
   if (sh.T > 0 && !ok_ptr(topk_idx)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_seq_stat(seq_p_sum, topk_idx, seq_offsets, n_seq, sh.N_r, sh.K_r,
+  return cuda_status(launch_seq_stat(seq_p_sum, topk_idx, seq_offsets, n_seq, sh.T, sh.N_r, sh.K_r,
                                      alpha, stat_per_seq, stat_mean, S(stream)));
 }
 

@@ -31,13 +31,15 @@ __global__ void bias_update_kernel(float* __restrict__ b, const int32_t* __restr
 // of the sequence's (token, slot) entries; CTA 0 of the cluster adds the histograms
 // (integers: exact in any order) through distributed shared memory, then forms
 // f_i = N_r/(K_r*T_j) * count_i and P_i = seq_p_sum[j, i] / T_j and sums f_i P_i by a
-// fixed-order fp64 tree.
+// fixed-order fp64 tree.  Offsets that are not 0 = off[0] <= ... <= off[n_seq] = T, and
+// selected experts outside [0, N_r), record MOE_ERR_INVALID_ARG and are left out (a
+// sequence whose own bounds are out of order or outside [0, T] counts as empty).
 constexpr int kStatSplit = 8;
 
 __global__ void __cluster_dims__(kStatSplit, 1, 1) __launch_bounds__(256)
     seq_stat_kernel(const float* __restrict__ seq_p_sum, const int32_t* __restrict__ topk_idx,
-                    const int32_t* __restrict__ seq_offsets, int N_r, int K_r, float alpha,
-                    float* __restrict__ stat_per_seq) {
+                    const int32_t* __restrict__ seq_offsets, int n_seq, int T, int N_r, int K_r,
+                    float alpha, float* __restrict__ stat_per_seq, int32_t* err) {
   __shared__ int32_t cnt[256];
   __shared__ double term[256];
   cg::cluster_group cluster = cg::this_cluster();
@@ -45,12 +47,21 @@ __global__ void __cluster_dims__(kStatSplit, 1, 1) __launch_bounds__(256)
   const int j = blockIdx.x / kStatSplit;
   cnt[threadIdx.x] = 0;
   __syncthreads();
-  const int a = seq_offsets[j], z = seq_offsets[j + 1];
+  int a = seq_offsets[j], z = seq_offsets[j + 1];
+  const bool bad = a < 0 || z < a || z > T || (j == 0 && a != 0) || (j == n_seq - 1 && z != T);
+  if (bad) {
+    if (threadIdx.x == 0 && rank == 0) record_error(err, MOE_ERR_INVALID_ARG);
+    if (a < 0 || z < a || z > T) a = z = 0;
+  }
   const long long n_ent = (long long)(z - a) * K_r;
   const long long slab = (n_ent + kStatSplit - 1) / kStatSplit;
   const long long x0 = rank * slab, x1 = min(n_ent, x0 + slab);
   const int32_t* src = topk_idx + (size_t)a * K_r;
-  for (long long x = x0 + threadIdx.x; x < x1; x += blockDim.x) atomicAdd(&cnt[__ldg(src + x)], 1);
+  for (long long x = x0 + threadIdx.x; x < x1; x += blockDim.x) {
+    const int ex = __ldg(src + x);
+    if ((unsigned)ex < (unsigned)N_r) atomicAdd(&cnt[ex], 1);
+    else record_error(err, MOE_ERR_INVALID_ARG);
+  }
   cluster.sync();   // every CTA's histogram is complete and visible to the cluster
   if (rank == 0) {
     const int i = threadIdx.x;
@@ -106,11 +117,12 @@ cudaError_t launch_bias_update(float* b, const int32_t* load, int T, int N_r, in
 }
 
 cudaError_t launch_seq_stat(const float* seq_p_sum, const int32_t* topk_idx,
-                            const int32_t* seq_offsets, int n_seq, int N_r, int K_r,
+                            const int32_t* seq_offsets, int n_seq, int T, int N_r, int K_r,
                             float alpha, float* stat_per_seq, float* stat_mean,
                             cudaStream_t st) {
-  seq_stat_kernel<<<n_seq * kStatSplit, 256, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, N_r, K_r,
-                                                      alpha, stat_per_seq);
+  seq_stat_kernel<<<n_seq * kStatSplit, 256, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, n_seq, T,
+                                                      N_r, K_r, alpha, stat_per_seq,
+                                                      dev_error_ptr());
   if (stat_mean) seq_mean_kernel<<<1, 1, 0, st>>>(stat_per_seq, n_seq, stat_mean);
   return cudaGetLastError();
 }

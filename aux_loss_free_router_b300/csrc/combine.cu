@@ -6,7 +6,9 @@
 // row read is a fully coalesced 512-byte warp access.  Small batches (decode) split each
 // row into column chunks over gridDim.y so that enough warps have loads in flight.  The
 // fp32 accumulation order of every element is fixed: u, shared experts ascending,
-// routed slots k ascending (deterministic, and independent of the chunking).
+// routed slots k ascending (deterministic, and independent of the chunking).  A routed
+// row index outside [0, T*K_r) (inv_row = -1 marks an entry dispatch skipped) adds
+// nothing and records MOE_ERR_INVALID_ARG in the device error word.
 #include <algorithm>
 
 #include "common.cuh"
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
                                                       const int32_t* __restrict__ inv_row,
                                                       int T, int d, int K_r, int N_s,
                                                       int pass_per_chunk,
-                                                      TOut* __restrict__ out) {
+                                                      TOut* __restrict__ out, int32_t* err) {
   constexpr int V = Vec<TIn>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -78,8 +80,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
   const int c_begin = blockIdx.y * pass_per_chunk * 64 * V;
   const int c_end = min(d, c_begin + pass_per_chunk * 64 * V);
   const float my_g = lane < K_r ? gate[(size_t)t * K_r + lane] : 0.f;
-  const int my_r = lane < K_r ? inv_row[(size_t)t * K_r + lane] : 0;
   const size_t routed_rows = (size_t)T * K_r;
+  int my_r = lane < K_r ? inv_row[(size_t)t * K_r + lane] : 0;
+  if ((size_t)(unsigned)my_r >= routed_rows) {     // also catches negative rows
+    if (blockIdx.y == 0) record_error(err, MOE_ERR_INVALID_ARG);
+    my_r = -1;
+  }
   // two 16-byte column vectors per lane per pass: twice the loads in flight
   for (int c0 = c_begin; c0 < c_end; c0 += 64 * V) {
     const int ca = c0 + lane * V, cb = ca + 32 * V;
@@ -103,6 +109,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
     for (int k = 0; k < K_r; ++k) {
       const float g = __shfl_sync(0xffffffffu, my_g, k);
       const int r = __shfl_sync(0xffffffffu, my_r, k);
+      if (r < 0) continue;
       const TIn* row = y + (size_t)r * d;
       if (oka) Vec<TIn>::load(row + ca, tmp[0]);
       if (okb) Vec<TIn>::load(row + cb, tmp[1]);
@@ -126,7 +133,8 @@ cudaError_t run(const void* u, const void* y, const float* gate, const int32_t* 
   const int ppc = (passes + chunks - 1) / chunks;
   const dim3 grid((T + 7) / 8, (passes + ppc - 1) / ppc);
   combine_kernel<TIn, TOut><<<grid, 256, 0, st>>>(
-      (const TIn*)u, (const TIn*)y, gate, inv_row, T, d, K_r, N_s, ppc, (TOut*)out);
+      (const TIn*)u, (const TIn*)y, gate, inv_row, T, d, K_r, N_s, ppc, (TOut*)out,
+      dev_error_ptr());
   return cudaGetLastError();
 }
 

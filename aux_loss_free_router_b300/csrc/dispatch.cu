@@ -14,6 +14,9 @@
 //            with t inside every expert: the order is deterministic and stable.
 //   gather:  one warp per token (per column chunk in small batches) reads its row once
 //            and writes it to its K_r rows.
+// An entry of topk_idx outside [0, N_r) is skipped everywhere (no count, no row, inv_row
+// = -1) and MOE_ERR_INVALID_ARG is recorded in the device error word: the caller's
+// routing is wrong, and no memory outside the buffers is touched.
 #include <algorithm>
 #include <mutex>
 
@@ -29,7 +32,8 @@ constexpr int kWarps = 4;
 constexpr int kGatherTargetWarps = 2048;
 
 __global__ void __launch_bounds__(kWarps * 32) dispatch_count_kernel(
-    const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r, int32_t* __restrict__ counts) {
+    const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r, int32_t* __restrict__ counts,
+    int32_t* err) {
   extern __shared__ int32_t cnt_sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kWarps + warp;
@@ -41,7 +45,11 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_count_kernel(
     const int t0 = chunk * kDispatchChunk;
     const int n_ent = (min(T, t0 + kDispatchChunk) - t0) * K_r;
     const int32_t* src = topk_idx + (size_t)t0 * K_r;
-    for (int x = lane; x < n_ent; x += 32) atomicAdd(&cnt[src[x]], 1);
+    for (int x = lane; x < n_ent; x += 32) {
+      const int ex = src[x];
+      if ((unsigned)ex < (unsigned)N_r) atomicAdd(&cnt[ex], 1);
+      else record_error(err, MOE_ERR_INVALID_ARG);
+    }
     __syncwarp();
     for (int i = lane; i < N_r; i += 32) counts[(size_t)i * n_chunks + chunk] = cnt[i];
   }
@@ -123,8 +131,10 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_scatter_kernel(
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int base = 0; base < n_ent; base += 32) {
     const int x = base + lane;
-    const bool valid = x < n_ent;
-    const int ex = valid ? topk_idx[e0 + x] : -1;
+    const bool in_range = x < n_ent;
+    const int ex = in_range ? topk_idx[e0 + x] : -1;
+    const bool valid = in_range && (unsigned)ex < (unsigned)N_r;
+    if (in_range && !valid) inv_row[e0 + x] = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, ex);
     const int rank = __popc(peers & lt_mask);
     int pos = 0;
@@ -163,7 +173,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(
     if (ok) val = __ldg(src + v);
     for (int k = 0; k < K_r; ++k) {
       const int r = __shfl_sync(0xffffffffu, my_row, k);
-      if (ok) reinterpret_cast<uint4*>(x_perm + (size_t)r * row_bytes)[v] = val;
+      if (ok && r >= 0) reinterpret_cast<uint4*>(x_perm + (size_t)r * row_bytes)[v] = val;
     }
   }
   if (u_scale && blockIdx.y == 0) {
@@ -173,7 +183,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(
       const float sc = ok ? u_scale[(size_t)t * scale_cols + c] : 0.f;
       for (int k = 0; k < K_r; ++k) {
         const int r = __shfl_sync(0xffffffffu, my_row, k);
-        if (ok) x_perm_scale[(size_t)r * scale_cols + c] = sc;
+        if (ok && r >= 0) x_perm_scale[(size_t)r * scale_cols + c] = sc;
       }
     }
   }
@@ -194,7 +204,8 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
   }
   const int blocks = (n_chunks + kWarps - 1) / kWarps;
   const size_t smem = sizeof(int32_t) * kWarps * N_r;
-  dispatch_count_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts);
+  dispatch_count_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
+                                                          dev_error_ptr());
   dispatch_scan_kernel<<<(N_r + 7) / 8, 256, 0, st>>>(ws_counts, n_chunks, N_r, load);
   dispatch_scatter_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
                                                             load, expert_offset, perm_token,

@@ -34,16 +34,23 @@ struct TileCoord {
 // All threads of the block call this; the caller synchronises afterwards.  With
 // `balanced` a segment's rows are cut into ceil(rows/BM) tiles of equal size rounded up
 // to 16 (at most BM), so that the tiles of one segment take the same time; otherwise
-// into tiles of exactly BM rows.
+// into tiles of exactly BM rows.  A routed segment that does not lie inside
+// [0, T*K_r) (expert_offset not produced by the dispatch) is treated as empty and
+// MOE_ERR_INVALID_ARG is recorded in `err`.
 __device__ __forceinline__ void build_seg_table(SegTable& tab, const int32_t* __restrict__ off,
                                                 int T, int K_r, int N_r, int N_s, int BM,
-                                                int n_tiles_n, bool balanced = false) {
+                                                int n_tiles_n, bool balanced, int32_t* err) {
   const int nseg = N_r + N_s;
   for (int i = threadIdx.x; i < nseg; i += blockDim.x) {
     int r0 = 0, rows = T;
     if (i < N_r) {
       r0 = off[i];
       rows = off[i + 1] - r0;
+      if (r0 < 0 || rows < 0 || (long long)r0 + rows > (long long)T * K_r) {
+        if (blockIdx.x == 0) record_error(err, MOE_ERR_INVALID_ARG);
+        r0 = 0;
+        rows = 0;
+      }
     }
     tab.row0[i] = r0;
     tab.rows[i] = rows;

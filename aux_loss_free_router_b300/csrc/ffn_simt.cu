@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(FfnShape s, const float* 
                                                        const float* __restrict__ w1,
                                                        const float* __restrict__ ws0,
                                                        const float* __restrict__ ws1,
-                                                       float* __restrict__ out) {
+                                                       float* __restrict__ out, int32_t* err) {
   __shared__ SegTable tab;
   __shared__ float As[BK][BM + 1];   // +1: the transposing stores hit 32 banks
   __shared__ float B0[BK][BN + 1];
@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(FfnShape s, const float* 
   const int K = MODE == 0 ? s.d : s.I;
   const int N = MODE == 0 ? s.I : s.d;
   const int n_tiles_n = (N + BN - 1) / BN;
-  build_seg_table(tab, expert_offset, s.T, s.K_r, s.N_r, s.N_s, BM, n_tiles_n);
+  build_seg_table(tab, expert_offset, s.T, s.K_r, s.N_r, s.N_s, BM, n_tiles_n, false, err);
   __syncthreads();
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   for (int tile = blockIdx.x; tile < tab.total; tile += gridDim.x) {
@@ -131,7 +131,7 @@ cudaError_t launch_ffn_up_simt(const FfnShape& s, const float* x_perm, const flo
   if (s.T == 0) return cudaSuccess;
   ffn_simt_kernel<0><<<grid_for(s, s.I), 256, 0, st>>>(
       s, x_perm, u, expert_offset, (const float*)w->gate, (const float*)w->up,
-      (const float*)w->s_gate, (const float*)w->s_up, h);
+      (const float*)w->s_gate, (const float*)w->s_up, h, dev_error_ptr());
   return cudaGetLastError();
 }
 
@@ -141,7 +141,7 @@ cudaError_t launch_ffn_down_simt(const FfnShape& s, const float* h,
   if (s.T == 0) return cudaSuccess;
   ffn_simt_kernel<1><<<grid_for(s, s.d), 256, 0, st>>>(
       s, h, nullptr, expert_offset, (const float*)w->down, nullptr, (const float*)w->s_down,
-      nullptr, y);
+      nullptr, y, dev_error_ptr());
   return cudaGetLastError();
 }
 

@@ -34,8 +34,8 @@ cudaError_t launch_router_gemm_simt(const void* u, const void* e, moe_dtype dt, 
                                     int N_r, float* z, cudaStream_t st);
 cudaError_t launch_router_select(const float* z_part, int S, const float* b, const RouteOut& p,
                                  cudaStream_t st);
-cudaError_t launch_seq_psum(const float* pwin, const int32_t* seq_offsets, int n_seq, int N_r,
-                            float* out, cudaStream_t st);
+cudaError_t launch_seq_psum(const float* pwin, const int32_t* seq_offsets, int n_seq, int T,
+                            int N_r, float* out, cudaStream_t st);
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
                             const void* u, size_t row_bytes, const float* u_scale,
@@ -79,7 +79,7 @@ cudaError_t launch_combine(const void* u, const void* y, moe_dtype dt, const flo
 cudaError_t launch_bias_update(float* b, const int32_t* load, int T, int N_r, int K_r,
                                float gamma, cudaStream_t st);
 cudaError_t launch_seq_stat(const float* seq_p_sum, const int32_t* topk_idx,
-                            const int32_t* seq_offsets, int n_seq, int N_r, int K_r,
+                            const int32_t* seq_offsets, int n_seq, int T, int N_r, int K_r,
                             float alpha, float* stat_per_seq, float* stat_mean,
                             cudaStream_t st);
 

@@ -572,14 +572,22 @@ inline bool warp_select_ok(int N_r, int K_r, int G, int M) {
 // out[j, i] = sum over the P-sum windows' run sums of sequence j: the run starting at
 // the sequence's first token and one at every window start inside the sequence.  A
 // block takes one sequence and 32 experts (lane = expert); its 8 warps take every 8th
-// run, accumulate in fp64, and the 8 partial sums are added in warp order.
+// run, accumulate in fp64, and the 8 partial sums are added in warp order.  Offsets
+// that are not 0 = off[0] <= ... <= off[n_seq] = T record MOE_ERR_INVALID_ARG; a
+// sequence whose own bounds are out of order or outside [0, T] is summed as empty.
 __global__ void __launch_bounds__(256) seq_psum_kernel(const float* __restrict__ pwin,
                                                        const int32_t* __restrict__ seq_offsets,
-                                                       int N_r, float* __restrict__ out) {
+                                                       int n_seq, int T, int N_r,
+                                                       float* __restrict__ out, int32_t* err) {
   __shared__ double part[8][32];
   const int j = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.y * 32 + lane;
-  const int a = seq_offsets[j], z = seq_offsets[j + 1];
+  int a = seq_offsets[j], z = seq_offsets[j + 1];
+  const bool bad = a < 0 || z < a || z > T || (j == 0 && a != 0) || (j == n_seq - 1 && z != T);
+  if (bad) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) record_error(err, MOE_ERR_INVALID_ARG);
+    if (a < 0 || z < a || z > T) a = z = 0;
+  }
   double acc = 0.0;
   if (i < N_r && a < z) {
     // run r = 0 starts at a; run r >= 1 at the r-th window start after a
@@ -660,11 +668,11 @@ cudaError_t launch_router_select(const float* z_part, int S, const float* b, con
   return cudaGetLastError();
 }
 
-cudaError_t launch_seq_psum(const float* pwin, const int32_t* seq_offsets, int n_seq, int N_r,
-                            float* out, cudaStream_t st) {
+cudaError_t launch_seq_psum(const float* pwin, const int32_t* seq_offsets, int n_seq, int T,
+                            int N_r, float* out, cudaStream_t st) {
   if (n_seq == 0) return cudaSuccess;
   const dim3 grid(n_seq, (N_r + 31) / 32);
-  seq_psum_kernel<<<grid, 256, 0, st>>>(pwin, seq_offsets, N_r, out);
+  seq_psum_kernel<<<grid, 256, 0, st>>>(pwin, seq_offsets, n_seq, T, N_r, out, dev_error_ptr());
   return cudaGetLastError();
 }
 

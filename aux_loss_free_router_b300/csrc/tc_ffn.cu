@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tmem_alloc_pair(&C.tmem_base, TMEM_COLS);
     tc::tmem_relinquish_pair();
   }
-  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BT, n_ft, true);
+  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BT, n_ft, true, args.err);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();

@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tmem_alloc(&C.tmem_base, TMEM_COLS);
     tc::tmem_relinquish();
   }
-  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BM, n_tiles_n);
+  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BM, n_tiles_n, false,
+                  args.err);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();

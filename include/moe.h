@@ -25,9 +25,18 @@
  *     call returns MOE_ERR_INVALID_ARG (or MOE_ERR_UNSUPPORTED for a dtype/shape
  *     combination with no kernel, MOE_ERR_WORKSPACE for a missing or short
  *     workspace) and enqueues nothing.  MOE_ERR_CUDA reports a failed launch.
- *   - Values of device-resident inputs (indices, offsets) are trusted: callers
- *     pass what the previous call in the chain produced.  NaN/Inf inputs are
- *     undefined behaviour.
+ *   - Values of device-resident inputs are checked by the kernels that read them:
+ *     an expert index outside [0, N_r), an inv_row outside [0, T*K_r), an
+ *     expert_offset segment outside [0, T*K_r), or seq_offsets that are not
+ *     0 = off[0] <= ... <= off[n_seq] = T are skipped (the entry adds nothing; an
+ *     out-of-order sequence counts as empty), no memory outside the buffers is
+ *     touched, and MOE_ERR_INVALID_ARG is recorded in the device error word (see
+ *     moe_device_error).  The results of such a call are meaningless.  NaN/Inf
+ *     inputs are undefined behaviour.
+ *   - The library caches, per device, the addresses of its built-in device arrays
+ *     (tile counters, dispatch scratch).  A device reset (cudaDeviceReset) frees
+ *     them: do not call the library on a device that has been reset in the same
+ *     process.
  *   - Token-level notation follows [P4] Method §2: u_t the layer input of token t,
  *     e_i the centroid of routed expert i, b_i its routing bias, N_r routed and
  *     N_s shared experts, K_r experts active per token, I the SwiGLU width.
@@ -105,8 +114,9 @@ MOE_API int moe_abi_version(void);
  *
  *   u [T, d], e [N_r, d]: both dtype `dt` (MOE_F32 or MOE_BF16).
  *   b [N_r] fp32: routing bias, read only.
- *   seq_offsets [n_seq+1] int32 (device), monotone, seq_offsets[n_seq] == T; may be
- *     NULL with n_seq == 0 when no sequence statistic is wanted.
+ *   seq_offsets [n_seq+1] int32 (device), 0 = off[0] <= off[1] <= ... <= off[n_seq]
+ *     = T (checked on the device, see above); may be NULL with n_seq == 0 when no
+ *     sequence statistic is wanted.
  *   topk_idx [T, K_r] int32 out: selected experts in descending s+b order, ties to
  *     the lower index.  topk_gate [T, K_r] fp32 out: s_{i,t} / sum over the
  *     selected s (raw s, never s+b).
@@ -251,8 +261,10 @@ MOE_API moe_status moe_seq_balance_stat(const float* seq_p_sum, const int32_t* t
 /* --------------------------------------------------------------------------------
  * Device error word.  Kernels that wait on asynchronous copies bound every wait;
  * a wait that runs out records MOE_ERR_TIMEOUT here and the kernel returns early.
- * This call synchronises the current device, copies the word to *code (MOE_OK if
- * nothing was recorded) and, if `clear` is non-zero, resets it. */
+ * Kernels that find an invalid device-resident value record MOE_ERR_INVALID_ARG.
+ * The word keeps the largest code recorded.  This call synchronises the current
+ * device, copies the word to *code (MOE_OK if nothing was recorded) and, if `clear`
+ * is non-zero, resets it. */
 MOE_API moe_status moe_device_error(int32_t* code, int32_t clear);
 
 #ifdef __cplusplus

@@ -169,3 +169,74 @@ def test_expert_gemms_every_token_tile_size():
         got = yg[r0:r0 + len(xs)].astype(np.float64)
         assert np.abs(got - ref).max() <= 2e-2, (r0, len(xs))
         assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref), (r0, len(xs))
+
+
+def test_out_of_range_expert_index_is_skipped_and_reported():
+    """One topk_idx entry outside [0, N_r): dispatch skips it (no count, inv_row = -1,
+    no gathered row), combine leaves it out, the device error word reads
+    MOE_ERR_INVALID_ARG, and nothing is written past the output buffers."""
+    T, d, N_r, K_r = 96, 256, 16, 2
+    dev = "cuda"
+    sh = moe.make_shape(T, d, N_r, K_r, 0, 128)
+    g = torch.Generator(device=dev).manual_seed(3)
+    idx = torch.stack([torch.randperm(N_r, generator=g, device=dev)[:K_r] for _ in range(T)]).int()
+    idx[40, 1] = N_r + 5                                  # the bad entry
+    u = torch.randn(T, d, device=dev, generator=g).bfloat16()
+    guard = 64
+    load = torch.empty(N_r, dtype=torch.int32, device=dev)
+    off = torch.empty(N_r + 1, dtype=torch.int32, device=dev)
+    perm = torch.full((T * K_r + guard,), -7, dtype=torch.int32, device=dev)
+    inv = torch.full((T * K_r + guard,), -7, dtype=torch.int32, device=dev)
+    xp = torch.full((T * K_r + guard, d), 3.0, device=dev).bfloat16()
+    moe.device_error(clear=True)
+    moe.dispatch(idx, sh, load, off, perm[:T * K_r], inv[:T * K_r].view(T, K_r), u=u,
+                 x_perm=xp[:T * K_r])
+    torch.cuda.synchronize()
+    assert moe.device_error(clear=True) == 1              # MOE_ERR_INVALID_ARG
+    assert int(load.sum()) == T * K_r - 1 and int(off[N_r]) == T * K_r - 1
+    assert int(inv[40 * K_r + 1]) == -1
+    assert (perm[T * K_r:] == -7).all() and (inv[T * K_r:] == -7).all()
+    assert (xp[T * K_r:] == 3.0).all()
+    valid = [(t, k) for t in range(T) for k in range(K_r) if (t, k) != (40, 1)]
+    rows = inv[:T * K_r].view(T, K_r)
+    for t, k in valid[::17]:
+        assert torch.equal(xp[int(rows[t, k])], u[t])
+    # combine: the skipped slot adds nothing
+    y = torch.randn(T * K_r, d, device=dev, generator=g).bfloat16()
+    gate = torch.full((T, K_r), 0.5, device=dev)
+    h = torch.empty(T, d, device=dev)
+    moe.combine(u, y, gate, rows.contiguous(), sh, h)
+    torch.cuda.synchronize()
+    assert moe.device_error(clear=True) == 1
+    want = u[40].float() + 0.5 * y[int(rows[40, 0])].float()
+    torch.testing.assert_close(h[40], want, rtol=1e-6, atol=1e-6)
+
+
+def test_bad_sequence_offsets_are_reported():
+    """seq_offsets that are not 0 <= ... <= T: the statistic records
+    MOE_ERR_INVALID_ARG, treats the out-of-order sequence as empty and reads nothing
+    outside topk_idx and seq_p_sum."""
+    T, N_r, K_r = 256, 32, 4
+    dev = "cuda"
+    sh = moe.make_shape(T, 256, N_r, K_r, 0, 128)
+    g = torch.Generator(device=dev).manual_seed(4)
+    idx = torch.stack([torch.randperm(N_r, generator=g, device=dev)[:K_r] for _ in range(T)]).int()
+    psum = torch.rand(3, N_r, device=dev, generator=g)
+    stat = torch.full((3,), -1.0, device=dev)
+    mean = torch.empty(1, device=dev)
+    ok_off = torch.tensor([0, 100, 180, T], dtype=torch.int32, device=dev)
+    moe.device_error(clear=True)
+    moe.seq_balance_stat(psum, idx, ok_off, 3, sh, 1e-4, stat, mean)
+    torch.cuda.synchronize()
+    assert moe.device_error(clear=True) == 0
+    good = stat.clone()
+    bad_off = torch.tensor([0, 180, 100, T], dtype=torch.int32, device=dev)   # 180 > 100
+    moe.seq_balance_stat(psum, idx, bad_off, 3, sh, 1e-4, stat, mean)
+    torch.cuda.synchronize()
+    assert moe.device_error(clear=True) == 1
+    assert float(stat[1]) == 0.0                         # [180, 100) counts as empty
+    short_off = torch.tensor([0, 100, 180, T - 1], dtype=torch.int32, device=dev)
+    moe.seq_balance_stat(psum, idx, short_off, 3, sh, 1e-4, stat, mean)
+    torch.cuda.synchronize()
+    assert moe.device_error(clear=True) == 1             # does not end at T
+    assert float(stat[0]) == float(good[0])
