@@ -350,8 +350,11 @@ def run_ours(args, cfg, ws, rank, local):
     pk = peaks()
     t_gu = stages["gate_up"] / 1e3
     achieved = wk["gate_up_flop"] / t_gu / 1e12
-    peak = pk["bf16_tflops_sustained"]
-    peak_source = f"{pk['source']} bf16 sustained"
+    # the timed region is K steps of a few ms (well under a second), so each GEMM
+    # launch is measured against the burst rate of a dense bf16 GEMM, not the rate it
+    # settles at after seconds under the power cap
+    peak = pk["bf16_tflops"]
+    peak_source = f"{pk['source']} bf16 burst"
     if cfg.fp8:   # E4M3 dense rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
         peak *= 2.0
         peak_source += " x 2 (nominal E4M3/bf16 ratio)"
