@@ -7,8 +7,9 @@
 // row into column chunks over gridDim.y so that enough warps have loads in flight.  The
 // fp32 accumulation order of every element is fixed: u, shared experts ascending,
 // routed slots k ascending (deterministic, and independent of the chunking).  A routed
-// row index outside [0, T*K_r) (inv_row = -1 marks an entry dispatch skipped) adds
-// nothing and records MOE_ERR_INVALID_ARG in the device error word.
+// row index outside [0, T*K_r) (inv_row = -1 marks an entry dispatch skipped) is read as
+// row 0 with gate 0, so it adds nothing, and MOE_ERR_INVALID_ARG is recorded in the
+// device error word.
 #include <algorithm>
 
 #include "common.cuh"
@@ -79,12 +80,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
   if (t >= T) return;
   const int c_begin = blockIdx.y * pass_per_chunk * 64 * V;
   const int c_end = min(d, c_begin + pass_per_chunk * 64 * V);
-  const float my_g = lane < K_r ? gate[(size_t)t * K_r + lane] : 0.f;
   const size_t routed_rows = (size_t)T * K_r;
+  float my_g = lane < K_r ? gate[(size_t)t * K_r + lane] : 0.f;
   int my_r = lane < K_r ? inv_row[(size_t)t * K_r + lane] : 0;
-  if ((size_t)(unsigned)my_r >= routed_rows) {     // also catches negative rows
-    if (blockIdx.y == 0) record_error(err, MOE_ERR_INVALID_ARG);
-    my_r = -1;
+  if ((size_t)(unsigned)my_r >= routed_rows) {     // also catches negative rows: the slot
+    if (blockIdx.y == 0) record_error(err, MOE_ERR_INVALID_ARG);   // adds exactly 0 * y[0]
+    my_r = 0;
+    my_g = 0.f;
   }
   // two 16-byte column vectors per lane per pass: twice the loads in flight
   for (int c0 = c_begin; c0 < c_end; c0 += 64 * V) {
@@ -109,7 +111,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
     for (int k = 0; k < K_r; ++k) {
       const float g = __shfl_sync(0xffffffffu, my_g, k);
       const int r = __shfl_sync(0xffffffffu, my_r, k);
-      if (r < 0) continue;
       const TIn* row = y + (size_t)r * d;
       if (oka) Vec<TIn>::load(row + ca, tmp[0]);
       if (okb) Vec<TIn>::load(row + cb, tmp[1]);

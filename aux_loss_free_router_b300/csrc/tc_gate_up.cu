@@ -1,5 +1,7 @@
-// Grouped SwiGLU expert GEMMs on the sm_103a tensor cores: tcgen05 pair MMAs over
-// TMEM, fed by TMA.
+// Grouped gate/up GEMM with the SwiGLU epilogue, on the sm_103a tensor cores: tcgen05
+// pair MMAs over TMEM, fed by TMA.  h = silu(x W_gate^T) * (x W_up^T) over the expert
+// segments of the FFN row space (DeepSeek-V3 Technical Report reading guide, Method §2:
+// the experts' FFN terms of h'_t; SwiGLU is the reading taken for the unnamed FFN).
 //
 // Weights on the M side, tokens on the N side: each MMA computes a block of the
 // transposed output, D^T = W X^T.  The MMA's N (tokens) goes down to 16 in steps of
@@ -7,64 +9,47 @@
 // 15 padding tokens), where a token-major M tile would pad up to 127 rows.
 //
 // Two CTAs on two SMs form a pair (a cluster of two) and issue M=256 MMAs together
-// (cta_group::2): each CTA holds 128 of the 256 weight rows and half of the token rows
-// of a K step, and receives its 128 rows of the accumulator in its own TMEM.  Per SM
-// a K step of 64 moves 32 KB (16 KB of weights, 16 KB of tokens) for 128 x 256 x 64
-// MACs, two thirds of what a single-SM M=128 x N=256 MMA needs; the TMA ingest of an
-// SM, not the tensor pipe, is what bounds these GEMMs.
+// (cta_group::2): each CTA holds 128 of the 256 weight rows (64 W_gate rows over the
+// same features' 64 W_up rows) and half of the token rows of a K step, and receives its
+// 128 rows of the accumulator in its own TMEM.  Per SM a K step of 64 moves 32 KB
+// (16 KB of weights, 16 KB of tokens) for 128 x 256 x 64 MACs.
+//
+// Tiles hold at most 256 tokens, so the two 256-column TMEM accumulators alternate and
+// the SwiGLU epilogue of tile i (two special-function operations per element) overlaps
+// the MMAs of tile i+1.  A wider tile would have to take both accumulators and stall the
+// next tile's MMAs behind its epilogue.
 //
 // Persistent pairs (as many as fit) take the tiles of the segment schedule
-// (ffn_sched.cuh: segment-major, then token tile of up to 256, then feature tile) in
-// order from a per-launch device counter, so the pairs running at one time always work
-// on neighbouring tiles and share their token and weight tiles through L2.  Warp roles
-// in each CTA:
+// (ffn_sched.cuh: segment-major, then token tile of up to 256, then feature tile of 128)
+// in order from a per-launch device counter, so the pairs running at one time always
+// work on neighbouring tiles and share their token and weight tiles through L2.  Warp
+// roles in each CTA:
 //   warp 0      TMA producer: this CTA's weight and token rows into a 6-stage ring
 //               (32 KB per stage); completion is counted on the even CTA's barrier.
 //   warp 1      allocates 512 TMEM columns (with the peer); in the even CTA one thread
-//               issues the pair MMAs into one of two 256-column accumulators, so the
-//               epilogue of tile i overlaps the MMAs of tile i+1.
-//   warps 2..5  epilogue: TMEM lane = feature row, column = token; each warp transposes
-//               32 features x 16 tokens through its own shared-memory scratch and
-//               writes 16-byte pieces of token rows.
-//
-// gate/up (MODE 0): a pair tile is 128 columns of h.  Each CTA's 128 weight rows are
-//   64 rows of W_gate over the same 64 rows of W_up, so TMEM lanes 0..63 hold gate and
-//   lanes 64..127 up of the same features; per 16 tokens the four epilogue warps stage
-//   their raw values in shared memory and each thread forms 8 features of
-//   h = silu(gate) * up for one token.
-// down (MODE 1): a pair tile is 256 columns of y, 128 W_down rows per CTA.
+//               issues the pair MMAs into one of two 256-column accumulators.
+//   warps 2..5  epilogue: TMEM lanes 0..63 hold gate and lanes 64..127 up of the same
+//               64 features; per 16 tokens the four warps stage their raw values in
+//               shared memory and each thread forms 8 features of h for one token and
+//               writes them as 16 bytes.
 // Tokens past the end of a tile's segment are loaded (or zero-filled past the tensor
-// end) but sit beyond the MMA's N or are not stored; features past the output width
-// are computed from the next expert's rows (or zeros) and not stored.
-#include <algorithm>
-#include <mutex>
-
-#include "common.cuh"
-#include "ffn_sched.cuh"
-#include "launch.h"
-#include "tc_ptx.cuh"
+// end) but sit beyond the MMA's N or are not stored; features past I are computed from
+// the next expert's rows (or zeros) and not stored.
+#include "tc_ffn_common.cuh"
 #include "tmap.h"
 
 namespace moe {
 
 namespace {
 
-constexpr int BK = 64, STAGES = 6, BT = 256;
-constexpr int SMALL_ROWS = 32;                  // token box of tiles with <= 64 tokens
+using namespace ffn_tc;
+
+constexpr int STAGES = 6, BT = 256;
 constexpr int A_BYTES = 128 * BK * 2;           // this CTA's 128 weight rows
 constexpr int B_BYTES = (BT / 2) * BK * 2;      // this CTA's half of the token rows
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
 constexpr int TMEM_COLS = 512, ACC_COLS = 256;
-constexpr int THREADS = 192;
-constexpr int SCRATCH = 16 * 32 * 2;            // per epilogue warp: 16 tokens x 32 features bf16
-constexpr int XCH = 2 * 16 * 128 * 4;           // gate/up: raw values [2 buffers][16 tokens][128 rows]
-
-template <int MODE> struct Pair {
-  static constexpr int FEAT = MODE == 0 ? 128 : 256;   // output columns per pair tile
-};
-
-constexpr int TQ = 4;                           // tile-index ring
-constexpr int kTileCounters = 64;               // counter slots handed out per launch
+constexpr int XCH = 2 * 16 * 128 * 4;           // raw values [2 buffers][16 tokens][128 rows]
 
 struct Ctrl {
   uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], xfull[2], xempty[2], fin;
@@ -75,71 +60,28 @@ struct Ctrl {
   SegTable tab;
 };
 
-constexpr size_t kSmemBytes =
-    (size_t)STAGES * STAGE_BYTES + 4 * SCRATCH + XCH + sizeof(Ctrl) + 1024;
+constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + XCH + sizeof(Ctrl) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
-struct TcArgs {
-  FfnShape s;
-  const int32_t* expert_offset;
-  __nv_bfloat16* out;
-  int32_t* err;
-  int* tile_ctr;     // zeroed before the launch; pairs claim tiles from it in order
-};
-
-// silu(g) * u = g * u / (1 + e^-g), with the fast reciprocal division (the result is
-// rounded to bf16).
-__device__ __forceinline__ float swiglu(float g, float u) {
-  return __fdividef(g * u, 1.f + __expf(-g));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// 16 tokens x 32 features of one warp (lane = feature, v[j] = token j) to token rows:
-// through the warp's scratch, then 16-byte pieces of 8 features.
-__device__ __forceinline__ void store_transposed(__nv_bfloat16* scr, const float (&v)[16], int lane,
-                                                 __nv_bfloat16* out, size_t row0, int j0, int n_tok,
-                                                 int f0, int N) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) scr[j * 32 + lane] = __float2bfloat16_rn(v[j]);
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int item = i * 32 + lane;      // 16 tokens x 4 pieces of 8 features
-    const int tok = item >> 2, piece = item & 3;
-    const int f = f0 + piece * 8;
-    if (j0 + tok < n_tok && f < N) {
-      const uint4 val = *reinterpret_cast<const uint4*>(scr + tok * 32 + piece * 8);
-      *reinterpret_cast<uint4*>(out + (row0 + j0 + tok) * N + f) = val;
-    }
-  }
-  __syncwarp();
-}
-
-template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    tc_ffn_kernel(const __grid_constant__ CUtensorMap mX_r, const __grid_constant__ CUtensorMap mX_s,
+    tc_gate_up_kernel(const __grid_constant__ CUtensorMap mX_r, const __grid_constant__ CUtensorMap mX_s,
                   const __grid_constant__ CUtensorMap mW0_r, const __grid_constant__ CUtensorMap mW1_r,
                   const __grid_constant__ CUtensorMap mW0_s, const __grid_constant__ CUtensorMap mW1_s,
                   const __grid_constant__ CUtensorMap mXs_r, const __grid_constant__ CUtensorMap mXs_s,
                   TcArgs args) {
-  constexpr int FEAT = Pair<MODE>::FEAT;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_off = tc::smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_off & 1023u)) & 1023u);
-  uint8_t* scratch = base + STAGES * STAGE_BYTES;
-  float* xch = reinterpret_cast<float*>(scratch + 4 * SCRATCH);
-  Ctrl& C = *reinterpret_cast<Ctrl*>(scratch + 4 * SCRATCH + XCH);
+  float* xch = reinterpret_cast<float*>(base + STAGES * STAGE_BYTES);
+  Ctrl& C = *reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES + XCH);
 
   const FfnShape s = args.s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_rank();
   const bool leader = rank == 0;
-  const int K = MODE == 0 ? s.d : s.I;
-  const int N = MODE == 0 ? s.I : s.d;            // output width
-  const int n_ft = (N + FEAT - 1) / FEAT;         // feature tiles per expert
+  const int K = s.d;
+  const int N = s.I;                              // output width
+  const int n_ft = (N + 128 - 1) / 128;         // feature tiles per expert
   const int nk = (K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -190,8 +132,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int t = got ? *reinterpret_cast<volatile int*>(&C.tq[slot]) : -1;
     return t;
   };
-  auto release_tile = [&](int k) {              // done reading slot k % TQ
-    tc::mbar_arrive_cluster(tc::cluster_addr(&C.tq_empty[k % TQ], 0));
+  auto release_tile = [&](int k) {              // done reading slot k % TQ (value in hand)
+    tc::mbar_arrive_cluster_relaxed(tc::cluster_addr(&C.tq_empty[k % TQ], 0));
   };
   auto claim_tile = [&](int k) -> int {         // even CTA's producer: publish tile k
     const int slot = k % TQ;
@@ -225,14 +167,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int half = ((n_tok + 15) & ~15) >> 1;     // token rows per CTA
         // a tile of <= 64 tokens loads 32-row token boxes (decode-sized batches)
         const bool small = half <= SMALL_ROWS;
-        const CUtensorMap* mX = (MODE == 0 && shared) ? (small ? &mXs_s : &mX_s)
-                                                      : (small ? &mXs_r : &mX_r);
+        const CUtensorMap* mX = shared ? (small ? &mXs_s : &mX_s) : (small ? &mXs_r : &mX_r);
         const uint32_t stage_tx = (uint32_t)(A_BYTES + (small ? SMALL_ROWS : BT / 2) * BK * 2);
-        const int x_row = (MODE == 0 ? (shared ? 0 : tcd.row0) : tcd.out_row0) + tcd.tok0 +
-                          (int)rank * half;
+        const int x_row = (shared ? 0 : tcd.row0) + tcd.tok0 + (int)rank * half;
         const CUtensorMap* mW0 = shared ? &mW0_s : &mW0_r;
         const CUtensorMap* mW1 = shared ? &mW1_s : &mW1_r;
-        const int w_row = e * N + tcd.n * FEAT + (int)rank * (FEAT / 2);
+        const int w_row = e * N + tcd.n * 128 + (int)rank * (128 / 2);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int st = it % STAGES;
@@ -241,12 +181,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t bar = tc::cluster_addr(&C.full[st], 0);   // the even CTA's barrier
           if (leader) tc::mbar_arrive_expect_tx(&C.full[st], 2 * stage_tx);
           uint8_t* sa = base + st * STAGE_BYTES;
-          if (MODE == 0) {
-            tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);                 // 64 gate rows
-            tc::tma_load_2d_pair(sa + A_BYTES / 2, mW1, bar, kb * BK, w_row);   // 64 up rows
-          } else {
-            tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);                 // 128 down rows
-          }
+          tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);                   // 64 gate rows
+          tc::tma_load_2d_pair(sa + A_BYTES / 2, mW1, bar, kb * BK, w_row);     // 64 up rows
           tc::tma_load_2d_pair(sa + A_BYTES, mX, bar, kb * BK, x_row);
         }
         if (!ok) break;
@@ -291,7 +227,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue --
     const int q = warp & 3;   // TMEM lane quarter this warp can access
-    __nv_bfloat16* scr = reinterpret_cast<__nv_bfloat16*>(scratch + q * SCRATCH);  // [16][32]
     const uint32_t tempty0 = tc::cluster_addr(&C.tempty[0], 0);
     const uint32_t tempty1 = tc::cluster_addr(&C.tempty[1], 0);
     int tcount = 0, cc = 0;
@@ -311,25 +246,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t t_base = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(q * 32) << 16);
       const size_t row0 = (size_t)tcd.out_row0 + (size_t)tcd.tok0;
       bool alive = true;
-      if (MODE == 1) {
-        const int f0 = tcd.n * FEAT + (int)rank * 128 + q * 32;
-#pragma unroll 1
-        for (int j0 = 0; j0 < n_tok; j0 += 16) {
-          uint32_t a[16];
-          float v[16];
-          tc::tmem_ld16(t_base + j0, a);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(a[j]);
-          store_transposed(scr, v, lane, args.out, row0, j0, n_tok, f0, N);
-        }
-      } else {
+      {
         // lanes 0..63: gate rows, 64..127: up rows of the same 64 features.  Per 16
         // tokens all four warps put their raw values in shared memory, then each
         // thread forms 8 features of h for one token and writes them as 16 bytes.
         const int t = q * 32 + lane;                 // this thread's piece: token t/8,
         const int tok = t >> 3, piece = t & 7;       // features 8*piece .. 8*piece+7
-        const int f = tcd.n * FEAT + (int)rank * 64 + piece * 8;
+        const int f = tcd.n * 128 + (int)rank * 64 + piece * 8;
 #pragma unroll 1
         for (int j0 = 0; j0 < n_tok; j0 += 16, ++cc) {
           const int xb = cc & 1;
@@ -361,7 +284,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!alive) break;
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive_cluster(acc ? tempty1 : tempty0);
+      // the accumulator's columns are in registers: the MMA may overwrite them
+      if (lane == 0) tc::mbar_arrive_cluster_relaxed(acc ? tempty1 : tempty0);
     }
   }
 
@@ -383,80 +307,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// Tile counters: one slot per launch, taken round-robin from kTileCounters, so that
-// launches in flight at the same time (up to kTileCounters of them) count separately.
-__device__ int g_tile_ctr[kTileCounters];
-
-int* tile_counter(cudaError_t* err) {
-  static std::mutex mu;
-  static int* base[64] = {};
-  static unsigned next_slot = 0;
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= 64) { *err = cudaErrorInvalidDevice; return nullptr; }
-  std::lock_guard<std::mutex> lock(mu);
-  if (base[dev] == nullptr) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_tile_ctr);
-    if (*err != cudaSuccess) return nullptr;
-    base[dev] = static_cast<int*>(p);
-  }
-  return base[dev] + (next_slot++ % kTileCounters);
-}
-
-// Pairs that fit on the device at once (cluster occupancy), cached per device.
-template <int MODE>
-int max_pairs(cudaLaunchConfig_t cfg) {
-  static std::mutex mu;
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_ffn_kernel<MODE>, &cfg) != cudaSuccess) return 0;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
-template <int MODE>
-cudaError_t launch(const FfnShape& s, const CUtensorMap* maps, const int32_t* off, void* out,
-                   cudaStream_t st) {
-  constexpr int FEAT = Pair<MODE>::FEAT;
-  const int N = MODE == 0 ? s.I : s.d;
-  const long long t_ub = (long long)s.T * s.K_r / BT + s.N_r + (long long)s.N_s * ((s.T + BT - 1) / BT);
-  const long long tiles_ub = t_ub * ((N + FEAT - 1) / FEAT);
-  auto k = tc_ffn_kernel<MODE>;
-  cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (err != cudaSuccess) return err;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (device_sm_count() / 2));
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const int fit = max_pairs<MODE>(cfg);
-  if (fit < 1) return cudaErrorInvalidConfiguration;
-  const int pairs = (int)std::min<long long>(fit, std::max<long long>(1, tiles_ub));
-  cfg.gridDim = dim3(2 * pairs);
-  int* ctr = tile_counter(&err);
-  if (ctr == nullptr) return err;
-  err = cudaMemsetAsync(ctr, 0, sizeof(int), st);
-  if (err != cudaSuccess) return err;
-  TcArgs a{s, off, static_cast<__nv_bfloat16*>(out), dev_error_ptr(), ctr};
-  err = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
-                           maps[7], a);
-  if (err != cudaSuccess) return err;
-  return cudaGetLastError();
-}
 
 constexpr CUtensorMapDataType kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
@@ -485,28 +335,11 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
     m[5] = m[3];
   }
   if (!ok) return cudaErrorInvalidValue;
-  return launch<0>(s, m, expert_offset, h, st);
-}
-
-cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h, const int32_t* expert_offset,
-                               const moe_expert_weights* w, void* y, cudaStream_t st) {
-  if (s.T == 0) return cudaSuccess;
-  CUtensorMap m[8];
-  const uint64_t rb = (uint64_t)s.I * 2;
-  const uint64_t rows = (uint64_t)s.T * s.K_r + (uint64_t)s.N_s * s.T;
-  bool ok = make_tmap_2d(&m[0], kBF16, h, s.I, rows, rb, BK, BT / 2) &&
-            make_tmap_2d(&m[6], kBF16, h, s.I, rows, rb, BK, SMALL_ROWS) &&
-            make_tmap_2d(&m[2], kBF16, w->down, s.I, (uint64_t)s.N_r * s.d, rb, BK, 128);
-  if (ok && s.N_s > 0)
-    ok = make_tmap_2d(&m[4], kBF16, w->s_down, s.I, (uint64_t)s.N_s * s.d, rb, BK, 128);
-  else
-    m[4] = m[2];
-  if (!ok) return cudaErrorInvalidValue;
-  m[1] = m[0];
-  m[3] = m[2];
-  m[5] = m[4];
-  m[7] = m[6];
-  return launch<1>(s, m, expert_offset, y, st);
+  const long long t_ub = (long long)s.T * s.K_r / BT + s.N_r + (long long)s.N_s * ((s.T + BT - 1) / BT);
+  static std::mutex mu;
+  static int fit[64] = {};
+  TcArgs a{s, expert_offset, static_cast<__nv_bfloat16*>(h), dev_error_ptr(), nullptr};
+  return launch_pairs(tc_gate_up_kernel, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st);
 }
 
 }  // namespace moe

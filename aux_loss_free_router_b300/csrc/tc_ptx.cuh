@@ -248,6 +248,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
                : "memory");
 }
 
+// Arrival with no memory ordering, for barriers that only say "this slot may be
+// reused" after the caller has already consumed what it read (a tile index in a
+// register, TMEM columns loaded and waited for): it does not wait for the thread's
+// outstanding global stores the way a cluster-scope release does.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
+               : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is signalled on an mbarrier
 // of either CTA of the pair (cluster-window address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,

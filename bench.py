@@ -160,7 +160,7 @@ def work(cfg):
 
 
 def kernel_src_sha() -> str:
-    with open(os.path.join(ROOT, "aux_loss_free_router_b300", "csrc", "tc_ffn.cu"), "rb") as f:
+    with open(os.path.join(ROOT, "aux_loss_free_router_b300", "csrc", "tc_gate_up.cu"), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 

@@ -74,6 +74,10 @@ CONFIGS = {
                       n_seq=2, dtype="bf16", bias="zero", skew=True),
     "fp8": MoEConfig("fp8", T=4096, d=2048, N_r=64, K_r=6, N_s=2, I=1408,
                      n_seq=4, dtype="bf16", bias="zero", fp8=True),
+    # a slice of the V3-shaped layer for hardware-counter captures: the same d, I, K_r
+    # and mean expert load (256 tokens) with 32 experts in 8 groups, ~3 GB on the device
+    "v3slice": MoEConfig("v3slice", T=1024, d=7168, N_r=32, K_r=8, N_s=1, I=2048, G=8, M=4,
+                         n_seq=1, dtype="bf16", bias="uniform"),
 }
 
 
