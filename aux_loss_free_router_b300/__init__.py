@@ -169,7 +169,17 @@ def route(u, e, b, sh: Shape, topk_idx, topk_gate, s_out=None, seq_offsets=None,
     _call("moe_route", _ptr(u), _ptr(e), _dt(u), _ptr(b), sh, _ptr(seq_offsets), n_seq,
           _ptr(topk_idx), _ptr(topk_gate), _ptr(s_out), _ptr(seq_p_sum), _ptr(ws),
           ws.numel() if ws is not None else 0, _stream(stream),
-          extra_kernels=2 if seq_p_sum is not None else 0)
+          extra_kernels=_route_kernels(sh, _dt(u), seq_p_sum is not None) - _KERNELS["moe_route"])
+
+
+def _route_kernels(sh: Shape, dt: int, with_stat: bool) -> int:
+    """Kernels one moe_route call launches: one for the fused bf16 path (64/128/256
+    experts, K_r <= 8, groups of whole 32-expert blocks keeping <= 2 keys, d >= 128),
+    else the affinity GEMM and the selection, plus the P-sum kernel with statistics."""
+    grouped_ok = sh.G == 1 or ((sh.N_r // 32) % sh.G == 0 and sh.K_r // sh.M <= 2)
+    if dt == BF16 and sh.N_r in (64, 128, 256) and sh.K_r <= 8 and grouped_ok and sh.d >= 128:
+        return 1
+    return 2 + (1 if with_stat else 0)
 
 
 def dispatch(topk_idx, sh: Shape, load, expert_offset, perm_token, inv_row, u=None,

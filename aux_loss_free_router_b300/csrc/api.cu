@@ -75,8 +75,11 @@ RouteWs route_ws(const moe_shape& sh, int n_seq, int S) {
 
 size_t moe_route_workspace(moe_shape sh, int32_t n_seq) {
   if (sh.T <= 0 || sh.N_r <= 0 || sh.d <= 0) return 0;
-  // sized for the tensor-core path's split-K partials (the CUDA-core path uses one)
-  return route_ws(sh, n_seq, router_tc_splits(sh.T, sh.d)).total();
+  // sized for the split path's partial products (the CUDA-core path uses one split);
+  // the fused path needs a counter and the P-sum rows, which is less
+  const size_t split = route_ws(sh, n_seq, router_tc_splits(sh.T, sh.d)).total();
+  const size_t fused = 256 + (n_seq > 0 ? align256((size_t)n_seq * sh.N_r * 8) : 0);
+  return split > fused ? split : fused;
 }
 
 moe_status moe_route(const void* u, const void* e, moe_dtype dt, const float* b, moe_shape sh,
@@ -94,6 +97,17 @@ moe_status moe_route(const void* u, const void* e, moe_dtype dt, const float* b,
   if (sh.T == 0) {
     if (!want_stat) return MOE_OK;
     return cuda_status(cudaMemsetAsync(seq_p_sum, 0, sizeof(float) * n_seq * sh.N_r, S(stream)));
+  }
+  if (dt == MOE_BF16 && router_fused_ok(sh.N_r, sh.K_r, sh.G, sh.M, sh.d)) {
+    // one launch: a counter (256 bytes), then the fixed-point P sums [n_seq, N_r] (8 bytes each)
+    const size_t need = 256 + (want_stat ? align256((size_t)n_seq * sh.N_r * 8) : 0);
+    if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    RouteOut p{sh.T, sh.N_r, sh.K_r, sh.G, sh.M, topk_idx, topk_gate, s_out,
+               want_stat ? reinterpret_cast<float*>(ws + 256) : nullptr, seq_offsets,
+               want_stat ? n_seq : 0};
+    return cuda_status(launch_router_fused(u, e, sh.d, b, p, seq_p_sum,
+                                           reinterpret_cast<int*>(ws), S(stream)));
   }
   const bool tc = router_uses_tc(sh, dt);
   const int splits = tc ? router_tc_splits(sh.T, sh.d) : 1;

@@ -34,6 +34,14 @@ cudaError_t launch_router_gemm_simt(const void* u, const void* e, moe_dtype dt, 
                                     int N_r, float* z, cudaStream_t st);
 cudaError_t launch_router_select(const float* z_part, int S, const float* b, const RouteOut& p,
                                  cudaStream_t st);
+// Fused routing (affinity GEMM, sigmoid, keys, group limit, Top-K_r, gates, P sums in
+// one launch) for bf16 layers: 64, 128 or 256 experts, K_r <= 8, groups of whole
+// 32-expert blocks with K_r/M <= 2, d >= 128.  done_ctr: one int of scratch (zeroed on
+// the stream before the kernel when P sums are wanted).
+bool router_fused_ok(int N_r, int K_r, int G, int M, int d);
+cudaError_t launch_router_fused(const void* u, const void* e, int d, const float* b,
+                                const RouteOut& p, float* seq_p_sum, int* done_ctr,
+                                cudaStream_t st);
 cudaError_t launch_seq_psum(const float* pwin, const int32_t* seq_offsets, int n_seq, int T,
                             int N_r, float* out, cudaStream_t st);
 
