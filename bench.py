@@ -41,10 +41,16 @@ import synth  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s at d=7168, 256e top-8; tensor-pipe & HBM % of peak"
 
-# ncu DRAM traffic (read + write bytes) of one gate/up GEMM launch at the V3-shaped
-# workload (dram__bytes_read.sum 18.03 GB + dram__bytes_write.sum 0.30 GB, one-pass
-# capture of a layer step), valid only for the kernel source with this hash.
-NCU_TRAFFIC = {"kernel_src_sha": "402c6ad5a658b33e", "bytes": 18.03e9 + 0.30e9}
+# DRAM traffic of the gate/up GEMM, from one ncu capture (not measured in the bench
+# run): dram__bytes_read.sum + dram__bytes_write.sum = 2.2439 GB + 0.0353 GB on the
+# V3-shaped slice (32 experts, 1024 tokens, d=7168, I=2048, ~3 GB on the device), whose
+# algorithmic bytes are 2.108 GB: 1.081 bytes moved per algorithmic byte.  A full V3
+# launch holds eight times the slice's segments with the same mean load (256 tokens), so
+# its traffic is taken as that ratio times its own algorithmic bytes.  Valid only for
+# the kernel source with this hash.
+NCU_TRAFFIC = {"kernel_src_sha": "8c610d65cc549236", "ratio": 2.2792e9 / 2.108e9,
+               "capture": "ncu --set full --clock-control none -k regex:tc_gate_up -s 3 -c 1 "
+                          "python bench.py --config v3slice --steps 2 --warmup 3 --no-cpu-baseline"}
 
 
 def log(*a):
@@ -359,8 +365,8 @@ def run_ours(args, cfg, ws, rank, local):
         peak *= 2.0
         peak_source += " x 2 (nominal E4M3/bf16 ratio)"
     sha = kernel_src_sha()
-    traffic = (NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["kernel_src_sha"] == sha and cfg.name == "v3"
-               and not cfg.fp8 else None)
+    traffic = (NCU_TRAFFIC["ratio"] * wk["gate_up_bytes"]
+               if NCU_TRAFFIC["kernel_src_sha"] == sha and cfg.name in ("v3", "v3slice") else None)
     tok_s = cfg.T * ws / (ms / 1e3)
     kernels = {
         "route": {"ms": stages["route"], "GB/s": wk["router_bytes"] / (stages["route"] / 1e3) / 1e9,
