@@ -21,6 +21,7 @@ __all__ = [
     "MoEError", "Shape", "load_library", "route", "dispatch", "dispatch_noalloc", "quantize_e4m3",
     "expert_gate_up", "expert_down", "expert_ffn", "combine", "bias_update",
     "seq_balance_stat", "device_error", "quantize_weights", "route_workspace_bytes",
+    "backward", "backward_workspace_bytes",
     "dispatch_workspace_bytes", "expert_ffn_workspace_bytes", "MoELayer",
     "LIB_PATH", "STATUS", "launch_counter", "launch_counter_reset", "make_shape",
 ]
@@ -67,6 +68,10 @@ _SIGS = {
     "moe_bias_update": (ctypes.c_int, [_P, _P, Shape, _F, _P]),
     "moe_seq_balance_stat": (ctypes.c_int, [_P, _P, _P, _I32, Shape, _F, _P, _P, _P]),
     "moe_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _I32]),
+    "moe_backward_workspace": (_S, [Shape, _I32]),
+    "moe_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Weights),
+                                    Shape, _P, _I32, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _S, _P]),
 }
 
 _lib = None
@@ -90,7 +95,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 # Kernels each call enqueues for a non-empty batch (the launch count of a step).
 _KERNELS = {"moe_route": 2, "moe_dispatch": 3, "moe_dispatch_noalloc": 3, "moe_quantize_e4m3": 1, "moe_expert_gate_up": 1,
             "moe_expert_down": 1, "moe_expert_ffn": 2, "moe_combine": 1, "moe_bias_update": 1,
-            "moe_seq_balance_stat": 1}
+            "moe_seq_balance_stat": 1,
+            # gate/up recompute, per-token prep, six GEMMs, combine (+ counts with the
+            # balance term)
+            "moe_backward": 9}
 _launches = 0
 
 
@@ -254,6 +262,28 @@ def seq_balance_stat(seq_p_sum, topk_idx, seq_offsets, n_seq: int, sh: Shape, al
     _call("moe_seq_balance_stat", _ptr(seq_p_sum), _ptr(topk_idx), _ptr(seq_offsets), n_seq, sh,
           alpha, _ptr(stat_per_seq), _ptr(stat_mean), _stream(stream),
           extra_kernels=1 if stat_mean is not None else 0)
+
+
+def backward_workspace_bytes(sh: Shape, n_seq: int) -> int:
+    return load_library().moe_backward_workspace(sh, n_seq)
+
+
+def backward(u, e, s, topk_idx, topk_gate, expert_offset, inv_row, x_perm, y, sh: Shape,
+             weights: dict, dh, grads: dict, seq_offsets=None, n_seq: int = 0,
+             alpha: float = 0.0, workspace=None, stream=None):
+    """moe_backward: gradients of sum(dh * h') (+ the mean balance loss) at the forward
+    pass's selection.  ``grads`` holds the fp32 outputs "u", "e", "w_gate", "w_up",
+    "w_down" and, with shared experts, "ws_gate", "ws_up", "ws_down"."""
+    wt = _weights(weights)
+    ws = workspace if workspace is not None else _workspace(backward_workspace_bytes(sh, n_seq), u.device)
+    g = lambda k: _ptr(grads.get(k))
+    balance = n_seq > 0 and alpha != 0.0
+    _call("moe_backward", _ptr(u), _ptr(e), _ptr(s), _ptr(topk_idx), _ptr(topk_gate),
+          _ptr(expert_offset), _ptr(inv_row), _ptr(x_perm), _ptr(y), ctypes.byref(wt), sh,
+          _ptr(seq_offsets), n_seq, alpha, _ptr(dh), g("u"), g("e"), g("w_gate"), g("w_up"),
+          g("w_down"), g("ws_gate"), g("ws_up"), g("ws_down"), _ptr(ws),
+          ws.numel() if ws is not None else 0, _stream(stream),
+          extra_kernels=1 if balance else 0)
 
 
 def device_error(clear: bool = True) -> int:
@@ -433,6 +463,30 @@ class MoELayer:
                 out_done[slot].record(s_out)
         comp.wait_stream(s_out)
         comp.wait_stream(s_in)
+
+    def backward(self, u: torch.Tensor, dh: torch.Tensor, seq_offsets: Optional[torch.Tensor] = None,
+                 stream=None) -> dict:
+        """Gradients at the selection of the last ``step()`` on the same ``u`` (the layer
+        must have been built with ``want_s=True``; bf16 only): of sum(dh * h') plus, with
+        ``seq_offsets``, the mean over sequences of the balance loss.  Returns fp32
+        tensors "u", "e", "w_gate", "w_up", "w_down" (and "ws_*" with shared experts);
+        they and the workspace are allocated on the first call and reused."""
+        if self.s_out is None:
+            raise ValueError("backward() needs the affinities: build the layer with want_s=True")
+        dev = self.e.device
+        if not hasattr(self, "_grads"):
+            keys = ["w_gate", "w_up", "w_down"] + (["ws_gate", "ws_up", "ws_down"] if self.N_s else [])
+            g = {k: torch.empty(self.weights[k].shape, dtype=torch.float32, device=dev) for k in keys}
+            g["u"] = torch.empty(self.T, self.d, dtype=torch.float32, device=dev)
+            g["e"] = torch.empty(self.N_r, self.d, dtype=torch.float32, device=dev)
+            self._grads = g
+            self._bwd_ws = _workspace(backward_workspace_bytes(self.shape, self.n_seq), dev)
+        n_seq = self.n_seq if seq_offsets is not None else 0
+        backward(u, self.e, self.s_out, self.topk_idx, self.topk_gate, self.expert_offset,
+                 self.inv_row, self.x_perm, self.y, self.shape, self.weights, dh, self._grads,
+                 seq_offsets, n_seq, self.alpha if seq_offsets is not None else 0.0,
+                 workspace=self._bwd_ws, stream=stream)
+        return self._grads
 
     def capture(self, u: torch.Tensor, seq_offsets: torch.Tensor, steps: int = 1,
                 events: Optional[list] = None, pre=None, post=None) -> "torch.cuda.CUDAGraph":

@@ -342,6 +342,103 @@ moe_status moe_seq_balance_stat(const float* seq_p_sum, const int32_t* topk_idx,
                                      alpha, stat_per_seq, stat_mean, S(stream)));
 }
 
+// ---------------------------------------------------------------------- backward ----
+
+namespace {
+
+struct BwdWs {
+  size_t h, a, c, dY, dA, dC, dX, dz, dur, counts, total;
+};
+
+BwdWs bwd_ws(const moe_shape& sh, int n_seq) {
+  const size_t R = (size_t)sh.T * sh.K_r + (size_t)sh.N_s * sh.T;
+  const size_t ri = align256(R * sh.I * 2), rd = align256(R * sh.d * 2);
+  BwdWs w;
+  size_t o = 0;
+  w.h = o; o += ri;
+  w.a = o; o += ri;
+  w.c = o; o += ri;
+  w.dA = o; o += ri;
+  w.dC = o; o += ri;
+  w.dY = o; o += rd;
+  w.dX = o; o += rd;
+  w.dz = o; o += align256((size_t)sh.T * sh.N_r * 2);
+  w.dur = o; o += align256((size_t)sh.T * sh.d * 4);
+  w.counts = o; o += align256((size_t)(n_seq > 0 ? n_seq : 1) * sh.N_r * 4);
+  w.total = o;
+  return w;
+}
+
+}  // namespace
+
+size_t moe_backward_workspace(moe_shape sh, int32_t n_seq) {
+  if (sh.T <= 0 || sh.N_r <= 0 || sh.d <= 0 || sh.I <= 0 || n_seq < 0) return 0;
+  return bwd_ws(sh, n_seq).total;
+}
+
+moe_status moe_backward(const void* u, const void* e, const float* s, const int32_t* topk_idx,
+                        const float* topk_gate, const int32_t* expert_offset,
+                        const int32_t* inv_row, const void* x_perm, const void* y,
+                        const moe_expert_weights* w, moe_shape sh, const int32_t* seq_offsets,
+                        int32_t n_seq, float alpha, const float* dh, float* du, float* de,
+                        float* dw_gate, float* dw_up, float* dw_down, float* dws_gate,
+                        float* dws_up, float* dws_down, void* workspace, size_t ws_bytes,
+                        void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(sh, w)) != MOE_OK) return st;
+  if (w->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (sh.N_r % 64 != 0 || n_seq < 0 || !(alpha >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(e) || !ok_ptr(de) || !ok_ptr(dw_gate) || !ok_ptr(dw_up) || !ok_ptr(dw_down))
+    return MOE_ERR_INVALID_ARG;
+  if (sh.N_s > 0 && (!ok_ptr(dws_gate) || !ok_ptr(dws_up) || !ok_ptr(dws_down)))
+    return MOE_ERR_INVALID_ARG;
+  const bool balance = n_seq > 0 && alpha != 0.f;
+  if (balance && !ok_ptr(seq_offsets)) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t cs = S(stream);
+  if (sh.T == 0) {   // no token: every gradient is zero
+    const size_t gi = (size_t)sh.I * sh.d * 4;
+    cudaError_t err = cudaMemsetAsync(de, 0, (size_t)sh.N_r * sh.d * 4, cs);
+    if (err == cudaSuccess) err = cudaMemsetAsync(dw_gate, 0, sh.N_r * gi, cs);
+    if (err == cudaSuccess) err = cudaMemsetAsync(dw_up, 0, sh.N_r * gi, cs);
+    if (err == cudaSuccess) err = cudaMemsetAsync(dw_down, 0, sh.N_r * gi, cs);
+    if (sh.N_s > 0) {
+      if (err == cudaSuccess) err = cudaMemsetAsync(dws_gate, 0, sh.N_s * gi, cs);
+      if (err == cudaSuccess) err = cudaMemsetAsync(dws_up, 0, sh.N_s * gi, cs);
+      if (err == cudaSuccess) err = cudaMemsetAsync(dws_down, 0, sh.N_s * gi, cs);
+    }
+    return cuda_status(err);
+  }
+  if (!ok_ptr(u) || !ok_ptr(s) || !ok_ptr(topk_idx) || !ok_ptr(topk_gate) || !ok_ptr(expert_offset) ||
+      !ok_ptr(inv_row) || !ok_ptr(x_perm) || !ok_ptr(y) || !ok_ptr(dh) || !ok_ptr(du))
+    return MOE_ERR_INVALID_ARG;
+  const BwdWs L = bwd_ws(sh, n_seq);
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
+  const FfnShape fs = ffn_shape(sh);
+  // the SwiGLU output and pre-activations, recomputed
+  cudaError_t err = launch_ffn_up_tc(fs, x_perm, u, expert_offset, w, bf(L.h), cs, bf(L.a), bf(L.c));
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  if (err == cudaSuccess && balance)
+    err = launch_seq_counts(topk_idx, seq_offsets, n_seq, sh.T, sh.N_r, sh.K_r, counts, cs);
+  if (err == cudaSuccess)
+    err = launch_bwd_prep(dh, y, s, topk_idx, topk_gate, inv_row, counts, seq_offsets,
+                          balance ? n_seq : 0, balance ? alpha : 0.f, sh.T, sh.d, sh.N_r, sh.K_r,
+                          sh.N_s, ws + L.dz, ws + L.dY, cs);
+  if (err == cudaSuccess) {
+    BwdGemmIo io{fs, expert_offset, w->gate, w->up, w->down, w->s_gate, w->s_up, w->s_down,
+                 x_perm, u, e, bf(L.a), bf(L.c), bf(L.h), ws + L.dY, ws + L.dz, bf(L.dA), bf(L.dC),
+                 bf(L.dX), dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down,
+                 reinterpret_cast<float*>(ws + L.dur), de};
+    err = launch_bwd_gemms(io, cs);
+  }
+  if (err == cudaSuccess)
+    err = launch_bwd_combine(dh, reinterpret_cast<const float*>(ws + L.dur), ws + L.dX, inv_row,
+                             sh.T, sh.d, sh.K_r, sh.N_s, du, cs);
+  return cuda_status(err);
+}
+
 moe_status moe_device_error(int32_t* code, int32_t clear) {
   if (code == nullptr) return MOE_ERR_INVALID_ARG;
   return cuda_status(read_dev_error(code, clear != 0));

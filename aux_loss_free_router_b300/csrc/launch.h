@@ -2,6 +2,7 @@
 // calls these; each enqueues its kernels on `st` and returns the launch status.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -65,9 +66,12 @@ cudaError_t launch_ffn_down_simt(const FfnShape& s, const float* h,
                                  const int32_t* expert_offset, const moe_expert_weights* w,
                                  float* y, cudaStream_t st);
 
+// save_a / save_c (optional, bf16 [R, I]): also write the pre-activations x W_gate^T
+// and x W_up^T (the backward pass reads them).
 cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* u,
                              const int32_t* expert_offset, const moe_expert_weights* w,
-                             void* h, cudaStream_t st);
+                             void* h, cudaStream_t st, void* save_a = nullptr,
+                             void* save_c = nullptr);
 cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h,
                                const int32_t* expert_offset, const moe_expert_weights* w,
                                void* y, cudaStream_t st);
@@ -79,6 +83,39 @@ cudaError_t launch_ffn_up_fp8(const FfnShape& s, const void* x_perm, const float
 cudaError_t launch_ffn_down_fp8(const FfnShape& s, const void* h, const float* h_scale,
                                 const int32_t* expert_offset, const moe_expert_weights* w,
                                 void* y, cudaStream_t st);
+
+// Backward pass (bwd_gemm.cu, bwd_misc.cu).  All activation arrays are in the FFN row
+// space R = T*K_r + N_s*T and bf16 unless noted.
+struct BwdGemmIo {
+  FfnShape s;
+  const int32_t* expert_offset;
+  const void *w_gate, *w_up, *w_down, *ws_gate, *ws_up, *ws_down;   // bf16 weights
+  const void* x_perm;   // [T*K_r, d]
+  const void* u;        // [T, d]
+  const void* e;        // [N_r, d]
+  const __nv_bfloat16 *a, *c, *h;   // [R, I]: pre-activations and SwiGLU output
+  const void* dY;       // [R, d]
+  const void* dz;       // [T, N_r]
+  __nv_bfloat16 *dA, *dC;           // [R, I]
+  __nv_bfloat16* dX;                // [R, d]
+  float *dw_gate, *dw_up, *dw_down, *dws_gate, *dws_up, *dws_down;
+  float* du_router;     // [T, d]
+  float* de;            // [N_r, d]
+};
+cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st);
+// Per (sequence, expert) selection counts (int32 [n_seq, N_r], zeroed here first).
+cudaError_t launch_seq_counts(const int32_t* topk_idx, const int32_t* seq_offsets, int n_seq,
+                              int T, int N_r, int K_r, int32_t* counts, cudaStream_t st);
+// Per token: dgate = dh . y rows, the gate and balance-loss backward to dz (bf16
+// [T, N_r]), and the expert-output gradients dY rows (bf16 [R, d]).
+cudaError_t launch_bwd_prep(const float* dh, const void* y, const float* s, const int32_t* topk_idx,
+                            const float* topk_gate, const int32_t* inv_row, const int32_t* counts,
+                            const int32_t* seq_offsets, int n_seq, float alpha, int T, int d,
+                            int N_r, int K_r, int N_s, void* dz, void* dY, cudaStream_t st);
+// du = dh + du_router + sum of the token's dX rows (routed slots and shared experts).
+cudaError_t launch_bwd_combine(const float* dh, const float* du_router, const void* dX,
+                               const int32_t* inv_row, int T, int d, int K_r, int N_s, float* du,
+                               cudaStream_t st);
 
 cudaError_t launch_combine(const void* u, const void* y, moe_dtype dt, const float* gate,
                            const int32_t* inv_row, int T, int d, int K_r, int N_s,

@@ -26,6 +26,10 @@ struct TcArgs {
   __nv_bfloat16* out;
   int32_t* err;
   int* tile_ctr;     // zeroed before the launch; pairs claim tiles from it in order
+  // gate/up only, optional: the pre-activations a = x W_gate^T and c = x W_up^T in bf16,
+  // in the same row space and layout as h (kept for the backward pass)
+  __nv_bfloat16* save_a = nullptr;
+  __nv_bfloat16* save_c = nullptr;
 };
 
 // silu(g) * u = g * u / (1 + e^-g), with the fast reciprocal division (the result is

@@ -278,6 +278,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         pack_bf16(swiglu(g1.x, u1.x), swiglu(g1.y, u1.y)),
                                         pack_bf16(swiglu(g1.z, u1.z), swiglu(g1.w, u1.w)));
             *reinterpret_cast<uint4*>(args.out + (row0 + j0 + tok) * N + f) = hv;
+            if (args.save_a) {
+              const size_t o = (row0 + j0 + tok) * N + f;
+              *reinterpret_cast<uint4*>(args.save_a + o) =
+                  make_uint4(pack_bf16(g0.x, g0.y), pack_bf16(g0.z, g0.w), pack_bf16(g1.x, g1.y),
+                             pack_bf16(g1.z, g1.w));
+              *reinterpret_cast<uint4*>(args.save_c + o) =
+                  make_uint4(pack_bf16(u0.x, u0.y), pack_bf16(u0.z, u0.w), pack_bf16(u1.x, u1.y),
+                             pack_bf16(u1.z, u1.w));
+            }
           }
         }
       }
@@ -314,7 +323,7 @@ constexpr CUtensorMapDataType kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
 cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* u,
                              const int32_t* expert_offset, const moe_expert_weights* w, void* h,
-                             cudaStream_t st) {
+                             cudaStream_t st, void* save_a, void* save_c) {
   if (s.T == 0) return cudaSuccess;
   CUtensorMap m[8];
   const uint64_t rb = (uint64_t)s.d * 2;
@@ -338,7 +347,8 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
   const long long t_ub = (long long)s.T * s.K_r / BT + s.N_r + (long long)s.N_s * ((s.T + BT - 1) / BT);
   static std::mutex mu;
   static int fit[64] = {};
-  TcArgs a{s, expert_offset, static_cast<__nv_bfloat16*>(h), dev_error_ptr(), nullptr};
+  TcArgs a{s, expert_offset, static_cast<__nv_bfloat16*>(h), dev_error_ptr(), nullptr,
+           static_cast<__nv_bfloat16*>(save_a), static_cast<__nv_bfloat16*>(save_c)};
   return launch_pairs(tc_gate_up_kernel, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st);
 }
 

@@ -350,6 +350,12 @@ def run_ours(args, cfg, ws, rank, local):
         balance = balance_run(moe, cfg, layer, off, dev, stream)
         decode = decode_pass(moe, cfg, x, dev, stream)
 
+    bwd = None
+    if cfg.dtype == "bf16" and not cfg.fp8 and not args.no_backward:
+        del layer                      # the backward gets its own layer (it keeps s)
+        torch.cuda.empty_cache()
+        bwd = backward_pass(moe, cfg, x, dev, stream, steps=max(3, min(K, 10)))
+
     if rank != 0:
         return
     wk = work(cfg)
@@ -405,14 +411,61 @@ def run_ours(args, cfg, ws, rank, local):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if bwd is not None:
+        line["backward"] = bwd
     if balance is not None:
         line["balance_run"] = balance
         line["decode"] = decode
     if ws == 1 and not args.no_cpu_baseline:
-        del layer, x, w
+        layer = None
+        del x, w
         torch.cuda.empty_cache()
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_tokens)
     print(json.dumps(line), flush=True)
+
+
+def backward_pass(moe, cfg, x, dev, stream, steps: int = 10) -> dict:
+    """The backward pass at the forward pass's selection (moe_backward: gradients of
+    sum(dh * h') and of the balance loss with respect to u, e and every expert weight),
+    timed over `steps` calls replayed from one CUDA graph after a forward step."""
+    w = {k: x[k] for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")}
+    lay = moe.MoELayer(T=cfg.T, d=cfg.d, N_r=cfg.N_r, K_r=cfg.K_r, N_s=cfg.N_s, I=cfg.I, G=cfg.G,
+                       M=cfg.M, e=x["e"], b=x["b"].clone(), weights=w, n_seq=cfg.n_seq,
+                       gamma=cfg.gamma, alpha=cfg.alpha, want_s=True)
+    u, off = x["u"], x["seq_offsets"]
+    lay.step(u, off, update_bias=False)
+    g = torch.Generator(device=dev).manual_seed(5)
+    dh = torch.randn(cfg.T, cfg.d, generator=g, device=dev)
+    for _ in range(3):
+        lay.backward(u, dh, off)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(steps):
+            lay.backward(u, dh, off)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if moe.device_error() != 0:
+        raise RuntimeError("device error word set during the backward pass")
+    ms = e0.elapsed_time(e1) / steps
+    R = cfg.T * cfg.K_r + cfg.N_s * cfg.T
+    ffn = 12.0 * R * cfg.d * cfg.I                    # dgrad + wgrad of the three expert GEMMs
+    router = 4.0 * cfg.T * cfg.d * cfg.N_r            # du = dz e and de = dz^T u
+    recompute = 4.0 * R * cfg.d * cfg.I               # the gate/up GEMM run again for a, c, h
+    pk = peaks()
+    del graph, lay
+    torch.cuda.empty_cache()
+    return {"ms": ms, "tokens_per_s": cfg.T / (ms / 1e3),
+            "flop_algorithmic": ffn + router, "flop_with_recompute": ffn + router + recompute,
+            "TFLOP/s_algorithmic": (ffn + router) / (ms / 1e3) / 1e12,
+            "TFLOP/s_executed": (ffn + router + recompute) / (ms / 1e3) / 1e12,
+            "frac_of_bf16_burst_executed": (ffn + router + recompute) / (ms / 1e3) / 1e12 / pk["bf16_tflops"],
+            "note": "at the forward pass's selection; the SwiGLU pre-activations are recomputed"}
 
 
 def balance_run(moe, cfg, layer, off, dev, stream, steps: int = 200) -> dict:
@@ -483,6 +536,8 @@ def main():
     ap.add_argument("--config", default="v3", choices=sorted(synth.CONFIGS))
     ap.add_argument("--cpu-tokens", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward-pass measurement (reported beside the forward)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -259,6 +259,39 @@ MOE_API moe_status moe_seq_balance_stat(const float* seq_p_sum, const int32_t* t
                                 void* stream);
 
 /* --------------------------------------------------------------------------------
+ * Backward pass of the layer at the forward pass's selection (bf16 layers).  The pages
+ * define the forward pass ([P4] Method §2: h'_t = u_t + sum_s FFN_s(u_t) +
+ * sum_k g_{k,t} FFN_{idx_k}(u_t), s_{i,t} = Sigmoid(u_t^T e_i), gates from the raw s of
+ * the selected experts); this call returns the gradients of
+ *     J = sum(dh * h') + mean over sequences of alpha * sum_i f_i P_i
+ * with respect to u, the centroids e and every expert weight, holding the selection
+ * fixed: Top-K_r and the group limit are piecewise constant, the bias b enters only the
+ * selection and gets no gradient ([P3] §1.1.3: it is moved by the sign rule), f_i counts
+ * selections and passes none; the gates pass theirs through the raw s ([P3] §1.1.2).
+ *
+ *   Forward state (from one moe_route / moe_dispatch / moe_expert_ffn step on the same
+ *   u): u [T, d] and e [N_r, d] bf16, s [T, N_r] fp32 (moe_route's s_out), topk_idx,
+ *   topk_gate, expert_offset, inv_row, x_perm [T*K_r, d] bf16, y [R, d] bf16 (the expert
+ *   outputs, R = T*K_r + N_s*T).  w: bf16 weights.  seq_offsets / n_seq / alpha: the
+ *   balance-loss term (n_seq = 0 or alpha = 0 leaves it out).
+ *   dh [T, d] fp32: dJ/dh'.
+ *   Outputs, fp32: du [T, d], de [N_r, d], dw_gate / dw_up [N_r, I, d], dw_down
+ *   [N_r, d, I], and the shared experts' dws_* [N_s, ...] (may be NULL when N_s = 0).
+ *   workspace: moe_backward_workspace(sh, n_seq) bytes.  The SwiGLU pre-activations are
+ *   recomputed (one gate/up GEMM) rather than kept from the forward pass.
+ * Requirements beyond the shape checks: N_r % 64 == 0, weights MOE_BF16. */
+MOE_API size_t moe_backward_workspace(moe_shape sh, int32_t n_seq);
+MOE_API moe_status moe_backward(const void* u, const void* e, const float* s,
+                                const int32_t* topk_idx, const float* topk_gate,
+                                const int32_t* expert_offset, const int32_t* inv_row,
+                                const void* x_perm, const void* y, const moe_expert_weights* w,
+                                moe_shape sh, const int32_t* seq_offsets, int32_t n_seq,
+                                float alpha, const float* dh, float* du, float* de,
+                                float* dw_gate, float* dw_up, float* dw_down, float* dws_gate,
+                                float* dws_up, float* dws_down, void* workspace,
+                                size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------------
  * Device error word.  Kernels that wait on asynchronous copies bound every wait;
  * a wait that runs out records MOE_ERR_TIMEOUT here and the kernel returns early.
  * Kernels that find an invalid device-resident value record MOE_ERR_INVALID_ARG.
