@@ -196,7 +196,7 @@ def dispatch(topk_idx, sh: Shape, load, expert_offset, perm_token, inv_row, u=No
     _call("moe_dispatch", _ptr(topk_idx), sh, _ptr(u), _dt(u) if u is not None else BF16,
           _ptr(u_scale), _ptr(load), _ptr(expert_offset), _ptr(perm_token), _ptr(inv_row),
           _ptr(x_perm), _ptr(x_perm_scale), _ptr(ws), ws.numel() if ws is not None else 0,
-          _stream(stream), extra_kernels=1 if x_perm is not None else 0)
+          _stream(stream), extra_kernels=_dispatch_kernels(sh, x_perm is not None) - 3)
 
 
 def dispatch_noalloc(topk_idx, sh: Shape, load, expert_offset, perm_token, inv_row, u=None,
@@ -207,7 +207,15 @@ def dispatch_noalloc(topk_idx, sh: Shape, load, expert_offset, perm_token, inv_r
     _call("moe_dispatch_noalloc", _ptr(topk_idx), sh, _ptr(u), _dt(u) if u is not None else BF16,
           _ptr(u_scale), _ptr(load), _ptr(expert_offset), _ptr(perm_token), _ptr(inv_row),
           _ptr(x_perm), _ptr(x_perm_scale), _stream(stream),
-          extra_kernels=1 if x_perm is not None else 0)
+          extra_kernels=_dispatch_kernels(sh, x_perm is not None) - 3)
+
+
+def _dispatch_kernels(sh: Shape, gather: bool) -> int:
+    """Kernels one dispatch launches: count, scan and scatter (one kernel for batches of at
+    most 2048 tokens, three above), plus the row gather."""
+    if sh.T == 0:
+        return 0
+    return (1 if sh.T <= 2048 else 3) + (1 if gather else 0)
 
 
 def quantize_e4m3(x, block_rows: int, q, scale, stream=None):
@@ -261,7 +269,7 @@ def seq_balance_stat(seq_p_sum, topk_idx, seq_offsets, n_seq: int, sh: Shape, al
                      stat_per_seq, stat_mean=None, stream=None):
     _call("moe_seq_balance_stat", _ptr(seq_p_sum), _ptr(topk_idx), _ptr(seq_offsets), n_seq, sh,
           alpha, _ptr(stat_per_seq), _ptr(stat_mean), _stream(stream),
-          extra_kernels=1 if stat_mean is not None else 0)
+          extra_kernels=1 if (stat_mean is not None and n_seq > 1) else 0)
 
 
 def backward_workspace_bytes(sh: Shape, n_seq: int) -> int:

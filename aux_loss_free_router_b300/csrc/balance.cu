@@ -39,7 +39,8 @@ constexpr int kStatSplit = 8;
 __global__ void __cluster_dims__(kStatSplit, 1, 1) __launch_bounds__(256)
     seq_stat_kernel(const float* __restrict__ seq_p_sum, const int32_t* __restrict__ topk_idx,
                     const int32_t* __restrict__ seq_offsets, int n_seq, int T, int N_r, int K_r,
-                    float alpha, float* __restrict__ stat_per_seq, int32_t* err) {
+                    float alpha, float* __restrict__ stat_per_seq, float* __restrict__ stat_mean,
+                    int32_t* err) {
   __shared__ int32_t cnt[256];
   __shared__ double term[256];
   cg::cluster_group cluster = cg::this_cluster();
@@ -79,7 +80,10 @@ __global__ void __cluster_dims__(kStatSplit, 1, 1) __launch_bounds__(256)
       if (threadIdx.x < h) term[threadIdx.x] += term[threadIdx.x + h];
       __syncthreads();
     }
-    if (threadIdx.x == 0) stat_per_seq[j] = (float)((double)alpha * term[0]);
+    if (threadIdx.x == 0) {
+      stat_per_seq[j] = (float)((double)alpha * term[0]);
+      if (stat_mean && n_seq == 1) *stat_mean = (float)((double)alpha * term[0]);   // its own mean
+    }
   }
   cluster.sync();   // the peers' histograms stay in place until CTA 0 has read them
 }
@@ -121,9 +125,10 @@ cudaError_t launch_seq_stat(const float* seq_p_sum, const int32_t* topk_idx,
                             float alpha, float* stat_per_seq, float* stat_mean,
                             cudaStream_t st) {
   seq_stat_kernel<<<n_seq * kStatSplit, 256, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, n_seq, T,
-                                                      N_r, K_r, alpha, stat_per_seq,
+                                                      N_r, K_r, alpha, stat_per_seq, stat_mean,
                                                       dev_error_ptr());
-  if (stat_mean) seq_mean_kernel<<<1, 1, 0, st>>>(stat_per_seq, n_seq, stat_mean);
+  // one sequence: the statistic kernel wrote the mean itself
+  if (stat_mean && n_seq > 1) seq_mean_kernel<<<1, 1, 0, st>>>(stat_per_seq, n_seq, stat_mean);
   return cudaGetLastError();
 }
 

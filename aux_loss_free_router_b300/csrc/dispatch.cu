@@ -2,7 +2,8 @@
 // token rows into expert order.  No token is dropped: an expert's segment holds
 // anywhere from 0 to T rows (pwwt.cn notes §1.4; szhzxw.cn "无Token丢弃").
 //
-// The token range is cut into chunks of kDispatchChunk tokens, one warp each.
+// The token range is cut into chunks of kDispatchChunk tokens, one warp each.  Batches of
+// at most 2048 tokens run count, scan and scatter in one CTA (dispatch_small_kernel).
 //   count:   per-chunk expert histogram (shared-memory integer atomics: exact),
 //            stored expert-major.
 //   scan:    one warp per expert: exclusive scan over its chunks; load = the total.
@@ -22,6 +23,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "route_select.cuh"
 
 namespace moe {
 
@@ -149,6 +151,100 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_scatter_kernel(
   }
 }
 
+// Small batches (at most kSmallChunks chunks of kDispatchChunk tokens): count, scan and
+// scatter in one CTA of 32 warps, the chunk counts in shared memory.  Warp w takes chunks
+// w and w + 32; the positions are the same as those of the three-kernel path (experts in
+// order, tokens ascending within each expert).
+constexpr int kSmallChunks = 64;   // T <= 2048
+
+__global__ void __launch_bounds__(1024) dispatch_small_kernel(
+    const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r, int32_t* __restrict__ load,
+    int32_t* __restrict__ expert_offset, int32_t* __restrict__ perm_token,
+    int32_t* __restrict__ inv_row, int32_t* err) {
+  extern __shared__ int32_t cnt[];            // [n_chunks][N_r], then off [N_r]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+  int32_t* off = cnt + n_chunks * N_r;
+  for (int i = threadIdx.x; i < n_chunks * N_r; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  for (int chunk = warp; chunk < n_chunks; chunk += 32) {
+    const int t0 = chunk * kDispatchChunk;
+    const int n_ent = (min(T, t0 + kDispatchChunk) - t0) * K_r;
+    const int32_t* src = topk_idx + (size_t)t0 * K_r;
+    for (int x = lane; x < n_ent; x += 32) {
+      const int ex = src[x];
+      if ((unsigned)ex < (unsigned)N_r) atomicAdd(&cnt[chunk * N_r + ex], 1);
+      else record_error(err, MOE_ERR_INVALID_ARG);
+    }
+  }
+  __syncthreads();
+  // per expert: exclusive scan over the chunks, the total is the load
+  for (int i = threadIdx.x; i < N_r; i += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int v = cnt[c * N_r + i];
+      cnt[c * N_r + i] = run;
+      run += v;
+    }
+    load[i] = run;
+    off[i] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {    // exclusive scan of the loads over the experts
+    const int span = (N_r + 31) / 32;
+    int local = 0;
+    for (int q = 0; q < span; ++q) {
+      const int i = lane * span + q;
+      if (i < N_r) local += off[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int run = incl - local;
+    for (int q = 0; q < span; ++q) {
+      const int i = lane * span + q;
+      if (i < N_r) {
+        const int v = off[i];
+        off[i] = run;
+        expert_offset[i] = run;
+        run += v;
+      }
+    }
+    if (lane == 31) expert_offset[N_r] = incl;
+  }
+  __syncthreads();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int chunk = warp; chunk < n_chunks; chunk += 32) {
+    int32_t* run = cnt + chunk * N_r;           // this chunk's next position per expert
+    for (int i = lane; i < N_r; i += 32) run[i] += off[i];
+    __syncwarp();
+    const int t0 = chunk * kDispatchChunk;
+    const int n_ent = (min(T, t0 + kDispatchChunk) - t0) * K_r;
+    const size_t e0 = (size_t)t0 * K_r;
+    for (int base = 0; base < n_ent; base += 32) {
+      const int x = base + lane;
+      const bool in_range = x < n_ent;
+      const int ex = in_range ? topk_idx[e0 + x] : -1;
+      const bool valid = in_range && (unsigned)ex < (unsigned)N_r;
+      if (in_range && !valid) inv_row[e0 + x] = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, ex);
+      const int rank = __popc(peers & lt_mask);
+      int pos = 0;
+      if (valid) pos = run[ex] + rank;
+      __syncwarp();
+      if (valid && rank == 0) run[ex] += __popc(peers);
+      __syncwarp();
+      if (valid) {
+        perm_token[pos] = (int32_t)((e0 + x) / K_r);
+        inv_row[e0 + x] = pos;
+      }
+    }
+  }
+}
+
 // 16-byte vector copy of each token's row to its K_r destination rows: one warp per
 // token and column chunk (small batches split each row over gridDim.y so that enough
 // warps have loads in flight); the chunk of blockIdx.y == 0 also copies the scales.
@@ -202,14 +298,35 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
     if (err == cudaSuccess) err = cudaMemsetAsync(expert_offset, 0, sizeof(int32_t) * (N_r + 1), st);
     return err;
   }
-  const int blocks = (n_chunks + kWarps - 1) / kWarps;
-  const size_t smem = sizeof(int32_t) * kWarps * N_r;
-  dispatch_count_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
-                                                          dev_error_ptr());
-  dispatch_scan_kernel<<<(N_r + 7) / 8, 256, 0, st>>>(ws_counts, n_chunks, N_r, load);
-  dispatch_scatter_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
-                                                            load, expert_offset, perm_token,
-                                                            inv_row);
+  if (n_chunks <= kSmallChunks) {
+    // one launch for count, scan and scatter; up to 65 x 256 counts of shared memory
+    static std::mutex mu;
+    static bool opted_in[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (!opted_in[dev]) {
+        err = cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)(sizeof(int32_t) * (kSmallChunks + 1) * kMaxExperts));
+        if (err != cudaSuccess) return err;
+        opted_in[dev] = true;
+      }
+    }
+    dispatch_small_kernel<<<1, 1024, sizeof(int32_t) * (size_t)(n_chunks + 1) * N_r, st>>>(
+        topk_idx, T, N_r, K_r, load, expert_offset, perm_token, inv_row, dev_error_ptr());
+  } else {
+    const int blocks = (n_chunks + kWarps - 1) / kWarps;
+    const size_t smem = sizeof(int32_t) * kWarps * N_r;
+    dispatch_count_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
+                                                            dev_error_ptr());
+    dispatch_scan_kernel<<<(N_r + 7) / 8, 256, 0, st>>>(ws_counts, n_chunks, N_r, load);
+    dispatch_scatter_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
+                                                              load, expert_offset, perm_token,
+                                                              inv_row);
+  }
   if (u && x_perm) {
     const int passes = (int)((row_bytes / 16 + 31) / 32);   // 512-byte passes of a warp
     const int chunks = std::min(passes, std::max(1, kGatherTargetWarps / T));
