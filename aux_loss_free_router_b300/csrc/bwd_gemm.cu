@@ -13,9 +13,11 @@
 //   kDUR   du (router part) = dz e           (dz: gradient of the affinity logits)
 //   kDE    de = dz^T u
 //
-// One persistent kernel template serves all six: single-CTA M=128 x N=128 tiles, K steps
-// of 64 through a 6-stage TMA ring of 32 KB, two 128-column TMEM accumulators (the
-// epilogue of a tile overlaps the next tile's MMAs), tiles handed out round-robin.  Each
+// One persistent kernel template serves all six: single-CTA M=128 x N=256 tiles (a tile
+// of token rows sizes N to its tokens in steps of 16), K steps of 64 through a 4-stage
+// TMA ring of 48 KB, two 256-column TMEM accumulators (the epilogue of a tile overlaps
+// the next tile's MMAs), tiles handed out round-robin.  An SM takes in 48 KB per
+// 128 x 256 x 64 MACs.  Each
 // operand is read in place, K-major or MN-major (shared-memory descriptor: 128-byte
 // swizzle; for MN-major the leading byte offset is the stride between 64-element chunks
 // of M or N and the stride byte offset the stride between 8-row groups of K), so no
@@ -35,10 +37,11 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 6, THREADS = 192;
-constexpr int OPB = 128 * BK * 2;          // one operand of a K step: 16 KB
-constexpr int STAGE = 2 * OPB;
-constexpr int TMEM_COLS = 256, ACC = 128;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, THREADS = 192;
+constexpr int OPA = BM * BK * 2;           // A of a K step: 16 KB
+constexpr int OPB = BN * BK * 2;           // B of a K step: 32 KB
+constexpr int STAGE = OPA + OPB;
+constexpr int TMEM_COLS = 512, ACC = 256;
 constexpr int SCR = 16 * 32 * 4;           // per epilogue warp: 16 columns x 32 rows fp32
 
 enum : int { kDH = 0, kDX = 1, kDWD = 2, kDWGU = 3, kDUR = 4, kDE = 5 };
@@ -143,8 +146,8 @@ __device__ __forceinline__ BTile decode(const SegTable& tab, const BwdArgs& g, i
   return b;
 }
 
-// Shared-memory descriptors of one operand chunk: K-major (128-byte rows of K) or
-// MN-major (two 64-element chunks of M or N, 8 KB apart, each with 64 rows of K).
+// Shared-memory descriptors of one operand: K-major (128-byte rows of K) or MN-major
+// (64-element chunks of M or N, 8 KB apart, each with 64 rows of K).
 __device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return tc::sdesc_sw128(saddr); }
 __device__ __forceinline__ uint64_t desc_mn(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(8192 >> 4) << 16) |
@@ -155,19 +158,19 @@ template <bool MN> __device__ __forceinline__ uint64_t desc_k16(uint64_t d, int 
   return d + (uint64_t)(MN ? 128 * kk : 2 * kk);
 }
 
-__host__ __device__ constexpr uint32_t idesc(bool a_mn, bool b_mn) {
+__host__ __device__ constexpr uint32_t idesc(bool a_mn, bool b_mn, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-// Loads of one operand chunk: MN-major -> two (64, 64) boxes at x, x + 64; K-major ->
-// one (64, 128) box.
-template <bool MN>
+// Loads of one operand of ROWS rows (M or N): MN-major -> ROWS/64 boxes of (64, 64) at
+// x, x + 64, ...; K-major -> one (64, ROWS) box.
+template <bool MN, int ROWS>
 __device__ __forceinline__ void load_op(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int x_mn,
                                         int k_or_row) {
   if (MN) {
-    tc::tma_load_2d(dst, m, bar, x_mn, k_or_row);
-    tc::tma_load_2d(dst + 8192, m, bar, x_mn + 64, k_or_row);
+#pragma unroll
+    for (int c = 0; c < ROWS / 64; ++c) tc::tma_load_2d(dst + c * 8192, m, bar, x_mn + 64 * c, k_or_row);
   } else {
     tc::tma_load_2d(dst, m, bar, k_or_row, x_mn);
   }
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (KIND == kDH || KIND == kDX) {
     const int mt = KIND == kDH ? (g.I + BM - 1) / BM : (g.d + BM - 1) / BM;
-    build_seg_table(C.tab, g.expert_offset, g.T, g.K_r, g.N_r, g.N_s, BN, mt, false, g.err);
+    build_seg_table(C.tab, g.expert_offset, g.T, g.K_r, g.N_r, g.N_s, BN, mt, true, g.err);
   } else if (KIND == kDWD || KIND == kDWGU) {
     build_seg_table(C.tab, g.expert_offset, g.T, g.K_r, g.N_r, g.N_s, 1 << 30, 1, false, g.err);
   }
@@ -242,27 +245,27 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint64_t* bar = &C.full[st];
           tc::mbar_arrive_expect_tx(bar, STAGE);
           uint8_t* sa = base + st * STAGE;
-          uint8_t* sb = sa + OPB;
+          uint8_t* sb = sa + OPA;
           if (KIND == kDH) {
-            load_op<true>(sa, sh ? &m1 : &m0, bar, b.m0, e * g.d + ks * BK);
-            load_op<false>(sb, &m4, bar, b.a_row0, ks * BK);
+            load_op<true, BM>(sa, sh ? &m1 : &m0, bar, b.m0, e * g.d + ks * BK);
+            load_op<false, BN>(sb, &m4, bar, b.a_row0, ks * BK);
           } else if (KIND == kDX) {
             const int nkI = b.nk / 2, ph = ks >= nkI, kk = ks - ph * nkI;
             const CUtensorMap* ma = ph ? (sh ? &m3 : &m1) : (sh ? &m2 : &m0);
-            load_op<true>(sa, ma, bar, b.m0, e * g.I + kk * BK);
-            load_op<false>(sb, ph ? &m5 : &m4, bar, b.a_row0, kk * BK);
+            load_op<true, BM>(sa, ma, bar, b.m0, e * g.I + kk * BK);
+            load_op<false, BN>(sb, ph ? &m5 : &m4, bar, b.a_row0, kk * BK);
           } else if (KIND == kDWD) {
-            load_op<true>(sa, &m0, bar, b.m0, b.a_row0 + ks * BK);
-            load_op<true>(sb, &m4, bar, b.n0, b.b_row0 + ks * BK);
+            load_op<true, BM>(sa, &m0, bar, b.m0, b.a_row0 + ks * BK);
+            load_op<true, BN>(sb, &m4, bar, b.n0, b.b_row0 + ks * BK);
           } else if (KIND == kDWGU) {
-            load_op<true>(sa, b.part ? &m1 : &m0, bar, b.m0, b.a_row0 + ks * BK);
-            load_op<true>(sb, sh ? &m5 : &m4, bar, b.n0, b.b_row0 + ks * BK);
+            load_op<true, BM>(sa, b.part ? &m1 : &m0, bar, b.m0, b.a_row0 + ks * BK);
+            load_op<true, BN>(sb, sh ? &m5 : &m4, bar, b.n0, b.b_row0 + ks * BK);
           } else if (KIND == kDUR) {
-            load_op<false>(sa, &m0, bar, b.m0, ks * BK);
-            load_op<true>(sb, &m4, bar, b.n0, ks * BK);
+            load_op<false, BM>(sa, &m0, bar, b.m0, ks * BK);
+            load_op<true, BN>(sb, &m4, bar, b.n0, ks * BK);
           } else {
-            load_op<true>(sa, &m0, bar, b.m0, ks * BK);
-            load_op<true>(sb, &m4, bar, b.n0, ks * BK);
+            load_op<true, BM>(sa, &m0, bar, b.m0, ks * BK);
+            load_op<true, BN>(sb, &m4, bar, b.n0, ks * BK);
           }
         }
       }
@@ -272,9 +275,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ---------------------------------------------------------- MMA issuer --
       int it = 0, tcount = 0;
       bool ok = true;
-      const uint32_t id = idesc(Tr::A_MN, Tr::B_MN);
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
         const BTile b = decode<KIND>(C.tab, g, tile);
+        // token tiles: N sized to the tile's tokens in steps of 16
+        const uint32_t id = idesc(Tr::A_MN, Tr::B_MN, Tr::TRANSPOSED ? (b.n_tok + 15) & ~15 : BN);
         const int acc = tcount & 1;
         if (!tc::mbar_wait(&C.tempty[acc], ((tcount >> 1) & 1) ^ 1, abort_flag, g.err)) break;
         tc::fence_after_sync();
@@ -287,9 +291,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           int k16 = BK / 16;
           if (Tr::ROW_K && ks == b.nk - 1 && b.kv_last < BK) {
             // rows kv_last .. (next multiple of 16) - 1 hold the next segment's rows: zero
-            // them (whole 128-byte rows, so the swizzle does not matter) in all four chunks
+            // them (whole 128-byte rows, so the swizzle does not matter) in all six 8 KB
+            // chunks of the stage (two of A, four of B)
             const int kv = b.kv_last, kend = (kv + 15) & ~15;
-            for (int ch = 0; ch < 4; ++ch)
+            for (int ch = 0; ch < STAGE / 8192; ++ch)
               for (int r = kv; r < kend; ++r) {
                 uint4* row = reinterpret_cast<uint4*>(sa + ch * 8192 + r * 128);
 #pragma unroll
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t s0 = tc::smem_u32(sa);
           const uint64_t ad = Tr::A_MN ? desc_mn(s0) : desc_k(s0);
-          const uint64_t bd = Tr::B_MN ? desc_mn(s0 + OPB) : desc_k(s0 + OPB);
+          const uint64_t bd = Tr::B_MN ? desc_mn(s0 + OPA) : desc_k(s0 + OPA);
           for (int kk = 0; kk < k16; ++kk)
             tc::mma_bf16(d_tmem, desc_k16<Tr::A_MN>(ad, kk), desc_k16<Tr::B_MN>(bd, kk), id,
                          (ks | kk) != 0);
@@ -438,9 +443,9 @@ constexpr CUtensorMapDataType kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 bool map_mn(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows) {
   return make_tmap_2d(m, kBF16, p, inner, rows, inner * 2, 64, 64);
 }
-// K-major map: inner = K (contiguous), outer = M/N rows; box 64 x 128.
-bool map_k(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows) {
-  return make_tmap_2d(m, kBF16, p, inner, rows, inner * 2, 64, 128);
+// K-major map: inner = K (contiguous), outer = M/N rows; box 64 x `box_rows`.
+bool map_k(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  return make_tmap_2d(m, kBF16, p, inner, rows, inner * 2, 64, box_rows);
 }
 
 template <int KIND>
@@ -489,7 +494,7 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
 
   // dH = dY W_down, then the SwiGLU backward -> dA, dC
   if (!map_mn(&m[0], io.w_down, s.I, (uint64_t)s.N_r * s.d) || !map_mn(&m[1], wsd, s.I, Es * s.d) ||
-      !map_k(&m[4], io.dY, s.d, R))
+      !map_k(&m[4], io.dY, s.d, R, BN))
     return cudaErrorInvalidValue;
   same(2);
   g.o_bf0 = io.dA;
@@ -499,7 +504,7 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
   // dX = dA W_gate + dC W_up
   if (!map_mn(&m[0], io.w_gate, s.d, (uint64_t)s.N_r * s.I) ||
       !map_mn(&m[1], io.w_up, s.d, (uint64_t)s.N_r * s.I) || !map_mn(&m[2], wsg, s.d, Es * s.I) ||
-      !map_mn(&m[3], wsu, s.d, Es * s.I) || !map_k(&m[4], io.dA, s.I, R) || !map_k(&m[5], io.dC, s.I, R))
+      !map_mn(&m[3], wsu, s.d, Es * s.I) || !map_k(&m[4], io.dA, s.I, R, BN) || !map_k(&m[5], io.dC, s.I, R, BN))
     return cudaErrorInvalidValue;
   g.o_bf0 = io.dX;
   g.o_bf1 = nullptr;
@@ -528,7 +533,7 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
     return err;
 
   // router: du = dz e, de = dz^T u
-  if (!map_k(&m[0], io.dz, s.N_r, s.T) || !map_mn(&m[4], io.e, s.d, s.N_r)) return cudaErrorInvalidValue;
+  if (!map_k(&m[0], io.dz, s.N_r, s.T, BM) || !map_mn(&m[4], io.e, s.d, s.N_r)) return cudaErrorInvalidValue;
   same(1);
   g.o_f0 = io.du_router;
   g.o_f1 = g.o_fs0 = g.o_fs1 = nullptr;
