@@ -331,8 +331,42 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (Tr::TRANSPOSED) {
         // lane = feature m0 + 32q + lane, column = token; out rows are tokens
         const int Fx = KIND == kDH ? g.I : g.d;
+        if (KIND == kDH) {
+          // bring the next tile's pre-activations into L2 while this tile is written
+          const int nt = tile + gridDim.x;
+          if (nt < total) {
+            const BTile nb = decode<KIND>(C.tab, g, nt);
+            const int f0 = nb.m0 + q * 32;
+            if (f0 < Fx)
+              for (int r = lane; r < nb.n_tok; r += 32) {
+                const size_t o = (size_t)(nb.a_row0 + r) * Fx + f0;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(g.a + o));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(g.c + o));
+              }
+          }
+        }
+        // a and c of a 16-token group are loaded one group ahead of their use
+        uint4 pa[2], pc[2];
+        auto fetch = [&](int j0) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int item = i * 32 + lane, tok = item >> 2, piece = item & 3;
+            const int f = b.m0 + q * 32 + piece * 8;
+            pa[i] = pc[i] = make_uint4(0, 0, 0, 0);
+            if (KIND == kDH && j0 + tok < b.n_tok && f < Fx) {
+              const size_t o = (size_t)(b.a_row0 + j0 + tok) * Fx + f;
+              pa[i] = *reinterpret_cast<const uint4*>(g.a + o);
+              pc[i] = *reinterpret_cast<const uint4*>(g.c + o);
+            }
+          }
+        };
+        if (KIND == kDH) fetch(0);
 #pragma unroll 1
         for (int j0 = 0; j0 < b.n_tok; j0 += 16) {
+          uint4 ca[2], cc2[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) { ca[i] = pa[i]; cc2[i] = pc[i]; }
+          if (KIND == kDH && j0 + 16 < b.n_tok) fetch(j0 + 16);
           uint32_t r[16];
           tc::tmem_ld16(t_base + j0, r);
           tc::tmem_ld_wait();
@@ -350,8 +384,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int x = 0; x < 8; ++x) v[x] = scr[tok * 32 + piece * 8 + x];
               if (KIND == kDH) {
-                const uint4 av = *reinterpret_cast<const uint4*>(g.a + o);
-                const uint4 cv = *reinterpret_cast<const uint4*>(g.c + o);
+                const uint4 av = ca[i];
+                const uint4 cv = cc2[i];
                 const __nv_bfloat16* ah = reinterpret_cast<const __nv_bfloat16*>(&av);
                 const __nv_bfloat16* ch = reinterpret_cast<const __nv_bfloat16*>(&cv);
                 uint4 da, dc;
@@ -394,6 +428,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           Nx = g.d;
           out = g.o_f0;
         }
+        // each lane writes its row's 32 columns per TMEM load as eight 16-byte pieces
+        // (staging through shared memory for 128-byte row stores measured slower: the
+        // extra shared-memory traffic competes with the MMAs' operand reads)
         const int row = b.m0 + q * 32 + lane;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
