@@ -211,11 +211,13 @@ def dispatch_noalloc(topk_idx, sh: Shape, load, expert_offset, perm_token, inv_r
 
 
 def _dispatch_kernels(sh: Shape, gather: bool) -> int:
-    """Kernels one dispatch launches: count, scan and scatter (one kernel for batches of at
-    most 2048 tokens, three above), plus the row gather."""
+    """Kernels one dispatch launches: count, scan and scatter (one kernel while each 32nd
+    of the tokens holds at most 512 (token, slot) entries, three above), plus the row
+    gather."""
     if sh.T == 0:
         return 0
-    return (1 if sh.T <= 2048 else 3) + (1 if gather else 0)
+    small = ((sh.T + 31) // 32) * sh.K_r <= 512
+    return (1 if small else 3) + (1 if gather else 0)
 
 
 def quantize_e4m3(x, block_rows: int, q, scale, stream=None):
@@ -380,6 +382,8 @@ class MoELayer:
         self.stat = z(self.n_seq, dtype=torch.float32)
         self.stat_mean = z(1, dtype=torch.float32)
         self.ws_route = _workspace(route_workspace_bytes(self.shape, self.n_seq), dev)
+        # the bias update and the statistic run on a second stream beside the expert FFNs
+        self._side = torch.cuda.Stream(device=dev) if dev.type == "cuda" else None
         self.ws_dispatch = _workspace(dispatch_workspace_bytes(self.shape), dev)
 
     def step(self, u: torch.Tensor, seq_offsets: torch.Tensor, update_bias: bool = True,
@@ -391,7 +395,8 @@ class MoELayer:
         shape and dtype as ``self.out``) when given, else to ``self.out``."""
         sh = self.shape
         out = self.out if out is None else out
-        ev = (lambda i: events[i].record(stream)) if events else (lambda i: None)
+        main = stream if stream is not None else torch.cuda.current_stream(self.e.device)
+        ev = (lambda i: events[i].record(main)) if events else (lambda i: None)
         ev(0)
         route(u, self.e, self.b, sh, self.topk_idx, self.topk_gate, self.s_out, seq_offsets,
               self.n_seq, self.seq_p_sum, self.ws_route, stream)
@@ -401,6 +406,7 @@ class MoELayer:
             dispatch(self.topk_idx, sh, self.load, self.expert_offset, self.perm_token,
                      self.inv_row, self.u_q, self.x_perm, self.u_scale, self.x_perm_scale,
                      workspace=self.ws_dispatch, stream=stream)
+            joined = self._end_of_step(main, seq_offsets, update_bias)
             ev(2)
             expert_gate_up(self.x_perm, self.u_q, self.expert_offset, sh, self.ffn_weights,
                            self.h_mid, self.x_perm_scale, self.u_scale, self.h_scale,
@@ -411,6 +417,7 @@ class MoELayer:
         else:
             dispatch(self.topk_idx, sh, self.load, self.expert_offset, self.perm_token,
                      self.inv_row, u, self.x_perm, workspace=self.ws_dispatch, stream=stream)
+            joined = self._end_of_step(main, seq_offsets, update_bias)
             ev(2)
             expert_gate_up(self.x_perm, u, self.expert_offset, sh, self.ffn_weights, self.h_mid,
                            stream=stream)
@@ -419,12 +426,24 @@ class MoELayer:
                         stream=stream)
         ev(4)
         combine(u, self.y, self.topk_gate, self.inv_row, sh, out, stream=stream)
-        if update_bias:
-            bias_update(self.b, self.load, sh, self.gamma, stream=stream)
-        seq_balance_stat(self.seq_p_sum, self.topk_idx, seq_offsets, self.n_seq, sh, self.alpha,
-                         self.stat, self.stat_mean, stream=stream)
+        main.wait_event(joined)
         ev(5)
         return out
+
+    def _end_of_step(self, main, seq_offsets, update_bias: bool):
+        """b <- b + gamma*sign(mean - load) and the sequence statistic on the side
+        stream, once the dispatch has written the loads; returns the event the main
+        stream waits on before the step ends (the next step's routing reads b)."""
+        forked = torch.cuda.Event()
+        forked.record(main)
+        self._side.wait_event(forked)
+        if update_bias:
+            bias_update(self.b, self.load, self.shape, self.gamma, stream=self._side)
+        seq_balance_stat(self.seq_p_sum, self.topk_idx, seq_offsets, self.n_seq, self.shape,
+                         self.alpha, self.stat, self.stat_mean, stream=self._side)
+        joined = torch.cuda.Event()
+        joined.record(self._side)
+        return joined
 
     def pipeline(self, u_host: list, out_host: list, seq_offsets: torch.Tensor,
                  load_host: Optional[list] = None, stat_host: Optional[list] = None) -> None:

@@ -19,6 +19,8 @@ __device__ int32_t g_dev_error = 0;
 // mean stay (pwwt.cn notes §1.1.3; gamma = 0.001 in the reading guide, Method §2).
 __global__ void bias_update_kernel(float* __restrict__ b, const int32_t* __restrict__ load,
                                    long long total, int N_r, float gamma) {
+  pdl_release();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= N_r) return;
   const long long diff = total - (long long)N_r * load[i];
@@ -43,6 +45,8 @@ __global__ void __cluster_dims__(kStatSplit, 1, 1) __launch_bounds__(256)
                     int32_t* err) {
   __shared__ int32_t cnt[256];
   __shared__ double term[256];
+  pdl_release();
+  pdl_wait();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int j = blockIdx.x / kStatSplit;
@@ -91,6 +95,8 @@ __global__ void __cluster_dims__(kStatSplit, 1, 1) __launch_bounds__(256)
 // Mean over sequences, summed in order in fp64 (one thread: n_seq is small).
 __global__ void seq_mean_kernel(const float* __restrict__ stat_per_seq, int n_seq,
                                 float* __restrict__ stat_mean) {
+  pdl_release();
+  pdl_wait();
   double s = 0.0;
   for (int j = 0; j < n_seq; ++j) s += (double)stat_per_seq[j];
   *stat_mean = n_seq > 0 ? (float)(s / n_seq) : 0.f;
@@ -116,20 +122,22 @@ cudaError_t read_dev_error(int32_t* code, bool clear) {
 
 cudaError_t launch_bias_update(float* b, const int32_t* load, int T, int N_r, int K_r,
                                float gamma, cudaStream_t st) {
-  bias_update_kernel<<<(N_r + 255) / 256, 256, 0, st>>>(b, load, (long long)T * K_r, N_r, gamma);
-  return cudaGetLastError();
+  const cudaError_t err = launch_pdl(bias_update_kernel, dim3((N_r + 255) / 256), dim3(256), 0, st, 0, b,
+                                     load, (long long)T * K_r, N_r, gamma);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_seq_stat(const float* seq_p_sum, const int32_t* topk_idx,
                             const int32_t* seq_offsets, int n_seq, int T, int N_r, int K_r,
                             float alpha, float* stat_per_seq, float* stat_mean,
                             cudaStream_t st) {
-  seq_stat_kernel<<<n_seq * kStatSplit, 256, 0, st>>>(seq_p_sum, topk_idx, seq_offsets, n_seq, T,
-                                                      N_r, K_r, alpha, stat_per_seq, stat_mean,
-                                                      dev_error_ptr());
+  cudaError_t err = launch_pdl(seq_stat_kernel, dim3(n_seq * kStatSplit), dim3(256), 0, st, 0, seq_p_sum,
+                               topk_idx, seq_offsets, n_seq, T, N_r, K_r, alpha, stat_per_seq,
+                               stat_mean, dev_error_ptr());
   // one sequence: the statistic kernel wrote the mean itself
-  if (stat_mean && n_seq > 1) seq_mean_kernel<<<1, 1, 0, st>>>(stat_per_seq, n_seq, stat_mean);
-  return cudaGetLastError();
+  if (err == cudaSuccess && stat_mean && n_seq > 1)
+    err = launch_pdl(seq_mean_kernel, dim3(1), dim3(1), 0, st, 0, (const float*)stat_per_seq, n_seq, stat_mean);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace moe

@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const TIn* __restrict__ u,
                                                       int pass_per_chunk,
                                                       TOut* __restrict__ out, int32_t* err) {
   constexpr int V = Vec<TIn>::N;
+  pdl_release();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
@@ -133,10 +135,10 @@ cudaError_t run(const void* u, const void* y, const float* gate, const int32_t* 
   const int chunks = std::min(passes, std::max(1, kTargetWarps / T));
   const int ppc = (passes + chunks - 1) / chunks;
   const dim3 grid((T + 7) / 8, (passes + ppc - 1) / ppc);
-  combine_kernel<TIn, TOut><<<grid, 256, 0, st>>>(
-      (const TIn*)u, (const TIn*)y, gate, inv_row, T, d, K_r, N_s, ppc, (TOut*)out,
-      dev_error_ptr());
-  return cudaGetLastError();
+  const cudaError_t err = launch_pdl(combine_kernel<TIn, TOut>, grid, dim3(256), 0, st, 0, (const TIn*)u,
+                                     (const TIn*)y, gate, inv_row, T, d, K_r, N_s, ppc, (TOut*)out,
+                                     dev_error_ptr());
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace

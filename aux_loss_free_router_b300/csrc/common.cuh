@@ -66,4 +66,42 @@ __device__ __forceinline__ KeyIdxVal warp_argmax(KeyIdxVal a) {
 
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
+// Programmatic dependent launch.  The forward kernels are launched with launch_pdl, so
+// the GPU may schedule a kernel while the one before it in the stream still runs.  Each
+// such kernel calls pdl_wait() before its first access to global memory that another
+// kernel writes, and before allocating tensor memory: the wait returns once the previous
+// kernel has completed and its writes are visible (a kernel launched without the
+// attribute, or after a non-kernel node, returns at once).  pdl_release() lets the next
+// kernel in the stream be scheduled; it is issued first thing, and the next kernel's
+// blocks then wait in their own pdl_wait().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kernel` with the programmatic-serialization attribute (and a cluster shape when
+// cluster_x > 1; kernels with compiled-in cluster dimensions pass 0).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       unsigned cluster_x, Args... args) {
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace moe

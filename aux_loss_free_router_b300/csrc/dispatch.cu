@@ -2,8 +2,9 @@
 // token rows into expert order.  No token is dropped: an expert's segment holds
 // anywhere from 0 to T rows (pwwt.cn notes §1.4; szhzxw.cn "无Token丢弃").
 //
-// The token range is cut into chunks of kDispatchChunk tokens, one warp each.  Batches of
-// at most 2048 tokens run count, scan and scatter in one CTA (dispatch_small_kernel).
+// The token range is cut into chunks of kDispatchChunk tokens, one warp each.  Batches
+// with at most 512 (token, slot) entries per 32nd of the tokens (T <= 2048 at K_r = 8) run
+// count, scan and scatter in one CTA (dispatch_small_kernel).
 //   count:   per-chunk expert histogram (shared-memory integer atomics: exact),
 //            stored expert-major.
 //   scan:    one warp per expert: exclusive scan over its chunks; load = the total.
@@ -37,6 +38,8 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_count_kernel(
     const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r, int32_t* __restrict__ counts,
     int32_t* err) {
   extern __shared__ int32_t cnt_sm[];
+  pdl_release();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kWarps + warp;
   const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
@@ -62,6 +65,8 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_count_kernel(
 __global__ void __launch_bounds__(256) dispatch_scan_kernel(int32_t* __restrict__ counts,
                                                             int n_chunks, int N_r,
                                                             int32_t* __restrict__ load) {
+  pdl_release();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (i >= N_r) return;
@@ -117,6 +122,8 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_scatter_kernel(
     int32_t* __restrict__ expert_offset, int32_t* __restrict__ perm_token,
     int32_t* __restrict__ inv_row) {
   extern __shared__ int32_t run_sm[];
+  pdl_release();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kWarps + warp;
   const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
@@ -151,29 +158,43 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_scatter_kernel(
   }
 }
 
-// Small batches (at most kSmallChunks chunks of kDispatchChunk tokens): count, scan and
-// scatter in one CTA of 32 warps, the chunk counts in shared memory.  Warp w takes chunks
-// w and w + 32; the positions are the same as those of the three-kernel path (experts in
-// order, tokens ascending within each expert).
-constexpr int kSmallChunks = 64;   // T <= 2048
+// Small batches: count, scan and scatter in one CTA of 32 warps.  Warp w takes the w-th
+// of 32 contiguous token chunks of ceil(T/32) tokens and loads its (token, slot) entries
+// once, kSmallPerLane per lane, into registers; the chunk counts live in shared memory.
+// The positions do not depend on the chunking (experts in order, tokens ascending within
+// each expert): they are those of the three-kernel path.
+constexpr int kSmallWarps = 32;
+constexpr int kSmallPerLane = 16;   // entries per warp <= 32 * 16 = 512 (e.g. T = 2048, K_r = 8)
 
-__global__ void __launch_bounds__(1024) dispatch_small_kernel(
+__host__ __device__ inline bool dispatch_small_ok(int T, int K_r) {
+  return (long long)((T + kSmallWarps - 1) / kSmallWarps) * K_r <= 32 * kSmallPerLane;
+}
+
+__global__ void __launch_bounds__(kSmallWarps * 32) dispatch_small_kernel(
     const int32_t* __restrict__ topk_idx, int T, int N_r, int K_r, int32_t* __restrict__ load,
     int32_t* __restrict__ expert_offset, int32_t* __restrict__ perm_token,
     int32_t* __restrict__ inv_row, int32_t* err) {
-  extern __shared__ int32_t cnt[];            // [n_chunks][N_r], then off [N_r]
+  extern __shared__ int32_t cnt[];            // [kSmallWarps][N_r], then off [N_r]
+  pdl_release();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_chunks = (T + kDispatchChunk - 1) / kDispatchChunk;
-  int32_t* off = cnt + n_chunks * N_r;
-  for (int i = threadIdx.x; i < n_chunks * N_r; i += blockDim.x) cnt[i] = 0;
-  __syncthreads();
-  for (int chunk = warp; chunk < n_chunks; chunk += 32) {
-    const int t0 = chunk * kDispatchChunk;
-    const int n_ent = (min(T, t0 + kDispatchChunk) - t0) * K_r;
-    const int32_t* src = topk_idx + (size_t)t0 * K_r;
-    for (int x = lane; x < n_ent; x += 32) {
-      const int ex = src[x];
-      if ((unsigned)ex < (unsigned)N_r) atomicAdd(&cnt[chunk * N_r + ex], 1);
+  int32_t* off = cnt + kSmallWarps * N_r;
+  for (int i = threadIdx.x; i < kSmallWarps * N_r; i += blockDim.x) cnt[i] = 0;
+  const int ct = (T + kSmallWarps - 1) / kSmallWarps;
+  const int t0 = min(T, warp * ct), t1 = min(T, t0 + ct);
+  const int n_ent = (t1 - t0) * K_r;                 // the same for every lane of the warp
+  const size_t e0 = (size_t)t0 * K_r;
+  pdl_wait();
+  int ex[kSmallPerLane];
+#pragma unroll
+  for (int j = 0; j < kSmallPerLane; ++j) {
+    const int x = j * 32 + lane;
+    ex[j] = x < n_ent ? topk_idx[e0 + x] : -1;
+  }
+  __syncthreads();                                   // counts zeroed
+#pragma unroll
+  for (int j = 0; j < kSmallPerLane; ++j) {
+    if (j * 32 + lane < n_ent) {
+      if ((unsigned)ex[j] < (unsigned)N_r) atomicAdd(&cnt[warp * N_r + ex[j]], 1);
       else record_error(err, MOE_ERR_INVALID_ARG);
     }
   }
@@ -181,7 +202,7 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
   // per expert: exclusive scan over the chunks, the total is the load
   for (int i = threadIdx.x; i < N_r; i += blockDim.x) {
     int run = 0;
-    for (int c = 0; c < n_chunks; ++c) {
+    for (int c = 0; c < kSmallWarps; ++c) {
       const int v = cnt[c * N_r + i];
       cnt[c * N_r + i] = run;
       run += v;
@@ -217,30 +238,27 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
   }
   __syncthreads();
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int chunk = warp; chunk < n_chunks; chunk += 32) {
-    int32_t* run = cnt + chunk * N_r;           // this chunk's next position per expert
-    for (int i = lane; i < N_r; i += 32) run[i] += off[i];
+  int32_t* run = cnt + warp * N_r;                   // this chunk's next position per expert
+  for (int i = lane; i < N_r; i += 32) run[i] += off[i];
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < kSmallPerLane; ++j) {
+    if (j * 32 >= n_ent) break;                      // warp-uniform
+    const int x = j * 32 + lane;
+    const bool in_range = x < n_ent;
+    const int e = in_range ? ex[j] : -1;
+    const bool valid = in_range && (unsigned)e < (unsigned)N_r;
+    if (in_range && !valid) inv_row[e0 + x] = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    int pos = 0;
+    if (valid) pos = run[e] + rank;
     __syncwarp();
-    const int t0 = chunk * kDispatchChunk;
-    const int n_ent = (min(T, t0 + kDispatchChunk) - t0) * K_r;
-    const size_t e0 = (size_t)t0 * K_r;
-    for (int base = 0; base < n_ent; base += 32) {
-      const int x = base + lane;
-      const bool in_range = x < n_ent;
-      const int ex = in_range ? topk_idx[e0 + x] : -1;
-      const bool valid = in_range && (unsigned)ex < (unsigned)N_r;
-      if (in_range && !valid) inv_row[e0 + x] = -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, ex);
-      const int rank = __popc(peers & lt_mask);
-      int pos = 0;
-      if (valid) pos = run[ex] + rank;
-      __syncwarp();
-      if (valid && rank == 0) run[ex] += __popc(peers);
-      __syncwarp();
-      if (valid) {
-        perm_token[pos] = (int32_t)((e0 + x) / K_r);
-        inv_row[e0 + x] = pos;
-      }
+    if (valid && rank == 0) run[e] += __popc(peers);
+    __syncwarp();
+    if (valid) {
+      perm_token[pos] = (int32_t)((e0 + x) / K_r);
+      inv_row[e0 + x] = pos;
     }
   }
 }
@@ -252,6 +270,8 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(
     const uint8_t* __restrict__ u, size_t row_bytes, const float* __restrict__ u_scale,
     int scale_cols, const int32_t* __restrict__ inv_row, int T, int K_r, int pass_per_chunk,
     uint8_t* __restrict__ x_perm, float* __restrict__ x_perm_scale) {
+  pdl_release();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
@@ -298,43 +318,35 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int N_r, int K_r,
     if (err == cudaSuccess) err = cudaMemsetAsync(expert_offset, 0, sizeof(int32_t) * (N_r + 1), st);
     return err;
   }
-  if (n_chunks <= kSmallChunks) {
-    // one launch for count, scan and scatter; up to 65 x 256 counts of shared memory
-    static std::mutex mu;
-    static bool opted_in[64] = {};
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+  if (dispatch_small_ok(T, K_r)) {
+    // one launch for count, scan and scatter; at most 33 x 256 counts of shared memory
+    const cudaError_t err = launch_pdl(dispatch_small_kernel, dim3(1), dim3(kSmallWarps * 32),
+                                       sizeof(int32_t) * (size_t)(kSmallWarps + 1) * N_r, st, 0, topk_idx,
+                                       T, N_r, K_r, load, expert_offset, perm_token, inv_row, dev_error_ptr());
     if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    {
-      std::lock_guard<std::mutex> lock(mu);
-      if (!opted_in[dev]) {
-        err = cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)(sizeof(int32_t) * (kSmallChunks + 1) * kMaxExperts));
-        if (err != cudaSuccess) return err;
-        opted_in[dev] = true;
-      }
-    }
-    dispatch_small_kernel<<<1, 1024, sizeof(int32_t) * (size_t)(n_chunks + 1) * N_r, st>>>(
-        topk_idx, T, N_r, K_r, load, expert_offset, perm_token, inv_row, dev_error_ptr());
   } else {
     const int blocks = (n_chunks + kWarps - 1) / kWarps;
     const size_t smem = sizeof(int32_t) * kWarps * N_r;
-    dispatch_count_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
-                                                            dev_error_ptr());
-    dispatch_scan_kernel<<<(N_r + 7) / 8, 256, 0, st>>>(ws_counts, n_chunks, N_r, load);
-    dispatch_scatter_kernel<<<blocks, kWarps * 32, smem, st>>>(topk_idx, T, N_r, K_r, ws_counts,
-                                                              load, expert_offset, perm_token,
-                                                              inv_row);
+    cudaError_t err = launch_pdl(dispatch_count_kernel, dim3(blocks), dim3(kWarps * 32), smem, st, 0,
+                                 topk_idx, T, N_r, K_r, ws_counts, dev_error_ptr());
+    if (err == cudaSuccess)
+      err = launch_pdl(dispatch_scan_kernel, dim3((N_r + 7) / 8), dim3(256), 0, st, 0, ws_counts,
+                       n_chunks, N_r, load);
+    if (err == cudaSuccess)
+      err = launch_pdl(dispatch_scatter_kernel, dim3(blocks), dim3(kWarps * 32), smem, st, 0, topk_idx,
+                       T, N_r, K_r, (const int32_t*)ws_counts, (const int32_t*)load, expert_offset,
+                       perm_token, inv_row);
+    if (err != cudaSuccess) return err;
   }
   if (u && x_perm) {
     const int passes = (int)((row_bytes / 16 + 31) / 32);   // 512-byte passes of a warp
     const int chunks = std::min(passes, std::max(1, kGatherTargetWarps / T));
     const int ppc = (passes + chunks - 1) / chunks;
     const dim3 grid((T + 7) / 8, (passes + ppc - 1) / ppc);
-    dispatch_gather_kernel<<<grid, 256, 0, st>>>(
-        (const uint8_t*)u, row_bytes, u_scale, scale_cols, inv_row, T, K_r, ppc,
-        (uint8_t*)x_perm, x_perm_scale);
+    const cudaError_t err = launch_pdl(dispatch_gather_kernel, grid, dim3(256), 0, st, 0, (const uint8_t*)u,
+                                       row_bytes, u_scale, scale_cols, (const int32_t*)inv_row, T, K_r,
+                                       ppc, (uint8_t*)x_perm, x_perm_scale);
+    if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
 }

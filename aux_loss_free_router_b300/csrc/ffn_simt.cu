@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(FfnShape s, const float* 
   __shared__ float As[BK][BM + 1];   // +1: the transposing stores hit 32 banks
   __shared__ float B0[BK][BN + 1];
   __shared__ float B1[BK][BN + 1];
+  pdl_release();
+  pdl_wait();
   const int K = MODE == 0 ? s.d : s.I;
   const int N = MODE == 0 ? s.I : s.d;
   const int n_tiles_n = (N + BN - 1) / BN;
@@ -129,20 +131,22 @@ cudaError_t launch_ffn_up_simt(const FfnShape& s, const float* x_perm, const flo
                                const int32_t* expert_offset, const moe_expert_weights* w,
                                float* h, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
-  ffn_simt_kernel<0><<<grid_for(s, s.I), 256, 0, st>>>(
-      s, x_perm, u, expert_offset, (const float*)w->gate, (const float*)w->up,
-      (const float*)w->s_gate, (const float*)w->s_up, h, dev_error_ptr());
-  return cudaGetLastError();
+  const cudaError_t err = launch_pdl(ffn_simt_kernel<0>, dim3(grid_for(s, s.I)), dim3(256), 0, st, 0, s,
+                                     x_perm, u, expert_offset, (const float*)w->gate,
+                                     (const float*)w->up, (const float*)w->s_gate,
+                                     (const float*)w->s_up, h, dev_error_ptr());
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_ffn_down_simt(const FfnShape& s, const float* h,
                                  const int32_t* expert_offset, const moe_expert_weights* w,
                                  float* y, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
-  ffn_simt_kernel<1><<<grid_for(s, s.d), 256, 0, st>>>(
-      s, h, nullptr, expert_offset, (const float*)w->down, nullptr, (const float*)w->s_down,
-      nullptr, y, dev_error_ptr());
-  return cudaGetLastError();
+  const cudaError_t err = launch_pdl(ffn_simt_kernel<1>, dim3(grid_for(s, s.d)), dim3(256), 0, st, 0, s, h,
+                                     (const float*)nullptr, expert_offset, (const float*)w->down,
+                                     (const float*)nullptr, (const float*)w->s_down,
+                                     (const float*)nullptr, y, dev_error_ptr());
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace moe

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const TIn* __restrict_
                                                           long long rows, long long cols,
                                                           uint8_t* __restrict__ q,
                                                           float* __restrict__ scale) {
+  pdl_release();
+  pdl_wait();
   const long long tiles_per_row = cols / 128;
   const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -55,6 +57,8 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const TIn* __restric
                                                             uint8_t* __restrict__ q,
                                                             float* __restrict__ scale) {
   __shared__ float red[8];
+  pdl_release();
+  pdl_wait();
   const long long br = blockIdx.y, bc = blockIdx.x;
   const TIn* base = x + br * 128 * cols + bc * 128;
   float amax = 0.f;
@@ -82,23 +86,26 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const TIn* __restric
 cudaError_t launch_quantize_e4m3(const void* x, moe_dtype x_dt, int64_t rows, int64_t cols,
                                  int block_rows, uint8_t* q, float* scale, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
+  cudaError_t err;
   if (block_rows == 1) {
     const long long warps = rows * (cols / 128);
-    const unsigned blocks = (unsigned)((warps + 7) / 8);
+    const dim3 blocks((unsigned)((warps + 7) / 8));
     if (x_dt == MOE_F32)
-      quant_1x128_kernel<float><<<blocks, 256, 0, st>>>((const float*)x, rows, cols, q, scale);
+      err = launch_pdl(quant_1x128_kernel<float>, blocks, dim3(256), 0, st, 0, (const float*)x,
+                       (long long)rows, (long long)cols, q, scale);
     else
-      quant_1x128_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows,
-                                                                cols, q, scale);
+      err = launch_pdl(quant_1x128_kernel<__nv_bfloat16>, blocks, dim3(256), 0, st, 0,
+                       (const __nv_bfloat16*)x, (long long)rows, (long long)cols, q, scale);
   } else {
     const dim3 grid((unsigned)(cols / 128), (unsigned)(rows / 128));
     if (x_dt == MOE_F32)
-      quant_128x128_kernel<float><<<grid, 256, 0, st>>>((const float*)x, cols, q, scale);
+      err = launch_pdl(quant_128x128_kernel<float>, grid, dim3(256), 0, st, 0, (const float*)x,
+                       (long long)cols, q, scale);
     else
-      quant_128x128_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)x, cols, q,
-                                                                scale);
+      err = launch_pdl(quant_128x128_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, 0,
+                       (const __nv_bfloat16*)x, (long long)cols, q, scale);
   }
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace moe

@@ -17,7 +17,8 @@
 // to that sequence's accumulator as a 64-bit fixed-point integer (units of 2^-32):
 // integer addition is exact and associative, so the totals do not depend on the order
 // the CTAs finish in.  The last CTA to finish (a per-launch atomic counter) converts the
-// totals to fp32 seq_p_sum.
+// totals to fp32 seq_p_sum.  A batch of at most 128 tokens is one cluster: there CTA 0
+// adds the CTAs' run sums over distributed shared memory instead (fp32, token order).
 // C is chosen so that the clusters fill the SMs: 2 at 8192 tokens, 8 for decode batches.
 #include <algorithm>
 
@@ -39,7 +40,9 @@ struct FCtrl {
   uint32_t tmem_base;
   int abort_flag;
   int is_last;
+  int nruns;            // one-cluster launches: runs of one sequence among this CTA's tokens
   int seqid[BM];
+  int runseq[BM];       // ... and the sequence of each run
 };
 
 // Row stride (floats) of a partial tile in shared memory: N_r + 4 keeps the float4
@@ -60,13 +63,42 @@ struct FusedArgs {
   RouteOut p;
   const float* b;
   int d, C;
-  int* done_ctr;                 // zeroed before the launch
+  int one_cluster;               // the launch is one cluster (T <= 128): P sums over DSMEM
+  int* done_ctr;                 // zeroed before the launch (more than one cluster)
   unsigned long long* p_acc;     // [n_seq, N_r] fixed-point P sums, zeroed before the launch
   float* seq_p_sum;              // [n_seq, N_r] or null
   int32_t* err;
 };
 
 constexpr double kFix = 4294967296.0;   // 2^32: fixed-point units of the P accumulators
+
+// z[qq] = sum over the CC slices, in slice order, of the float4 at row + 32*qq in the
+// partial tile of each CTA of the cluster.  The loads of a batch of slices (at most 16
+// float4) are all issued before the first add.
+template <int Q, int CC>
+__device__ __forceinline__ void sum_slices(float4 (&z)[Q], const float* row) {
+  constexpr int PER = (16 / Q) < CC ? (16 / Q) : CC;
+#pragma unroll
+  for (int s0 = 0; s0 < CC; s0 += PER) {
+    float4 w[PER][Q];
+#pragma unroll
+    for (int bb = 0; bb < PER; ++bb)
+#pragma unroll
+      for (int qq = 0; qq < Q; ++qq)
+        w[bb][qq] = tc::ld_cluster_f4(tc::cluster_addr(row + 32 * qq, (uint32_t)(s0 + bb)));
+#pragma unroll
+    for (int bb = 0; bb < PER; ++bb)
+#pragma unroll
+      for (int qq = 0; qq < Q; ++qq) {
+        if (s0 + bb == 0) {
+          z[qq] = w[bb][qq];
+        } else {
+          z[qq].x = __fadd_rn(z[qq].x, w[bb][qq].x); z[qq].y = __fadd_rn(z[qq].y, w[bb][qq].y);
+          z[qq].z = __fadd_rn(z[qq].z, w[bb][qq].z); z[qq].w = __fadd_rn(z[qq].w, w[bb][qq].w);
+        }
+      }
+  }
+}
 
 template <int Q>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -75,6 +107,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int N = 32 * Q;
   constexpr int LD = part_stride(N);
   extern __shared__ uint8_t smem_raw[];
+  pdl_release();
+  pdl_wait();
   const uint32_t raw_off = tc::smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_off & 1023u)) & 1023u);
   constexpr int SBYTES = A_BYTES + N * BK * 2;
@@ -187,25 +221,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     float4 z[Q];
 #pragma unroll
     for (int qq = 0; qq < Q; ++qq) z[qq] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) {
-      const uint32_t off = tc::smem_u32(part + (size_t)rrow * LD + 4 * part_id);
-      for (int src = 0; src < C; ++src) {          // slice order: the same sum everywhere
-#pragma unroll
-        for (int qq = 0; qq < Q; ++qq) {
-          float4 w;
-          uint32_t addr;
-          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(off + 128u * qq), "r"(src));
-          asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(w.x), "=f"(w.y), "=f"(w.z), "=f"(w.w)
-                       : "r"(addr));
-          if (src == 0) {
-            z[qq] = w;
-          } else {
-            z[qq].x = __fadd_rn(z[qq].x, w.x); z[qq].y = __fadd_rn(z[qq].y, w.y);
-            z[qq].z = __fadd_rn(z[qq].z, w.z); z[qq].w = __fadd_rn(z[qq].w, w.w);
-          }
-        }
-      }
+    if (valid) {                                 // slice order: the same sum everywhere
+      const float* row = part + (size_t)rrow * LD + 4 * part_id;
+      if (C == 2) sum_slices<Q, 2>(z, row);
+      else if (C == 4) sum_slices<Q, 4>(z, row);
+      else sum_slices<Q, 8>(z, row);
     }
     float sv[Q][4], bv[Q][4];
 #pragma unroll
@@ -241,37 +261,91 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   __syncthreads();
 
-  if (want_p && !aborted && ntok > 0) {
-    for (int i = threadIdx.x; i < N; i += blockDim.x) {
-      float acc = 0.f;
-      for (int r = 0; r < ntok; ++r) {
-        acc = __fadd_rn(acc, sp_tile[(size_t)r * N + i]);
-        if (r == ntok - 1 || F.seqid[r + 1] != F.seqid[r]) {   // end of a run
-          const unsigned long long v = (unsigned long long)__double2ll_rn((double)acc * kFix);
-          atomicAdd(a.p_acc + (size_t)F.seqid[r] * N + i, v);
+  if (a.one_cluster) {
+    // One cluster covers the batch: each CTA leaves its run sums in shared memory and
+    // CTA 0 adds them per sequence over distributed shared memory, in token order (fp32;
+    // no atomics and no scratch to zero).
+    if (want_p) {
+      if (threadIdx.x == 0) {
+        int n = 0;
+        for (int r = 0; r < ntok && !aborted; ++r)
+          if (r == 0 || F.seqid[r] != F.seqid[r - 1]) F.runseq[n++] = F.seqid[r];
+        F.nruns = n;
+      }
+      if (!aborted) {
+        for (int i = threadIdx.x; i < N; i += blockDim.x) {   // run k's sum goes to row k
+          float acc = 0.f;
+          for (int r = 0, k = 0; r < ntok; ++r) {
+            acc = __fadd_rn(acc, sp_tile[(size_t)r * N + i]);
+            if (r == ntok - 1 || F.seqid[r + 1] != F.seqid[r]) {
+              sp_tile[(size_t)(k++) * N + i] = acc;
+              acc = 0.f;
+            }
+          }
+        }
+      }
+    }
+    tc::cluster_sync();   // every CTA's run sums and run list are in place
+    if (want_p && c == 0) {
+      for (int j = threadIdx.x; j < p.n_seq; j += blockDim.x) {   // offsets 0 <= ... <= T
+        const int s0 = p.seq_offsets[j], s1 = p.seq_offsets[j + 1];
+        if (s0 < 0 || s1 < s0 || s1 > p.T || (j == 0 && s0 != 0) || (j == p.n_seq - 1 && s1 != p.T))
+          record_error(a.err, MOE_ERR_INVALID_ARG);
+      }
+      for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        int j = 0;
+        float acc = 0.f;
+        for (int src = 0; src < C; ++src) {
+          const int nr = tc::ld_cluster_s32(tc::cluster_addr(&F.nruns, (uint32_t)src));
+          for (int k = 0; k < nr; ++k) {
+            const int sid = tc::ld_cluster_s32(tc::cluster_addr(&F.runseq[k], (uint32_t)src));
+            const float v = tc::ld_cluster_f32(tc::cluster_addr(sp_tile + (size_t)k * N + i, (uint32_t)src));
+            for (; j < sid && j < p.n_seq; ++j) {
+              a.seq_p_sum[(size_t)j * N + i] = acc;
+              acc = 0.f;
+            }
+            acc = __fadd_rn(acc, v);
+          }
+        }
+        for (; j < p.n_seq; ++j) {
+          a.seq_p_sum[(size_t)j * N + i] = acc;
           acc = 0.f;
         }
       }
     }
-    __threadfence();
-  }
-  __syncthreads();
-  if (want_p) {
-    // the last CTA to get here adds the run sums of every sequence
-    if (threadIdx.x == 0) {
+  } else {
+    if (want_p && !aborted && ntok > 0) {
+      for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        float acc = 0.f;
+        for (int r = 0; r < ntok; ++r) {
+          acc = __fadd_rn(acc, sp_tile[(size_t)r * N + i]);
+          if (r == ntok - 1 || F.seqid[r + 1] != F.seqid[r]) {   // end of a run
+            const unsigned long long v = (unsigned long long)__double2ll_rn((double)acc * kFix);
+            atomicAdd(a.p_acc + (size_t)F.seqid[r] * N + i, v);
+            acc = 0.f;
+          }
+        }
+      }
       __threadfence();
-      F.is_last = atomicAdd(a.done_ctr, 1) == (int)gridDim.x - 1;
     }
     __syncthreads();
-    if (F.is_last) {
-      __threadfence();
-      if (threadIdx.x < p.n_seq) {   // offsets that are not 0 <= ... <= T are reported
-        const int j = threadIdx.x, s0 = p.seq_offsets[j], s1 = p.seq_offsets[j + 1];
-        if (s0 < 0 || s1 < s0 || s1 > p.T || (j == 0 && s0 != 0) || (j == p.n_seq - 1 && s1 != p.T))
-          record_error(a.err, MOE_ERR_INVALID_ARG);
+    if (want_p) {
+      // the last CTA to get here adds the run sums of every sequence
+      if (threadIdx.x == 0) {
+        __threadfence();
+        F.is_last = atomicAdd(a.done_ctr, 1) == (int)gridDim.x - 1;
       }
-      for (int x = threadIdx.x; x < p.n_seq * N; x += blockDim.x)
-        a.seq_p_sum[x] = (float)((double)(long long)__ldcg(a.p_acc + x) / kFix);
+      __syncthreads();
+      if (F.is_last) {
+        __threadfence();
+        if (threadIdx.x < p.n_seq) {   // offsets that are not 0 <= ... <= T are reported
+          const int j = threadIdx.x, s0 = p.seq_offsets[j], s1 = p.seq_offsets[j + 1];
+          if (s0 < 0 || s1 < s0 || s1 > p.T || (j == 0 && s0 != 0) || (j == p.n_seq - 1 && s1 != p.T))
+            record_error(a.err, MOE_ERR_INVALID_ARG);
+        }
+        for (int x = threadIdx.x; x < p.n_seq * N; x += blockDim.x)
+          a.seq_p_sum[x] = (float)((double)(long long)__ldcg(a.p_acc + x) / kFix);
+      }
     }
   }
 
@@ -322,28 +396,17 @@ cudaError_t launch_router_fused(const void* u, const void* e, int d, const float
   const int C = fused_cluster(p.T, d);
   // scratch: the counter, then the fixed-point accumulators, zeroed together
   unsigned long long* p_acc = reinterpret_cast<unsigned long long*>(done_ctr + 64);
-  FusedArgs a{p, b, d, C, done_ctr, p_acc, seq_p_sum, dev_error_ptr()};
+  const int one = (p.T + BM - 1) / BM == 1 ? 1 : 0;
+  FusedArgs a{p, b, d, C, one, done_ctr, p_acc, seq_p_sum, dev_error_ptr()};
   cudaError_t err = cudaSuccess;
-  if (p.pwin)
+  if (p.pwin && !one)
     err = cudaMemsetAsync(done_ctr, 0, 256 + (size_t)p.n_seq * p.N_r * sizeof(unsigned long long), st);
   if (err != cudaSuccess) return err;
   const size_t smem = fused_smem(p.N_r, C);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(((p.T + BM - 1) / BM) * C);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   auto go = [&](auto kernel) {
     cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e2 != cudaSuccess) return e2;
-    return cudaLaunchKernelEx(&cfg, kernel, mU, mE, a);
+    return launch_pdl(kernel, dim3(((p.T + BM - 1) / BM) * C), dim3(THREADS), smem, st, (unsigned)C, mU, mE, a);
   };
   switch (p.N_r) {
     case 64: err = go(router_fused_kernel<2>); break;

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) router_gemm_simt_kernel(const TIn* __rest
   extern __shared__ float sm[];
   float* u_tile = sm;                          // [kTok][kKc+1]
   float* e_tile = u_tile + kTok * (kKc + 1);   // [N_r][kKc+1]
+  pdl_release();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int t0 = blockIdx.x * kTok;
   const int ty = tid >> 3, tx = tid & 7;
@@ -93,6 +95,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(
   __shared__ float b_sm[kMaxExperts];
   __shared__ float rs_sm[kTok];
   __shared__ int seqid[kTok];
+  pdl_release();
+  pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int N_r = p.N_r, T = p.T, stride = N_r + 1;
   const int t0 = blockIdx.x * kTok;
@@ -197,6 +201,8 @@ __global__ void __launch_bounds__(256, 2) router_select_warp_kernel(const float*
   constexpr int WARPS = 8, TPW = kPWindow / WARPS, N = 32 * E;
   __shared__ __align__(16) float sp_tile[kPWindow][N];
   __shared__ int seqid[kPWindow];
+  pdl_release();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.T, t0 = blockIdx.x * kPWindow;
   const int ntok = min(kPWindow, T - t0);
@@ -331,6 +337,8 @@ __global__ void __launch_bounds__(256, 2) router_select_oct_kernel(const float* 
   constexpr int N = 32 * Q;
   __shared__ __align__(16) float sp_tile[kPWindow][N];
   __shared__ int seqid[kPWindow];
+  pdl_release();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.T, t0 = blockIdx.x * kPWindow;
   const int ntok = min(kPWindow, T - t0);
@@ -428,6 +436,8 @@ __global__ void __launch_bounds__(256) seq_psum_kernel(const float* __restrict__
                                                        int n_seq, int T, int N_r,
                                                        float* __restrict__ out, int32_t* err) {
   __shared__ double part[8][32];
+  pdl_release();
+  pdl_wait();
   const int j = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.y * 32 + lane;
   int a = seq_offsets[j], z = seq_offsets[j + 1];
@@ -466,9 +476,10 @@ cudaError_t launch_router_gemm_simt(const void* u, const void* e, moe_dtype dt, 
   int jn = 1;
   while (jn * 8 < N_r) jn <<= 1;
   auto smem = [&](int kc) { return sizeof(float) * (size_t)(kTok + N_r) * (kc + 1); };
-#define MOE_SIMT_GEMM(TIN, JN)                                                              \
-  router_gemm_simt_kernel<TIN, JN><<<grid, 256, smem(simt_kc<JN>()), st>>>(                 \
-      (const TIN*)u, (const TIN*)e, T, d, N_r, z)
+  cudaError_t err;
+#define MOE_SIMT_GEMM(TIN, JN)                                                                   \
+  err = launch_pdl(router_gemm_simt_kernel<TIN, JN>, grid, dim3(256), smem(simt_kc<JN>()), st, 0, \
+                   (const TIN*)u, (const TIN*)e, T, d, N_r, z)
   if (dt == MOE_F32) {
     switch (jn) {
       case 1: MOE_SIMT_GEMM(float, 1); break;
@@ -489,39 +500,42 @@ cudaError_t launch_router_gemm_simt(const void* u, const void* e, moe_dtype dt, 
     }
   }
 #undef MOE_SIMT_GEMM
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_router_select(const float* z_part, int S, const float* b, const RouteOut& p,
                                  cudaStream_t st) {
   if (p.T == 0) return cudaSuccess;
-  const int blocks = (p.T + kPWindow - 1) / kPWindow;
+  const dim3 blocks((p.T + kPWindow - 1) / kPWindow);
+  auto go = [&](auto kernel) { return launch_pdl(kernel, blocks, dim3(256), 0, st, 0, z_part, S, b, p); };
+  cudaError_t err;
   if (oct_select_ok(p.N_r, p.K_r, p.G, p.M)) {
     switch (p.N_r) {
-      case 64: router_select_oct_kernel<2><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
-      case 128: router_select_oct_kernel<4><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
-      default: router_select_oct_kernel<8><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
+      case 64: err = go(router_select_oct_kernel<2>); break;
+      case 128: err = go(router_select_oct_kernel<4>); break;
+      default: err = go(router_select_oct_kernel<8>); break;
     }
   } else if (warp_select_ok(p.N_r, p.K_r, p.G, p.M)) {
     switch (p.N_r) {
-      case 32: router_select_warp_kernel<1><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
-      case 64: router_select_warp_kernel<2><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
-      case 128: router_select_warp_kernel<4><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
-      default: router_select_warp_kernel<8><<<blocks, 256, 0, st>>>(z_part, S, b, p); break;
+      case 32: err = go(router_select_warp_kernel<1>); break;
+      case 64: err = go(router_select_warp_kernel<2>); break;
+      case 128: err = go(router_select_warp_kernel<4>); break;
+      default: err = go(router_select_warp_kernel<8>); break;
     }
   } else {
     const int fast = fast_select_ok(p.N_r, p.K_r, p.G, p.M) ? 1 : 0;
-    router_select_kernel<<<blocks, kSelWarps * 32, 0, st>>>(z_part, S, b, p, fast);
+    err = launch_pdl(router_select_kernel, blocks, dim3(kSelWarps * 32), 0, st, 0, z_part, S, b, p, fast);
   }
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_seq_psum(const float* pwin, const int32_t* seq_offsets, int n_seq, int T,
                             int N_r, float* out, cudaStream_t st) {
   if (n_seq == 0) return cudaSuccess;
   const dim3 grid(n_seq, (N_r + 31) / 32);
-  seq_psum_kernel<<<grid, 256, 0, st>>>(pwin, seq_offsets, n_seq, T, N_r, out, dev_error_ptr());
-  return cudaGetLastError();
+  const cudaError_t err = launch_pdl(seq_psum_kernel, grid, dim3(256), 0, st, 0, pwin, seq_offsets, n_seq,
+                                     T, N_r, out, dev_error_ptr());
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace moe

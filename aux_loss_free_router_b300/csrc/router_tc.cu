@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                           uint32_t tmem_cols, int T, int kb_per_split,
                           float* __restrict__ z_part, int32_t* err) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_release();
+  pdl_wait();
   const uint32_t raw_off = tc::smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_off & 1023u)) & 1023u);
   const int half = n_r / 2;                       // centroid rows per CTA
@@ -170,20 +172,8 @@ cudaError_t launch_router_gemm_tc(const void* u, const void* e, int T, int d, in
   const int nk = (d + BK - 1) / BK;
   const int S = router_tc_splits(T, d);
   const int per = (nk + S - 1) / S;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pair_count(T), S);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, router_gemm_tc_kernel, mU, mE, d, N_r, cols, T, per, z_part,
-                           dev_error_ptr());
+  err = launch_pdl(router_gemm_tc_kernel, dim3(2 * pair_count(T), S), dim3(THREADS), smem, st, 2, mU, mE,
+                   d, N_r, cols, T, per, z_part, dev_error_ptr());
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

@@ -49,8 +49,10 @@ namespace ffn_tc {
 
 // Tile counters: one slot per launch, taken round-robin from kTileCounters, so that
 // launches in flight at the same time (up to kTileCounters of them) count separately.
+// A slot is two ints (tiles claimed, CTAs done); the last CTA of a launch zeroes both,
+// so a slot is zero whenever no launch holds it.
 constexpr int kTileCounters = 64;
-__device__ int g_tile_ctr[kTileCounters];
+__device__ int g_tile_ctr[2 * kTileCounters];
 
 int* tile_counter(cudaError_t* err) {
   static std::mutex mu;
@@ -67,7 +69,7 @@ int* tile_counter(cudaError_t* err) {
     if (*err != cudaSuccess) return nullptr;
     base[dev] = static_cast<int*>(p);
   }
-  return base[dev] + (next_slot++ % kTileCounters);
+  return base[dev] + 2 * (next_slot++ % kTileCounters);
 }
 
 }  // namespace ffn_tc
@@ -176,6 +178,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tma_prefetch_desc(&mX_r);
     tc::tma_prefetch_desc(&mW0_r);
   }
+  pdl_release();
+  pdl_wait();   // before the tile counter, expert_offset and tensor memory are touched
   if (warp == 1) {
     tc::tmem_alloc_pair(&C.tmem_base, TMEM_COLS);
     tc::tmem_relinquish_pair();
@@ -394,6 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1 && lane == 0) tc::mbar_drain(&C.fin, 0);
   __syncthreads();
   tc::cluster_sync();   // neither CTA leaves while its peer may still touch it
+  if (threadIdx.x == 0) release_tile_counter(args.tile_ctr);   // the producer's claims are done
   if (warp == 1) {
     __syncwarp();
     tc::fence_after_sync();

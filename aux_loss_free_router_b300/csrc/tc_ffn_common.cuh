@@ -25,7 +25,7 @@ struct TcArgs {
   const int32_t* expert_offset;
   __nv_bfloat16* out;
   int32_t* err;
-  int* tile_ctr;     // zeroed before the launch; pairs claim tiles from it in order
+  int* tile_ctr;     // [claimed, done], zero at launch; pairs claim tiles in order
   // gate/up only, optional: the pre-activations a = x W_gate^T and c = x W_up^T in bf16,
   // in the same row space and layout as h (kept for the backward pass)
   __nv_bfloat16* save_a = nullptr;
@@ -69,9 +69,21 @@ __device__ __forceinline__ void store_transposed(__nv_bfloat16* scr, const float
 // 64 launches in flight at once count separately.
 int* tile_counter(cudaError_t* err);
 
+// Called once by every CTA of a launch, after its producer's last claim: the last CTA
+// to get here puts the slot back to zero for the next launch that takes it (in stream
+// order that launch reads the counter only after this one has completed).
+__device__ __forceinline__ void release_tile_counter(int* ctr) {
+  __threadfence();
+  if (atomicAdd(ctr + 1, 1) == (int)(gridDim.x * gridDim.y * gridDim.z) - 1) {
+    __threadfence();
+    atomicExch(ctr, 0);
+    atomicExch(ctr + 1, 0);
+  }
+}
+
 // Launch `kernel` as persistent CTA pairs (clusters of two): as many pairs as fit on
-// the device at once (cached per device in `fit_cache`), at most `tiles_ub`.  The tile
-// counter is zeroed on the stream first.
+// the device at once (cached per device in `fit_cache`), at most `tiles_ub`, with the
+// programmatic-serialization attribute.
 template <typename Kernel>
 cudaError_t launch_pairs(Kernel kernel, int* fit_cache, std::mutex& mu, size_t smem,
                          long long tiles_ub, const CUtensorMap* m, TcArgs a, cudaStream_t st) {
@@ -106,8 +118,8 @@ cudaError_t launch_pairs(Kernel kernel, int* fit_cache, std::mutex& mu, size_t s
   cfg.gridDim = dim3(2 * (int)std::min<long long>(fit, std::max<long long>(1, tiles_ub)));
   a.tile_ctr = tile_counter(&err);
   if (a.tile_ctr == nullptr) return err;
-  if ((err = cudaMemsetAsync(a.tile_ctr, 0, sizeof(int), st)) != cudaSuccess) return err;
-  err = cudaLaunchKernelEx(&cfg, kernel, m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], a);
+  err = launch_pdl(kernel, cfg.gridDim, cfg.blockDim, smem, st, 2, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+                   m[7], a);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                       const __grid_constant__ CUtensorMap mB0_s,
                       const __grid_constant__ CUtensorMap mB1_s, Fp8Args args) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_release();
+  pdl_wait();
   const uint32_t raw_off = tc::smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_off & 1023u)) & 1023u);
   Ctrl& C = *reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
@@ -345,8 +347,9 @@ cudaError_t launch(const FfnShape& s, const CUtensorMap* maps, const Fp8Args& a,
   auto k = tc_ffn_fp8_kernel<MODE>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (err != cudaSuccess) return err;
-  k<<<grid, THREADS, kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
-  return cudaGetLastError();
+  err = launch_pdl(k, dim3(grid), dim3(THREADS), kSmemBytes, st, 0, maps[0], maps[1], maps[2], maps[3],
+                   maps[4], maps[5], a);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 constexpr CUtensorMapDataType kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;

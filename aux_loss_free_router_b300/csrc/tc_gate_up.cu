@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tma_prefetch_desc(&mX_r);
     tc::tma_prefetch_desc(&mW0_r);
   }
+  pdl_release();
+  pdl_wait();   // before the tile counter, expert_offset and tensor memory are touched
   if (warp == 1) {
     tc::tmem_alloc_pair(&C.tmem_base, TMEM_COLS);
     tc::tmem_relinquish_pair();
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1 && lane == 0) tc::mbar_drain(&C.fin, 0);
   __syncthreads();
   tc::cluster_sync();   // neither CTA leaves while its peer may still touch it
+  if (threadIdx.x == 0) release_tile_counter(args.tile_ctr);   // the producer's claims are done
   if (warp == 1) {
     __syncwarp();
     tc::fence_after_sync();

@@ -238,6 +238,25 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
   return r;
 }
 
+// Loads from the shared memory of a CTA of the cluster (addresses from cluster_addr).
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t a) {
+  float4 w;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(w.x), "=f"(w.y), "=f"(w.z), "=f"(w.w)
+               : "r"(a));
+  return w;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
+  float w;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(w) : "r"(a));
+  return w;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
+  int w;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(w) : "r"(a));
+  return w;
+}
+
 // Store to a 32-bit variable in the shared memory of a CTA of the cluster.
 __device__ __forceinline__ void st_cluster_s32(uint32_t cluster_addr_, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr_), "r"(v) : "memory");
