@@ -1,4 +1,4 @@
-"""E4M3 rounding and the 1x128 / 128x128 fp32-scaled quantisation (CPU oracle).
+"""E4M3 rounding and the 1x128 / 128x1 / 128x128 fp32-scaled quantisation (CPU oracle).
 
 TEST INFRASTRUCTURE ONLY.  Imported by ``tests/``, ``__graft_entry__.smoke()`` and
 the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py``; never by the
@@ -6,7 +6,10 @@ library or its Python binding.
 
 The granularity follows the DeepSeek-V3 Technical Report reading guide
 (xyznot.com, "Key ideas", FP8 mixed-precision bullet): E4M3 on all tensors,
-activations scaled per 1x128 tile, weights per 128x128 block.  The pages fix only
+activations scaled per 1x128 tile, weights per 128x128 block.  The 128x1 tiles (one
+column, 128 rows) serve the backward's weight-gradient GEMMs, whose contraction runs
+over the rows (tokens): a tile lies along the contraction axis there, as the 1x128
+tile does in the forward (see ``moe_backward.layer_backward_fp8``).  The pages fix only
 the granularity; the scale rule used here is the plainest one that maps each tile's
 largest magnitude onto the format's largest finite value: scale = amax / 448 in
 fp32, code = E4M3(x / scale) rounded to nearest-even with saturation, and
@@ -120,3 +123,36 @@ def dequantize_128x128(q, scale) -> np.ndarray:
     *lead, R, C = q.shape
     blocks = q.reshape(*lead, R // TILE, TILE, C // TILE, TILE)
     return (blocks * scale.astype(np.float64)[..., :, None, :, None]).reshape(q.shape)
+
+
+def quantize_128x1(x) -> tuple[np.ndarray, np.ndarray]:
+    """Per-column, per-128-row tile quantisation of an fp32 matrix [n, C] whose rows
+    are the tokens of one expert segment.
+
+    The rows are cut into ceil(n/128) tiles from the first row; the last tile may be
+    short (its amax is over its own rows).  Returns (q, scale): q [n, C] float64
+    values on the E4M3 grid, scale [ceil(n/128), C] fp32.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    n, C = x.shape
+    nb = -(-n // TILE)
+    padded = np.zeros((nb * TILE, C), dtype=np.float32)
+    padded[:n] = x
+    tiles = padded.reshape(nb, TILE, C)
+    scale = _scales(np.abs(tiles).max(axis=1))                   # [nb, C]
+    q = e4m3_round((tiles / scale[:, None, :]).astype(np.float32))
+    return q.reshape(nb * TILE, C)[:n], scale
+
+
+def dequantize_128x1(q, scale) -> np.ndarray:
+    q = np.asarray(q, dtype=np.float64)
+    n = q.shape[0]
+    rows = np.repeat(scale.astype(np.float64), TILE, axis=0)[:n]
+    return q * rows
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round fp32 values to bfloat16 (nearest, ties to even), returned as fp32."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    return b.astype(np.uint32).view(np.float32)

@@ -32,9 +32,11 @@ import numpy as np
 
 from . import moe_oracle as _fw
 
+from . import fp8 as _fp8
+
 __all__ = [
     "sigmoid64", "silu_grad", "expert_ffn_backward", "gate_backward", "balance_backward",
-    "forward64", "layer_backward",
+    "forward64", "layer_backward", "expert_ffn_backward_fp8", "layer_backward_fp8",
 ]
 
 
@@ -197,6 +199,126 @@ def layer_backward(u, e, b, weights: dict, dh, K_r: int, G: int = 1, M: int = 1,
         dy = gate[rows, ks][:, None] * dh[rows]
         dx, dg_, du_, dd_ = expert_ffn_backward(u[rows], routed["w_gate"][i], routed["w_up"][i],
                                                 routed["w_down"][i], dy)
+        np.add.at(du, rows, dx)
+        grads["w_gate"][i] += dg_
+        grads["w_up"][i] += du_
+        grads["w_down"][i] += dd_
+    dgate = np.einsum("td,tkd->tk", dh, y)
+    ds = gate_backward(s, idx, dgate)
+    if seq_offsets is not None:
+        ds += balance_backward(s, idx, seq_offsets, K_r, alpha)
+    dz = ds * s * (1.0 - s)
+    du += dz @ e
+    de = dz.T @ u
+    return dict(grads, du=du, de=de, db=np.zeros(np.asarray(b).shape))
+
+
+# ----------------------------------------------------------------- FP8 backward -----
+#
+# The pages run all three GEMMs of a linear layer in E4M3 - Fprop, Dgrad (activation
+# gradient) and Wgrad (weight gradient) - with fp32 outputs, fp32 scales per 1x128
+# activation tile and per 128x128 weight block, promotion to fp32 every 128 elements
+# of the contraction, and the activations that Wgrad needs kept in E4M3 from the
+# forward pass (pwwt.cn notes §三; xyznot.com reading guide, Key ideas, FP8 bullet).
+# Readings where the pages are silent:
+#
+# * an activation tile lies along the contraction axis of the GEMM that consumes it:
+#   1x128 (one token, 128 features) in Fprop and Dgrad, 128x1 (one feature, 128 tokens
+#   of an expert's segment, the last tile short) in Wgrad, whose contraction runs over
+#   the tokens; the weights keep their 128x128 blocks (a block is a block of W^T too);
+# * Wgrad takes the cached forward activations - the E4M3 tokens x and the E4M3 h the
+#   forward's down GEMM consumed - and re-tiles them 128x1 (dequantise, quantise);
+# * the gradients dY = g * dh, dA and dC are quantised for Dgrad (1x128) and for Wgrad
+#   (128x1) each from its own value;
+# * the router stays as in the FP8 forward: affinities, gates and the balance loss on
+#   the unquantised bf16 tokens, their gradients in float64.
+#
+# Where a value is rounded before it is quantised, the oracle rounds it where the
+# kernels do (bf16 a and c, dY, dH, and the dA / dC that Wgrad quantises), so that both
+# sides decide every E4M3 code on the same number.  The products are float64 sums of
+# dequantised operands: promotion every 128 with fp32 scales is this sum up to fp32
+# rounding of the partial sums.
+
+def _cached_activation(m) -> np.ndarray:
+    """A forward activation as the FP8 layer keeps it: E4M3 per 1x128 tile."""
+    return _fp8.dequantize_1x128(*_fp8.quantize_1x128(np.asarray(m, np.float32)))
+
+
+def _dgrad_operand(m) -> np.ndarray:
+    """An activation gradient entering a Dgrad GEMM: E4M3 per 1x128 tile (the
+    contraction runs over the features)."""
+    return _fp8.dequantize_1x128(*_fp8.quantize_1x128(np.asarray(m, np.float32)))
+
+
+def _wgrad_operand(m) -> np.ndarray:
+    """An operand of a Wgrad GEMM over one expert's tokens: E4M3 per 128x1 tile (the
+    contraction runs over the tokens)."""
+    return _fp8.dequantize_128x1(*_fp8.quantize_128x1(np.asarray(m, np.float32)))
+
+
+def _cached_tokens(u) -> np.ndarray:
+    """The FP8 layer's token rows: u in E4M3 per 1x128 tile."""
+    return _fp8.dequantize_1x128(*_fp8.quantize_1x128(np.asarray(u, np.float32)))
+
+
+def expert_ffn_backward_fp8(x, w_gate, w_up, w_down, dy):
+    """FP8 gradients of one expert.  x [n, d]: the forward's dequantised E4M3 token
+    rows; w_gate, w_up [I, d], w_down [d, I]: dequantised E4M3 weights; dy [n, d] fp32.
+    Returns (dx [n, d], dw_gate [I, d], dw_up [I, d], dw_down [d, I]), float64."""
+    x = np.asarray(x, np.float64)
+    wg, wu, wd = (np.asarray(w, np.float64) for w in (w_gate, w_up, w_down))
+    a64 = x @ wg.T
+    c64 = x @ wu.T
+    h = _cached_activation(_fw.silu(a64) * c64)      # what the forward's down GEMM read
+    a = _fp8.bf16_round(a64).astype(np.float64)
+    c = _fp8.bf16_round(c64).astype(np.float64)
+    dY = _fp8.bf16_round(dy).astype(np.float64)
+    # Dgrad: dH = dY W_down, the SwiGLU backward, dx = dA W_gate + dC W_up
+    dH = _fp8.bf16_round(_dgrad_operand(dY) @ wd).astype(np.float64)
+    dA = (dH * c * silu_grad(a)).astype(np.float32)
+    dC = (dH * _fw.silu(a)).astype(np.float32)
+    dx = _dgrad_operand(dA) @ wg + _dgrad_operand(dC) @ wu
+    # Wgrad: contractions over the expert's tokens
+    dw_down = _wgrad_operand(dY).T @ _wgrad_operand(h)
+    xc = _wgrad_operand(x)
+    dw_gate = _wgrad_operand(_fp8.bf16_round(dA)).T @ xc
+    dw_up = _wgrad_operand(_fp8.bf16_round(dC)).T @ xc
+    return dx, dw_gate, dw_up, dw_down
+
+
+def layer_backward_fp8(u, e, b, weights: dict, dh, K_r: int, G: int = 1, M: int = 1,
+                       N_s: int = 0, seq_offsets=None, alpha: float = 0.0, idx=None) -> dict:
+    """``layer_backward`` for the FP8 layer: the forward with E4M3 tokens (1x128), E4M3
+    weights (128x128) and the re-quantised h, and the expert gradients of
+    ``expert_ffn_backward_fp8``; routing, gates, the balance loss and the affinity
+    gradients stay in float64 on the unquantised u.  dy = fp32(g) * fp32(dh) for a
+    routed slot, dh for a shared expert.  Same keys as ``layer_backward``."""
+    fw = forward64(u, e, b, weights, K_r, G, M, N_s, seq_offsets, alpha, idx)
+    u = np.asarray(u, np.float64)
+    e = np.asarray(e, np.float64)
+    dh = np.asarray(dh, np.float64)
+    s, idx, gate = fw["s"], fw["idx"], fw["gate"]
+    wq = lambda w: _fp8.dequantize_128x128(*_fp8.quantize_128x128(np.asarray(w, np.float32)))
+    x = _cached_tokens(u)
+    routed = {k: wq(weights[k]) for k in ("w_gate", "w_up", "w_down")}
+    shared = [tuple(wq(np.asarray(weights[k])[j]) for k in ("ws_gate", "ws_up", "ws_down"))
+              for j in range(N_s)]
+    du = dh.copy()
+    grads = {k: np.zeros_like(v) for k, v in routed.items()}
+    for k in ("ws_gate", "ws_up", "ws_down"):
+        grads[k] = np.zeros((N_s,) + np.asarray(weights[k]).shape[1:])
+    dh32 = dh.astype(np.float32)
+    for j, (wg, wu, wd) in enumerate(shared):
+        dx, dg_, du_, dd_ = expert_ffn_backward_fp8(x, wg, wu, wd, dh32)
+        du += dx
+        grads["ws_gate"][j], grads["ws_up"][j], grads["ws_down"][j] = dg_, du_, dd_
+    y = np.zeros(idx.shape + (u.shape[1],))
+    for i in np.unique(idx):
+        rows, ks = np.nonzero(idx == i)
+        wg, wu, wd = routed["w_gate"][i], routed["w_up"][i], routed["w_down"][i]
+        y[rows, ks] = _fw.expert_ffn(x[rows], wg, wu, wd, h_quant=True)
+        dy = gate[rows, ks].astype(np.float32)[:, None] * dh32[rows]
+        dx, dg_, du_, dd_ = expert_ffn_backward_fp8(x[rows], wg, wu, wd, dy)
         np.add.at(du, rows, dx)
         grads["w_gate"][i] += dg_
         grads["w_up"][i] += du_
