@@ -50,6 +50,11 @@ class _Weights(ctypes.Structure):
             "s_gate", "s_up", "s_down", "s_gate_scale", "s_up_scale", "s_down_scale")]
 
 
+class _DgradWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "wdt", "wdt_scale", "wgut", "wgut_scale", "s_wdt", "s_wdt_scale", "s_wgut", "s_wgut_scale")]
+
+
 _P, _S, _I32, _I64, _F = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -72,6 +77,11 @@ _SIGS = {
     "moe_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Weights),
                                     Shape, _P, _I32, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                     _S, _P]),
+    "moe_fp8_dgrad_weights_make": (ctypes.c_int, [ctypes.POINTER(_Weights), Shape,
+                                                  ctypes.POINTER(_DgradWeights), _P]),
+    "moe_backward_fp8_workspace": (_S, [Shape, _I32]),
+    "moe_backward_fp8": (ctypes.c_int, [_P] * 12 + [ctypes.POINTER(_Weights), ctypes.POINTER(_DgradWeights),
+                                                    Shape, _P, _I32, _F] + [_P] * 10 + [_S, _P]),
 }
 
 _lib = None
@@ -98,7 +108,12 @@ _KERNELS = {"moe_route": 2, "moe_dispatch": 3, "moe_dispatch_noalloc": 3, "moe_q
             "moe_seq_balance_stat": 1,
             # gate/up recompute, per-token prep, six GEMMs, combine (+ counts with the
             # balance term)
-            "moe_backward": 9}
+            "moe_backward": 9,
+            # weight transposes: W_down^T, W_gate^T, W_up^T (routed; again for shared)
+            "moe_fp8_dgrad_weights_make": 3,
+            # gate/up recompute, prep, dY quantisation, two Dgrad GEMMs, SwiGLU backward,
+            # five Wgrad operand quantisations, three Wgrad GEMMs, two router GEMMs, combine
+            "moe_backward_fp8": 17}
 _launches = 0
 
 
@@ -293,6 +308,49 @@ def backward(u, e, s, topk_idx, topk_gate, expert_offset, inv_row, x_perm, y, sh
           _ptr(seq_offsets), n_seq, alpha, _ptr(dh), g("u"), g("e"), g("w_gate"), g("w_up"),
           g("w_down"), g("ws_gate"), g("ws_up"), g("ws_down"), _ptr(ws),
           ws.numel() if ws is not None else 0, _stream(stream),
+          extra_kernels=1 if balance else 0)
+
+
+def fp8_dgrad_weights(weights8: dict, sh: Shape, stream=None) -> dict:
+    """moe_fp8_dgrad_weights_make: the transposed E4M3 weights of the FP8 Dgrad GEMMs
+    ("wdt" [E, I, d], "wgut" [E, d, 2I] with their "_scale" grids; "s_*" for the shared
+    experts) from the E4M3 weights of ``quantize_weights``."""
+    wq = weights8["w_gate"]
+    dev, N_r, I, d = wq.device, sh.N_r, sh.I, sh.d
+    out = {}
+    for pre, E in (("", N_r), ("s_", sh.N_s)):
+        out[pre + "wdt"] = torch.empty(E, I, d, dtype=torch.uint8, device=dev)
+        out[pre + "wdt_scale"] = torch.empty(E, I // 128, d // 128, dtype=torch.float32, device=dev)
+        out[pre + "wgut"] = torch.empty(E, d, 2 * I, dtype=torch.uint8, device=dev)
+        out[pre + "wgut_scale"] = torch.empty(E, d // 128, 2 * I // 128, dtype=torch.float32, device=dev)
+    st = _DgradWeights(*[_ptr(out[k]) if out[k].numel() else None for k in (
+        "wdt", "wdt_scale", "wgut", "wgut_scale", "s_wdt", "s_wdt_scale", "s_wgut", "s_wgut_scale")])
+    wt = _weights(weights8)
+    _call("moe_fp8_dgrad_weights_make", ctypes.byref(wt), sh, ctypes.byref(st), _stream(stream),
+          extra_kernels=3 if sh.N_s else 0)
+    out["_struct"] = st
+    return out
+
+
+def backward_fp8_workspace_bytes(sh: Shape, n_seq: int) -> int:
+    return load_library().moe_backward_fp8_workspace(sh, n_seq)
+
+
+def backward_fp8(u, u_q, u_scale, e, s, topk_idx, topk_gate, expert_offset, inv_row, x_perm_q,
+                 x_perm_scale, y, sh: Shape, weights8: dict, dgrad_weights: dict, dh, grads: dict,
+                 seq_offsets=None, n_seq: int = 0, alpha: float = 0.0, workspace=None, stream=None):
+    """moe_backward_fp8: the gradients of ``backward`` for an FP8 layer, its expert GEMMs
+    (Fprop again, Dgrad, Wgrad) in E4M3.  ``weights8``: ``quantize_weights`` output;
+    ``dgrad_weights``: ``fp8_dgrad_weights`` output."""
+    wt = _weights(weights8)
+    ws = workspace if workspace is not None else _workspace(backward_fp8_workspace_bytes(sh, n_seq), u.device)
+    g = lambda k: _ptr(grads.get(k))
+    balance = n_seq > 0 and alpha != 0.0
+    _call("moe_backward_fp8", _ptr(u), _ptr(u_q), _ptr(u_scale), _ptr(e), _ptr(s), _ptr(topk_idx),
+          _ptr(topk_gate), _ptr(expert_offset), _ptr(inv_row), _ptr(x_perm_q), _ptr(x_perm_scale),
+          _ptr(y), ctypes.byref(wt), ctypes.byref(dgrad_weights["_struct"]), sh, _ptr(seq_offsets),
+          n_seq, alpha, _ptr(dh), g("u"), g("e"), g("w_gate"), g("w_up"), g("w_down"), g("ws_gate"),
+          g("ws_up"), g("ws_down"), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream),
           extra_kernels=1 if balance else 0)
 
 
@@ -494,10 +552,11 @@ class MoELayer:
     def backward(self, u: torch.Tensor, dh: torch.Tensor, seq_offsets: Optional[torch.Tensor] = None,
                  stream=None) -> dict:
         """Gradients at the selection of the last ``step()`` on the same ``u`` (the layer
-        must have been built with ``want_s=True``; bf16 only): of sum(dh * h') plus, with
-        ``seq_offsets``, the mean over sequences of the balance loss.  Returns fp32
-        tensors "u", "e", "w_gate", "w_up", "w_down" (and "ws_*" with shared experts);
-        they and the workspace are allocated on the first call and reused."""
+        must have been built with ``want_s=True``): of sum(dh * h') plus, with
+        ``seq_offsets``, the mean over sequences of the balance loss.  An FP8 layer runs
+        its expert GEMMs' backward in E4M3 (moe_backward_fp8).  Returns fp32 tensors "u",
+        "e", "w_gate", "w_up", "w_down" (and "ws_*" with shared experts); they and the
+        workspace are allocated on the first call and reused."""
         if self.s_out is None:
             raise ValueError("backward() needs the affinities: build the layer with want_s=True")
         dev = self.e.device
@@ -507,8 +566,17 @@ class MoELayer:
             g["u"] = torch.empty(self.T, self.d, dtype=torch.float32, device=dev)
             g["e"] = torch.empty(self.N_r, self.d, dtype=torch.float32, device=dev)
             self._grads = g
-            self._bwd_ws = _workspace(backward_workspace_bytes(self.shape, self.n_seq), dev)
+            ws_bytes = (backward_fp8_workspace_bytes if self.fp8 else backward_workspace_bytes)(self.shape, self.n_seq)
+            self._bwd_ws = _workspace(ws_bytes, dev)
+            if self.fp8:
+                self._dgrad_w = fp8_dgrad_weights(self.ffn_weights, self.shape, stream=stream)
         n_seq = self.n_seq if seq_offsets is not None else 0
+        if self.fp8:
+            backward_fp8(u, self.u_q, self.u_scale, self.e, self.s_out, self.topk_idx, self.topk_gate,
+                         self.expert_offset, self.inv_row, self.x_perm, self.x_perm_scale, self.y,
+                         self.shape, self.ffn_weights, self._dgrad_w, dh, self._grads, seq_offsets, n_seq,
+                         self.alpha if seq_offsets is not None else 0.0, workspace=self._bwd_ws, stream=stream)
+            return self._grads
         backward(u, self.e, self.s_out, self.topk_idx, self.topk_gate, self.expert_offset,
                  self.inv_row, self.x_perm, self.y, self.shape, self.weights, dh, self._grads,
                  seq_offsets, n_seq, self.alpha if seq_offsets is not None else 0.0,

@@ -371,6 +371,25 @@ BwdWs bwd_ws(const moe_shape& sh, int n_seq) {
 
 }  // namespace
 
+namespace {
+
+moe_status zero_grads(const moe_shape& sh, float* de, float* dw_gate, float* dw_up, float* dw_down,
+                      float* dws_gate, float* dws_up, float* dws_down, cudaStream_t cs) {
+  const size_t gi = (size_t)sh.I * sh.d * 4;
+  cudaError_t err = cudaMemsetAsync(de, 0, (size_t)sh.N_r * sh.d * 4, cs);
+  if (err == cudaSuccess) err = cudaMemsetAsync(dw_gate, 0, sh.N_r * gi, cs);
+  if (err == cudaSuccess) err = cudaMemsetAsync(dw_up, 0, sh.N_r * gi, cs);
+  if (err == cudaSuccess) err = cudaMemsetAsync(dw_down, 0, sh.N_r * gi, cs);
+  if (sh.N_s > 0) {
+    if (err == cudaSuccess) err = cudaMemsetAsync(dws_gate, 0, sh.N_s * gi, cs);
+    if (err == cudaSuccess) err = cudaMemsetAsync(dws_up, 0, sh.N_s * gi, cs);
+    if (err == cudaSuccess) err = cudaMemsetAsync(dws_down, 0, sh.N_s * gi, cs);
+  }
+  return cuda_status(err);
+}
+
+}  // namespace
+
 size_t moe_backward_workspace(moe_shape sh, int32_t n_seq) {
   if (sh.T <= 0 || sh.N_r <= 0 || sh.d <= 0 || sh.I <= 0 || n_seq < 0) return 0;
   return bwd_ws(sh, n_seq).total;
@@ -396,19 +415,8 @@ moe_status moe_backward(const void* u, const void* e, const float* s, const int3
   const bool balance = n_seq > 0 && alpha != 0.f;
   if (balance && !ok_ptr(seq_offsets)) return MOE_ERR_INVALID_ARG;
   const cudaStream_t cs = S(stream);
-  if (sh.T == 0) {   // no token: every gradient is zero
-    const size_t gi = (size_t)sh.I * sh.d * 4;
-    cudaError_t err = cudaMemsetAsync(de, 0, (size_t)sh.N_r * sh.d * 4, cs);
-    if (err == cudaSuccess) err = cudaMemsetAsync(dw_gate, 0, sh.N_r * gi, cs);
-    if (err == cudaSuccess) err = cudaMemsetAsync(dw_up, 0, sh.N_r * gi, cs);
-    if (err == cudaSuccess) err = cudaMemsetAsync(dw_down, 0, sh.N_r * gi, cs);
-    if (sh.N_s > 0) {
-      if (err == cudaSuccess) err = cudaMemsetAsync(dws_gate, 0, sh.N_s * gi, cs);
-      if (err == cudaSuccess) err = cudaMemsetAsync(dws_up, 0, sh.N_s * gi, cs);
-      if (err == cudaSuccess) err = cudaMemsetAsync(dws_down, 0, sh.N_s * gi, cs);
-    }
-    return cuda_status(err);
-  }
+  if (sh.T == 0)   // no token: every gradient is zero
+    return zero_grads(sh, de, dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down, cs);
   if (!ok_ptr(u) || !ok_ptr(s) || !ok_ptr(topk_idx) || !ok_ptr(topk_gate) || !ok_ptr(expert_offset) ||
       !ok_ptr(inv_row) || !ok_ptr(x_perm) || !ok_ptr(y) || !ok_ptr(dh) || !ok_ptr(du))
     return MOE_ERR_INVALID_ARG;
@@ -436,6 +444,209 @@ moe_status moe_backward(const void* u, const void* e, const float* s, const int3
   if (err == cudaSuccess)
     err = launch_bwd_combine(dh, reinterpret_cast<const float*>(ws + L.dur), ws + L.dX, inv_row,
                              sh.T, sh.d, sh.K_r, sh.N_s, du, cs);
+  return cuda_status(err);
+}
+
+moe_status moe_fp8_dgrad_weights_make(const moe_expert_weights* w, moe_shape sh,
+                                      const moe_fp8_dgrad_weights* wt, void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(sh, w)) != MOE_OK) return st;
+  if (w->dtype != MOE_E4M3 || wt == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(wt->wdt) || !ok_ptr(wt->wdt_scale) || !ok_ptr(wt->wgut) || !ok_ptr(wt->wgut_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (sh.N_s > 0 && (!ok_ptr(wt->s_wdt) || !ok_ptr(wt->s_wdt_scale) || !ok_ptr(wt->s_wgut) ||
+                     !ok_ptr(wt->s_wgut_scale)))
+    return MOE_ERR_INVALID_ARG;
+  const cudaStream_t cs = S(stream);
+  auto u8 = [](const void* p) { return static_cast<const uint8_t*>(p); };
+  auto m8 = [](void* p) { return static_cast<uint8_t*>(p); };
+  cudaError_t err = cudaSuccess;
+  for (int sh_part = 0; sh_part < 2 && err == cudaSuccess; ++sh_part) {
+    const int E = sh_part ? sh.N_s : sh.N_r;
+    if (E == 0) continue;
+    const void* gate = sh_part ? w->s_gate : w->gate;
+    const void* up = sh_part ? w->s_up : w->up;
+    const void* down = sh_part ? w->s_down : w->down;
+    const float* gs = sh_part ? w->s_gate_scale : w->gate_scale;
+    const float* us = sh_part ? w->s_up_scale : w->up_scale;
+    const float* ds = sh_part ? w->s_down_scale : w->down_scale;
+    void* wdt = sh_part ? wt->s_wdt : wt->wdt;
+    float* wdts = sh_part ? wt->s_wdt_scale : wt->wdt_scale;
+    void* wgut = sh_part ? wt->s_wgut : wt->wgut;
+    float* wguts = sh_part ? wt->s_wgut_scale : wt->wgut_scale;
+    err = launch_fp8_transpose(u8(down), ds, E, sh.d, sh.I, m8(wdt), wdts, sh.d, 0, cs);
+    if (err == cudaSuccess) err = launch_fp8_transpose(u8(gate), gs, E, sh.I, sh.d, m8(wgut), wguts, 2 * sh.I, 0, cs);
+    if (err == cudaSuccess)
+      err = launch_fp8_transpose(u8(up), us, E, sh.I, sh.d, m8(wgut), wguts, 2 * sh.I, sh.I, cs);
+  }
+  return cuda_status(err);
+}
+
+namespace {
+
+struct Fp8BwdWs {
+  size_t hq, hs, a, c, dY, dYq, dYs, dH, acq, acs, dA, dC, dX;
+  size_t t_dY, s_dY, t_h, s_h, t_dA, s_dA, t_dC, s_dC, t_x, s_x, dz, dur, counts, total;
+  long long Rp;
+};
+
+Fp8BwdWs fp8_bwd_ws(const moe_shape& sh, int n_seq) {
+  const size_t R = (size_t)sh.T * sh.K_r + (size_t)sh.N_s * sh.T;
+  const size_t d = sh.d, I = sh.I;
+  Fp8BwdWs w;
+  // padded Wgrad row space: every segment rounded up to whole 128-token blocks
+  w.Rp = (long long)(((R + 127) / 128) * 128 + 128 * (size_t)(sh.N_r + sh.N_s));
+  const size_t Rp = (size_t)w.Rp, nb = Rp / 128;
+  size_t o = 0;
+  auto take = [&](size_t& f, size_t bytes) { f = o; o += align256(bytes); };
+  take(w.hq, R * I);
+  take(w.hs, R * (I / 128) * 4);
+  take(w.a, R * I * 2);
+  take(w.c, R * I * 2);
+  take(w.dY, R * d * 2);
+  take(w.dYq, R * d);
+  take(w.dYs, R * (d / 128) * 4);
+  take(w.dH, R * I * 2);
+  take(w.acq, R * 2 * I);
+  take(w.acs, R * (2 * I / 128) * 4);
+  take(w.dA, R * I * 2);
+  take(w.dC, R * I * 2);
+  take(w.dX, R * d * 2);
+  take(w.t_dY, d * Rp);
+  take(w.s_dY, nb * d * 4);
+  take(w.t_h, I * Rp);
+  take(w.s_h, nb * I * 4);
+  take(w.t_dA, I * Rp);
+  take(w.s_dA, nb * I * 4);
+  take(w.t_dC, I * Rp);
+  take(w.s_dC, nb * I * 4);
+  take(w.t_x, d * Rp);
+  take(w.s_x, nb * d * 4);
+  take(w.dz, (size_t)sh.T * sh.N_r * 2);
+  take(w.dur, (size_t)sh.T * d * 4);
+  take(w.counts, (size_t)(n_seq > 0 ? n_seq : 1) * sh.N_r * 4);
+  w.total = o;
+  return w;
+}
+
+}  // namespace
+
+size_t moe_backward_fp8_workspace(moe_shape sh, int32_t n_seq) {
+  if (sh.T <= 0 || sh.N_r <= 0 || sh.d <= 0 || sh.I <= 0 || n_seq < 0) return 0;
+  return fp8_bwd_ws(sh, n_seq).total;
+}
+
+moe_status moe_backward_fp8(const void* u, const void* u_q, const float* u_scale, const void* e,
+                            const float* s, const int32_t* topk_idx, const float* topk_gate,
+                            const int32_t* expert_offset, const int32_t* inv_row, const void* x_perm_q,
+                            const float* x_perm_scale, const void* y, const moe_expert_weights* w,
+                            const moe_fp8_dgrad_weights* wt, moe_shape sh, const int32_t* seq_offsets,
+                            int32_t n_seq, float alpha, const float* dh, float* du, float* de,
+                            float* dw_gate, float* dw_up, float* dw_down, float* dws_gate,
+                            float* dws_up, float* dws_down, void* workspace, size_t ws_bytes,
+                            void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(sh, w)) != MOE_OK) return st;
+  if (w->dtype != MOE_E4M3 || wt == nullptr) return MOE_ERR_INVALID_ARG;
+  if (sh.N_r % 64 != 0 || n_seq < 0 || !(alpha >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(e) || !ok_ptr(de) || !ok_ptr(dw_gate) || !ok_ptr(dw_up) || !ok_ptr(dw_down))
+    return MOE_ERR_INVALID_ARG;
+  if (sh.N_s > 0 && (!ok_ptr(dws_gate) || !ok_ptr(dws_up) || !ok_ptr(dws_down)))
+    return MOE_ERR_INVALID_ARG;
+  const bool balance = n_seq > 0 && alpha != 0.f;
+  if (balance && !ok_ptr(seq_offsets)) return MOE_ERR_INVALID_ARG;
+  if (sh.T == 0)   // no token: every gradient is zero
+    return zero_grads(sh, de, dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down, S(stream));
+  if (!ok_ptr(u) || !ok_ptr(u_q) || !ok_ptr(u_scale) || !ok_ptr(s) || !ok_ptr(topk_idx) ||
+      !ok_ptr(topk_gate) || !ok_ptr(expert_offset) || !ok_ptr(inv_row) || !ok_ptr(x_perm_q) ||
+      !ok_ptr(x_perm_scale) || !ok_ptr(y) || !ok_ptr(dh) || !ok_ptr(du) || !ok_ptr(wt->wdt) ||
+      !ok_ptr(wt->wdt_scale) || !ok_ptr(wt->wgut) || !ok_ptr(wt->wgut_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (sh.N_s > 0 && (!ok_ptr(wt->s_wdt) || !ok_ptr(wt->s_wdt_scale) || !ok_ptr(wt->s_wgut) ||
+                     !ok_ptr(wt->s_wgut_scale)))
+    return MOE_ERR_INVALID_ARG;
+  const Fp8BwdWs L = fp8_bwd_ws(sh, n_seq);
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  auto at = [&](size_t off) { return static_cast<void*>(ws + off); };
+  auto u8 = [&](size_t off) { return reinterpret_cast<uint8_t*>(ws + off); };
+  auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  const cudaStream_t cs = S(stream);
+  const FfnShape fs = ffn_shape(sh);
+  const long long R = (long long)sh.T * sh.K_r + (long long)sh.N_s * sh.T;
+  const long long routed = (long long)sh.T * sh.K_r;
+  // Fprop again: the E4M3 h Wgrad reads, and the pre-activations a, c (bf16)
+  cudaError_t err = launch_ffn_up_fp8(fs, x_perm_q, x_perm_scale, u_q, u_scale, expert_offset, w, at(L.hq),
+                                      f32(L.hs), cs, at(L.a), at(L.c));
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  if (err == cudaSuccess && balance)
+    err = launch_seq_counts(topk_idx, seq_offsets, n_seq, sh.T, sh.N_r, sh.K_r, counts, cs);
+  if (err == cudaSuccess)
+    err = launch_bwd_prep(dh, y, s, topk_idx, topk_gate, inv_row, counts, seq_offsets, balance ? n_seq : 0,
+                          balance ? alpha : 0.f, sh.T, sh.d, sh.N_r, sh.K_r, sh.N_s, at(L.dz), at(L.dY), cs);
+  // Dgrad: dH = dY W_down (dY in 1x128 tiles), the SwiGLU backward, dX = [dA|dC] [W_gate; W_up]
+  if (err == cudaSuccess) err = launch_quantize_e4m3(at(L.dY), MOE_BF16, R, sh.d, 1, u8(L.dYq), f32(L.dYs), cs);
+  if (err == cudaSuccess) {
+    FfnShape fd = fs;
+    fd.d = sh.I;
+    fd.I = sh.d;
+    moe_expert_weights wd{};
+    wd.dtype = MOE_E4M3;
+    wd.down = wt->wdt;
+    wd.down_scale = wt->wdt_scale;
+    wd.s_down = wt->s_wdt;
+    wd.s_down_scale = wt->s_wdt_scale;
+    err = launch_ffn_down_fp8(fd, at(L.dYq), f32(L.dYs), expert_offset, &wd, at(L.dH), cs);
+  }
+  if (err == cudaSuccess)
+    err = launch_fp8_swiglu_bwd(at(L.dH), at(L.a), at(L.c), R, sh.I, u8(L.acq), f32(L.acs), at(L.dA), at(L.dC), cs);
+  if (err == cudaSuccess) {
+    FfnShape fx = fs;
+    fx.I = 2 * sh.I;
+    moe_expert_weights wx{};
+    wx.dtype = MOE_E4M3;
+    wx.down = wt->wgut;
+    wx.down_scale = wt->wgut_scale;
+    wx.s_down = wt->s_wgut;
+    wx.s_down_scale = wt->s_wgut_scale;
+    err = launch_ffn_down_fp8(fx, at(L.acq), f32(L.acs), expert_offset, &wx, at(L.dX), cs);
+  }
+  // Wgrad operands: 128x1 tiles over each segment's tokens, transposed
+  const auto bf = [&](size_t off, long long row, int C) {
+    return static_cast<const void*>(ws + off + (size_t)row * C * 2);
+  };
+  const struct { ColQuantSrc src; int C; size_t q, sc; } ops[5] = {
+      {{bf(L.dY, 0, sh.d), bf(L.dY, routed, sh.d), nullptr, nullptr, sh.T}, sh.d, L.t_dY, L.s_dY},
+      {{ws + L.hq, ws + L.hq + (size_t)routed * sh.I, f32(L.hs), f32(L.hs) + (size_t)routed * (sh.I / 128), sh.T},
+       sh.I, L.t_h, L.s_h},
+      {{bf(L.dA, 0, sh.I), bf(L.dA, routed, sh.I), nullptr, nullptr, sh.T}, sh.I, L.t_dA, L.s_dA},
+      {{bf(L.dC, 0, sh.I), bf(L.dC, routed, sh.I), nullptr, nullptr, sh.T}, sh.I, L.t_dC, L.s_dC},
+      {{x_perm_q, u_q, x_perm_scale, u_scale, 0}, sh.d, L.t_x, L.s_x}};
+  for (int i = 0; i < 5 && err == cudaSuccess; ++i)
+    err = launch_fp8_colquant(ops[i].src, expert_offset, sh.T, sh.K_r, sh.N_r, sh.N_s, ops[i].C, u8(ops[i].q),
+                              f32(ops[i].sc), L.Rp, cs);
+  // Wgrad: dW_down = dY^T h, dW_gate = dA^T x, dW_up = dC^T x per expert
+  if (err == cudaSuccess)
+    err = launch_fp8_wgrad(u8(L.t_dY), f32(L.s_dY), u8(L.t_h), f32(L.s_h), sh.d, sh.I, L.Rp, expert_offset,
+                           sh.T, sh.K_r, sh.N_r, sh.N_s, dw_down, dws_down, cs);
+  if (err == cudaSuccess)
+    err = launch_fp8_wgrad(u8(L.t_dA), f32(L.s_dA), u8(L.t_x), f32(L.s_x), sh.I, sh.d, L.Rp, expert_offset,
+                           sh.T, sh.K_r, sh.N_r, sh.N_s, dw_gate, dws_gate, cs);
+  if (err == cudaSuccess)
+    err = launch_fp8_wgrad(u8(L.t_dC), f32(L.s_dC), u8(L.t_x), f32(L.s_x), sh.I, sh.d, L.Rp, expert_offset,
+                           sh.T, sh.K_r, sh.N_r, sh.N_s, dw_up, dws_up, cs);
+  // router: du = dz e, de = dz^T u (bf16, as in the FP8 forward)
+  if (err == cudaSuccess) {
+    BwdGemmIo io{fs, expert_offset, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, u, e,
+                 nullptr, nullptr, nullptr, nullptr, at(L.dz), nullptr, nullptr, nullptr, nullptr, nullptr,
+                 nullptr, nullptr, nullptr, nullptr, f32(L.dur), de};
+    io.experts = false;
+    err = launch_bwd_gemms(io, cs);
+  }
+  if (err == cudaSuccess)
+    err = launch_bwd_combine(dh, f32(L.dur), at(L.dX), inv_row, sh.T, sh.d, sh.K_r, sh.N_s, du, cs);
   return cuda_status(err);
 }
 

@@ -529,45 +529,48 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
   };
   cudaError_t err;
 
-  // dH = dY W_down, then the SwiGLU backward -> dA, dC
-  if (!map_mn(&m[0], io.w_down, s.I, (uint64_t)s.N_r * s.d) || !map_mn(&m[1], wsd, s.I, Es * s.d) ||
-      !map_k(&m[4], io.dY, s.d, R, BN))
-    return cudaErrorInvalidValue;
-  same(2);
-  g.o_bf0 = io.dA;
-  g.o_bf1 = io.dC;
-  if ((err = launch_kind<kDH>(m, g, tok_tiles * ((s.I + BM - 1) / BM), st)) != cudaSuccess) return err;
+  if (io.experts) {
+    // dH = dY W_down, then the SwiGLU backward -> dA, dC
+    if (!map_mn(&m[0], io.w_down, s.I, (uint64_t)s.N_r * s.d) || !map_mn(&m[1], wsd, s.I, Es * s.d) ||
+        !map_k(&m[4], io.dY, s.d, R, BN))
+      return cudaErrorInvalidValue;
+    same(2);
+    g.o_bf0 = io.dA;
+    g.o_bf1 = io.dC;
+    if ((err = launch_kind<kDH>(m, g, tok_tiles * ((s.I + BM - 1) / BM), st)) != cudaSuccess) return err;
 
-  // dX = dA W_gate + dC W_up
-  if (!map_mn(&m[0], io.w_gate, s.d, (uint64_t)s.N_r * s.I) ||
-      !map_mn(&m[1], io.w_up, s.d, (uint64_t)s.N_r * s.I) || !map_mn(&m[2], wsg, s.d, Es * s.I) ||
-      !map_mn(&m[3], wsu, s.d, Es * s.I) || !map_k(&m[4], io.dA, s.I, R, BN) || !map_k(&m[5], io.dC, s.I, R, BN))
-    return cudaErrorInvalidValue;
-  g.o_bf0 = io.dX;
-  g.o_bf1 = nullptr;
-  if ((err = launch_kind<kDX>(m, g, tok_tiles * ((s.d + BM - 1) / BM), st)) != cudaSuccess) return err;
+    // dX = dA W_gate + dC W_up
+    if (!map_mn(&m[0], io.w_gate, s.d, (uint64_t)s.N_r * s.I) ||
+        !map_mn(&m[1], io.w_up, s.d, (uint64_t)s.N_r * s.I) || !map_mn(&m[2], wsg, s.d, Es * s.I) ||
+        !map_mn(&m[3], wsu, s.d, Es * s.I) || !map_k(&m[4], io.dA, s.I, R, BN) || !map_k(&m[5], io.dC, s.I, R, BN))
+      return cudaErrorInvalidValue;
+    g.o_bf0 = io.dX;
+    g.o_bf1 = nullptr;
+    if ((err = launch_kind<kDX>(m, g, tok_tiles * ((s.d + BM - 1) / BM), st)) != cudaSuccess) return err;
 
-  // dW_down[e] = dY^T h over the expert's rows
-  if (!map_mn(&m[0], io.dY, s.d, R) || !map_mn(&m[4], io.h, s.I, R)) return cudaErrorInvalidValue;
-  same(1);
-  g.o_f0 = io.dw_down;
-  g.o_fs0 = io.dws_down;
-  if ((err = launch_kind<kDWD>(m, g, (long long)segs * ((s.d + BM - 1) / BM) * ((s.I + BN - 1) / BN),
-                               st)) != cudaSuccess)
-    return err;
+    // dW_down[e] = dY^T h over the expert's rows
+    if (!map_mn(&m[0], io.dY, s.d, R) || !map_mn(&m[4], io.h, s.I, R)) return cudaErrorInvalidValue;
+    same(1);
+    g.o_f0 = io.dw_down;
+    g.o_fs0 = io.dws_down;
+    if ((err = launch_kind<kDWD>(m, g, (long long)segs * ((s.d + BM - 1) / BM) * ((s.I + BN - 1) / BN),
+                                 st)) != cudaSuccess)
+      return err;
 
-  // dW_gate[e] = dA^T x, dW_up[e] = dC^T x (x: x_perm rows, or u for the shared experts)
-  if (!map_mn(&m[0], io.dA, s.I, R) || !map_mn(&m[1], io.dC, s.I, R) ||
-      !map_mn(&m[4], io.x_perm, s.d, (uint64_t)s.T * s.K_r) || !map_mn(&m[5], io.u, s.d, s.T))
-    return cudaErrorInvalidValue;
-  m[2] = m[3] = m[0];
-  g.o_f0 = io.dw_gate;
-  g.o_f1 = io.dw_up;
-  g.o_fs0 = io.dws_gate;
-  g.o_fs1 = io.dws_up;
-  if ((err = launch_kind<kDWGU>(m, g, 2LL * segs * ((s.I + BM - 1) / BM) * ((s.d + BN - 1) / BN),
-                                st)) != cudaSuccess)
-    return err;
+    // dW_gate[e] = dA^T x, dW_up[e] = dC^T x (x: x_perm rows, or u for the shared experts)
+    if (!map_mn(&m[0], io.dA, s.I, R) || !map_mn(&m[1], io.dC, s.I, R) ||
+        !map_mn(&m[4], io.x_perm, s.d, (uint64_t)s.T * s.K_r) || !map_mn(&m[5], io.u, s.d, s.T))
+      return cudaErrorInvalidValue;
+    m[2] = m[3] = m[0];
+    g.o_f0 = io.dw_gate;
+    g.o_f1 = io.dw_up;
+    g.o_fs0 = io.dws_gate;
+    g.o_fs1 = io.dws_up;
+    if ((err = launch_kind<kDWGU>(m, g, 2LL * segs * ((s.I + BM - 1) / BM) * ((s.d + BN - 1) / BN),
+                                  st)) != cudaSuccess)
+      return err;
+  }
+  if (!io.router) return cudaSuccess;
 
   // router: du = dz e, de = dz^T u
   if (!map_k(&m[0], io.dz, s.N_r, s.T, BM) || !map_mn(&m[4], io.e, s.d, s.N_r)) return cudaErrorInvalidValue;

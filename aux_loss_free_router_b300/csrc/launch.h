@@ -79,7 +79,7 @@ cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h,
 cudaError_t launch_ffn_up_fp8(const FfnShape& s, const void* x_perm, const float* x_perm_scale,
                               const void* u, const float* u_scale, const int32_t* expert_offset,
                               const moe_expert_weights* w, void* h, float* h_scale,
-                              cudaStream_t st);
+                              cudaStream_t st, void* save_a = nullptr, void* save_c = nullptr);
 cudaError_t launch_ffn_down_fp8(const FfnShape& s, const void* h, const float* h_scale,
                                 const int32_t* expert_offset, const moe_expert_weights* w,
                                 void* y, cudaStream_t st);
@@ -101,8 +101,44 @@ struct BwdGemmIo {
   float *dw_gate, *dw_up, *dw_down, *dws_gate, *dws_up, *dws_down;
   float* du_router;     // [T, d]
   float* de;            // [N_r, d]
+  bool experts = true;  // the expert GEMMs (dH, dX, dW_*) ...
+  bool router = true;   // ... and the router's (du = dz e, de = dz^T u)
 };
 cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st);
+
+// FP8 backward (bwd_fp8.cu).
+// dst [E][C, ldd] at column col0 <- src [E][R, C]^T (E4M3 codes), and the 128x128 block
+// scales dst_s [E][C/128, ldd/128] at column col0/128 <- src_s [E][R/128, C/128]^T.
+cudaError_t launch_fp8_transpose(const uint8_t* src, const float* src_s, int E, int R, int C,
+                                 uint8_t* dst, float* dst_s, int ldd, int col0, cudaStream_t st);
+// SwiGLU backward from dH, a, c (bf16 [rows, I]): dA = dH c silu'(a), dC = dH silu(a) in
+// fp32; ac_q [rows, 2I] = E4M3 1x128 tiles of (dA | dC) with scales ac_s [rows, 2I/128],
+// and dA, dC rounded to bf16.
+cudaError_t launch_fp8_swiglu_bwd(const void* dH, const void* a, const void* c, long long rows, int I,
+                                  uint8_t* ac_q, float* ac_s, void* dA, void* dC, cudaStream_t st);
+// Wgrad operand: the columns of an activation [rows, C] over each expert segment's tokens,
+// E4M3 per 128x1 tile, transposed: q [C, Rp] (segment s at column pstart(s), padded to a
+// multiple of 128 with zero codes) and scales [Rp/128, C].  Segment i < N_r is rows
+// [off[i], off[i+1]) of `routed`; shared segment j reads rows j*shared_stride .. + T of
+// `shared`.  Source values: bf16 (src_scale null) or E4M3 codes with 1x128 scales
+// (src_scale [rows, C/128], shared_scale likewise).
+struct ColQuantSrc {
+  const void* routed;
+  const void* shared;
+  const float* routed_scale;
+  const float* shared_scale;
+  long long shared_stride;   // rows between shared segments in `shared`
+};
+cudaError_t launch_fp8_colquant(const ColQuantSrc& src, const int32_t* expert_offset, int T, int K_r,
+                                int N_r, int N_s, int C, uint8_t* q, float* scale, long long Rp,
+                                cudaStream_t st);
+// Wgrad GEMM per expert segment: out_e [M, N] (fp32, row-major) = sum over the segment's
+// 128-token blocks kb of diag(sa[kb, :]) (A_kb B_kb^T) diag(sb[kb, :]), with A = qa [M, Rp],
+// B = qb [N, Rp] E4M3 (K = tokens), sa [Rp/128, M], sb [Rp/128, N]; routed experts to out
+// [N_r][M, N], shared ones to out_s [N_s][M, N].  An expert without tokens gets zeros.
+cudaError_t launch_fp8_wgrad(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                             int M, int N, long long Rp, const int32_t* expert_offset, int T, int K_r,
+                             int N_r, int N_s, float* out, float* out_s, cudaStream_t st);
 // Per (sequence, expert) selection counts (int32 [n_seq, N_r], zeroed here first).
 cudaError_t launch_seq_counts(const int32_t* topk_idx, const int32_t* seq_offsets, int n_seq,
                               int T, int N_r, int K_r, int32_t* counts, cudaStream_t st);

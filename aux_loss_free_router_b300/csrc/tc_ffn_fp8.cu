@@ -68,6 +68,10 @@ struct Fp8Args {
   void* out;                 // MODE 0: h codes [R, I]; MODE 1: y bf16 [R, d]
   float* out_scale;          // MODE 0: h scales [R, I/128]
   int32_t* err;
+  // MODE 0, optional: the fp32 pre-activations a = x W_gate^T and c = x W_up^T rounded
+  // to bf16, [R, I] in h's row space (kept for the backward pass)
+  __nv_bfloat16* save_a = nullptr;
+  __nv_bfloat16* save_c = nullptr;
 };
 
 __device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
@@ -284,6 +288,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool row_ok = row_local < tcd.rows;
       const size_t out_row = (size_t)tcd.out_row0 + row_local;
       if (MODE == 0) {
+        if (args.save_a && row_ok) {
+          const size_t o = out_row * N + tcd.n * 128 + cq * 32;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            reinterpret_cast<uint4*>(args.save_a + o)[v] =
+                make_uint4(pack_bf16(acc[8 * v], acc[8 * v + 1]), pack_bf16(acc[8 * v + 2], acc[8 * v + 3]),
+                           pack_bf16(acc[8 * v + 4], acc[8 * v + 5]), pack_bf16(acc[8 * v + 6], acc[8 * v + 7]));
+            reinterpret_cast<uint4*>(args.save_c + o)[v] =
+                make_uint4(pack_bf16(acc[32 + 8 * v], acc[33 + 8 * v]), pack_bf16(acc[34 + 8 * v], acc[35 + 8 * v]),
+                           pack_bf16(acc[36 + 8 * v], acc[37 + 8 * v]), pack_bf16(acc[38 + 8 * v], acc[39 + 8 * v]));
+          }
+        }
         // h for this thread's 32 columns, then the 1x128 tile scale from all four quarters
         float amax = 0.f;
 #pragma unroll
@@ -359,7 +375,7 @@ constexpr CUtensorMapDataType kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 cudaError_t launch_ffn_up_fp8(const FfnShape& s, const void* x_perm, const float* x_perm_scale,
                               const void* u, const float* u_scale, const int32_t* expert_offset,
                               const moe_expert_weights* w, void* h, float* h_scale,
-                              cudaStream_t st) {
+                              cudaStream_t st, void* save_a, void* save_c) {
   if (s.T == 0) return cudaSuccess;
   CUtensorMap m[6];
   const uint64_t rb = (uint64_t)s.d;
@@ -378,7 +394,8 @@ cudaError_t launch_ffn_up_fp8(const FfnShape& s, const void* x_perm, const float
   if (!ok) return cudaErrorInvalidValue;
   Fp8Args a{s, expert_offset, x_perm_scale, u_scale, w->gate_scale, w->up_scale,
             s.N_s > 0 ? w->s_gate_scale : w->gate_scale, s.N_s > 0 ? w->s_up_scale : w->up_scale,
-            h, h_scale, dev_error_ptr()};
+            h, h_scale, dev_error_ptr(), static_cast<__nv_bfloat16*>(save_a),
+            static_cast<__nv_bfloat16*>(save_c)};
   return launch<0>(s, m, a, st);
 }
 

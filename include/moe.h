@@ -292,6 +292,58 @@ MOE_API moe_status moe_backward(const void* u, const void* e, const float* s,
                                 size_t ws_bytes, void* stream);
 
 /* --------------------------------------------------------------------------------
+ * FP8 backward pass: the same gradients for a layer whose expert GEMMs run in E4M3.
+ * pwwt.cn notes §三: the three GEMMs of a linear layer - Fprop, Dgrad (activation
+ * gradient) and Wgrad (weight gradient) - take E4M3 inputs with fp32 outputs, and
+ * Wgrad reads activations kept in E4M3 from the forward pass; the reading guide's FP8
+ * bullet (Key ideas): activations scaled per 1x128 tile, weights per 128x128 block,
+ * promotion to fp32 every 128 elements of the contraction.  Here an activation tile
+ * lies along the contraction of the GEMM that reads it: 1x128 in Fprop and Dgrad,
+ * 128x1 (one feature over 128 tokens of an expert's segment, the last tile short) in
+ * Wgrad; dY = g*dh, dA and dC are quantised from their own values for each; Wgrad's
+ * activations are the forward's E4M3 tokens and E4M3 h (the latter recomputed by the
+ * forward's FP8 gate/up kernel), re-tiled 128x1.  Routing, gates, the balance loss and
+ * the affinity gradients du = dz e, de = dz^T u stay bf16 / fp32, as in the FP8 forward.
+ *
+ * moe_fp8_dgrad_weights_make: the transposed E4M3 weights Dgrad multiplies by (once per
+ * weight update): for the routed experts (E = N_r) and the shared ones (E = N_s, s_*),
+ *   wdt  [E, I, d]  = W_down^T                    scales [E, I/128, d/128]
+ *   wgut [E, d, 2I] = [W_gate^T | W_up^T]         scales [E, d/128, 2I/128]
+ * taken from w (MOE_E4M3, d and I multiples of 128); the codes and scales are those of
+ * w, moved (a 128x128 block of W is one of W^T).
+ *
+ * moe_backward_fp8: inputs as moe_backward, plus the forward's E4M3 state: u_q / u_scale
+ * (moe_quantize_e4m3 of u, 1x128), x_perm_q / x_perm_scale (the dispatched codes and
+ * scales); y: the FP8 forward's expert outputs (bf16); w: the E4M3 weights; wt: from
+ * moe_fp8_dgrad_weights_make.  u (bf16) feeds the router gradients.  Outputs as
+ * moe_backward.  workspace: moe_backward_fp8_workspace(sh, n_seq) bytes.
+ * Requirements beyond the shape checks: N_r % 64 == 0, d % 128 == 0, I % 128 == 0. */
+typedef struct {
+    void* wdt;
+    float* wdt_scale;
+    void* wgut;
+    float* wgut_scale;
+    void* s_wdt;
+    float* s_wdt_scale;
+    void* s_wgut;
+    float* s_wgut_scale;
+} moe_fp8_dgrad_weights;
+MOE_API moe_status moe_fp8_dgrad_weights_make(const moe_expert_weights* w, moe_shape sh,
+                                              const moe_fp8_dgrad_weights* wt, void* stream);
+MOE_API size_t moe_backward_fp8_workspace(moe_shape sh, int32_t n_seq);
+MOE_API moe_status moe_backward_fp8(const void* u, const void* u_q, const float* u_scale,
+                                    const void* e, const float* s, const int32_t* topk_idx,
+                                    const float* topk_gate, const int32_t* expert_offset,
+                                    const int32_t* inv_row, const void* x_perm_q,
+                                    const float* x_perm_scale, const void* y,
+                                    const moe_expert_weights* w, const moe_fp8_dgrad_weights* wt,
+                                    moe_shape sh, const int32_t* seq_offsets, int32_t n_seq,
+                                    float alpha, const float* dh, float* du, float* de,
+                                    float* dw_gate, float* dw_up, float* dw_down, float* dws_gate,
+                                    float* dws_up, float* dws_down, void* workspace,
+                                    size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------------
  * Device error word.  Kernels that wait on asynchronous copies bound every wait;
  * a wait that runs out records MOE_ERR_TIMEOUT here and the kernel returns early.
  * Kernels that find an invalid device-resident value record MOE_ERR_INVALID_ARG.
