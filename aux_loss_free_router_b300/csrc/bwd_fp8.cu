@@ -275,19 +275,24 @@ __global__ void __launch_bounds__(256) fp8_colquant_kernel(ColQuantSrc src, cons
 //               kind::f8f6f4 MMAs of K = 32 into one of two 256-column TMEM buffers;
 //   warps 2..17 promote each block into fp32 registers: acc += P * (sa[row] * sb[col]),
 //               four warps per TMEM lane quarter, 64 columns each, and store the tile.
-constexpr int WG_BM = 128, WG_BK = 128, WG_BN = 256, WG_STAGES = 4;
+//               A block's 256 column scales sit in a shared-memory double buffer: the
+//               epilogue loads the next block's while it promotes this one (an mbarrier
+//               per buffer says all 512 epilogue threads have stored theirs).
+constexpr int WG_BM = 128, WG_BK = 128, WG_BN = 256, WG_STAGES = 3;
 constexpr int WG_A = WG_BM * WG_BK, WG_B = WG_BN * WG_BK, WG_STAGE = WG_A + WG_B;
 constexpr int WG_EPI_WARPS = 16, WG_THREADS = 64 + WG_EPI_WARPS * 32;
+constexpr int WG_SCR = 32 * 33 * 4;   // per epilogue warp: 32 rows x 32 columns (+1 pad), fp32
 
 struct WgCtrl {
-  uint64_t full[WG_STAGES], empty[WG_STAGES], pfull[2], pempty[2], fin;
+  uint64_t full[WG_STAGES], empty[WG_STAGES], pfull[2], pempty[2], sfill[2], fin;
   uint32_t tmem_base;
   int abort_flag;
+  float sbuf[2][WG_BN];   // column scales of a 128-token block, by block parity
   int blk[kMaxSegs + 1];
   int seg_rows[kMaxSegs];
 };
 
-constexpr size_t kWgSmem = (size_t)WG_STAGES * WG_STAGE + sizeof(WgCtrl) + 1024;
+constexpr size_t kWgSmem = (size_t)WG_STAGES * WG_STAGE + (size_t)WG_EPI_WARPS * WG_SCR + sizeof(WgCtrl) + 1024;
 static_assert(kWgSmem <= 227 * 1024, "shared memory per CTA");
 
 struct WgArgs {
@@ -305,7 +310,8 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_off = tc::smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_off & 1023u)) & 1023u);
-  WgCtrl& C = *reinterpret_cast<WgCtrl*>(base + WG_STAGES * WG_STAGE);
+  float* scr_all = reinterpret_cast<float*>(base + WG_STAGES * WG_STAGE);
+  WgCtrl& C = *reinterpret_cast<WgCtrl*>(base + WG_STAGES * WG_STAGE + WG_EPI_WARPS * WG_SCR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nseg = g.N_r + g.N_s;
   const int mt = g.M / WG_BM, nt = (g.N + WG_BN - 1) / WG_BN;
@@ -319,6 +325,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&C.pfull[i], 1);
       tc::mbar_init(&C.pempty[i], WG_EPI_WARPS * 32);
+      tc::mbar_init(&C.sfill[i], WG_EPI_WARPS * 32);   // every epilogue thread, per use
     }
     tc::mbar_init(&C.fin, 1);
     C.abort_flag = 0;
@@ -392,8 +399,27 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     // ------------------------------------------------------------ epilogue --
     const int q = warp & 3;               // TMEM lane quarter
     const int cq = (warp - 2) >> 2;       // column quarter: 64 columns
+    const int et = threadIdx.x - 64;      // 0 .. 511
+    // the (tile, block) after (tile, kb) in this CTA's walk, or tile = -1
+    auto next_chunk = [&](int tile, int kb, int& nt_tile, int& nkb) {
+      const int seg = tile / (mt * nt);
+      if (kb + 1 < C.blk[seg + 1]) { nt_tile = tile; nkb = kb + 1; return; }
+      for (int t2 = tile + (int)gridDim.x; t2 < total; t2 += (int)gridDim.x) {
+        const int s2 = t2 / (mt * nt);
+        if (C.blk[s2 + 1] > C.blk[s2]) { nt_tile = t2; nkb = C.blk[s2]; return; }
+      }
+      nt_tile = -1;
+      nkb = 0;
+    };
+    // the scale of column et (< 256) of (tile, block kb), 0 past N
+    auto col_scale = [&](int tile, int kb) -> float {
+      const int rem = tile - (tile / (mt * nt)) * (mt * nt);
+      const int col = (rem % nt) * WG_BN + et;
+      return (et < WG_BN && col < g.N) ? __ldg(g.sb + (size_t)kb * g.N + col) : 0.f;
+    };
     int c = 0;
     bool alive = true;
+    bool staged = false;                  // sbuf[c & 1] already holds this block's scales
     for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x) {
       const int seg = tile / (mt * nt), rem = tile - seg * (mt * nt);
       const int m = rem / nt, n = rem - m * nt;
@@ -405,22 +431,28 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
       for (int j = 0; j < 64; ++j) acc[j] = 0.f;
 #pragma unroll 1
       for (int kb = C.blk[seg]; kb < C.blk[seg + 1]; ++kb, ++c) {
-        const float sa = __ldg(g.sa + (size_t)kb * g.M + row);
-        const float* sbp = g.sb + (size_t)kb * g.N + col0;
         const int buf = c & 1;
+        if (!staged) {
+          if (et < WG_BN) C.sbuf[buf][et] = col_scale(tile, kb);
+          tc::mbar_arrive(&C.sfill[buf]);   // release: the store is visible after the wait
+        }
+        const bool filled = tc::mbar_wait(&C.sfill[buf], (c >> 1) & 1, abort_flag, g.err);
+        if (!__all_sync(0xffffffffu, filled)) { alive = false; break; }
+        int t2, kb2;
+        next_chunk(tile, kb, t2, kb2);
+        const float pf = t2 >= 0 ? col_scale(t2, kb2) : 0.f;   // in flight during the promotion
+        const float sa = __ldg(g.sa + (size_t)kb * g.M + row);
         const bool got = tc::mbar_wait(&C.pfull[buf], (c >> 1) & 1, abort_flag, g.err);
         if (!__all_sync(0xffffffffu, got)) { alive = false; break; }
         tc::fence_after_sync();
         const uint32_t t_base = tmem_base + (uint32_t)(buf * WG_BN) + ((uint32_t)(q * 32) << 16) + cq * 64;
+        const float* sbs = C.sbuf[buf] + cq * 64;
 #pragma unroll
         for (int g0 = 0; g0 < 64; g0 += 8) {
           uint32_t pv[8];
           tc::tmem_ld8(t_base + g0, pv);
-          float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-          if (cols_ok) {
-            s0 = __ldg(reinterpret_cast<const float4*>(sbp + g0));
-            s1 = __ldg(reinterpret_cast<const float4*>(sbp + g0 + 4));
-          }
+          const float4 s0 = *reinterpret_cast<const float4*>(sbs + g0);
+          const float4 s1 = *reinterpret_cast<const float4*>(sbs + g0 + 4);
           tc::tmem_ld_wait();
           const float sb[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
@@ -428,13 +460,31 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         }
         tc::fence_before_sync();
         tc::mbar_arrive(&C.pempty[buf]);
+        // the next block's scales into the other buffer: every thread finished reading
+        // it (block c - 1) before arriving on this block's sfill, which this thread
+        // has waited for
+        if (t2 >= 0) {
+          if (et < WG_BN) C.sbuf[buf ^ 1][et] = pf;
+          tc::mbar_arrive(&C.sfill[buf ^ 1]);
+        }
+        staged = t2 >= 0;
       }
       if (!alive) break;
       if (cols_ok) {
+        // 32 rows x 64 columns through the warp's scratch, 32 columns at a time, so that
+        // each store writes 128 contiguous bytes of one row
         float* out = seg < g.N_r ? g.out + (size_t)seg * g.M * g.N : g.out_s + (size_t)(seg - g.N_r) * g.M * g.N;
-        float4* dst = reinterpret_cast<float4*>(out + (size_t)row * g.N + col0);
+        float* scr = scr_all + (warp - 2) * (WG_SCR / 4);
+        float* dst = out + (size_t)(row - lane) * g.N + col0 + lane;
 #pragma unroll
-        for (int v = 0; v < 16; ++v) dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) scr[lane * 33 + j] = acc[32 * h + j];
+          __syncwarp();
+#pragma unroll 8
+          for (int r = 0; r < 32; ++r) dst[(size_t)r * g.N + 32 * h] = scr[r * 33 + lane];
+          __syncwarp();
+        }
       }
     }
   }
