@@ -9,10 +9,10 @@
 // of the 128 tokens with all N_r centroids over the c-th slice of d (single-CTA M=128
 // MMAs, TMEM lane = token, column = expert; u and e stream through a 4-stage TMA ring)
 // and writes its partial tile to its own shared memory.  After a cluster barrier CTA c
-// takes tokens [c*R, (c+1)*R), R = 128/C: eight threads per token read the C partials
-// over distributed shared memory and add them in slice order (z is the same for every
-// C-way split of a given launch shape, and bit-identical run to run), then form s, the
-// keys and the decision (route_oct.cuh).  Each CTA sums s_{i,t}/sum_j s_{j,t} over each
+// takes tokens [c*R, (c+1)*R), R = 128/C: one warp per token (lane l: experts l + 32j)
+// reads the C partials over distributed shared memory and adds them in slice order (z is
+// the same for every C-way split of a given launch shape, and bit-identical run to run),
+// then forms s, the keys and the decision with warp reductions (route_warp.cuh).  Each CTA sums s_{i,t}/sum_j s_{j,t} over each
 // run of its tokens that lies in one sequence (fp32, token order) and adds the run sum
 // to that sequence's accumulator as a 64-bit fixed-point integer (units of 2^-32):
 // integer addition is exact and associative, so the totals do not depend on the order
@@ -24,6 +24,7 @@
 
 #include "launch.h"
 #include "route_oct.cuh"
+#include "route_warp.cuh"
 #include "route_select.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -72,35 +73,27 @@ struct FusedArgs {
 
 constexpr double kFix = 4294967296.0;   // 2^32: fixed-point units of the P accumulators
 
-// z[qq] = sum over the CC slices, in slice order, of the float4 at row + 32*qq in the
+// z[j] = sum over the CC slices, in slice order, of the value at row + 32*j in the
 // partial tile of each CTA of the cluster.  The loads of a batch of slices (at most 16
-// float4) are all issued before the first add.
+// values) are all issued before the first add.
 template <int Q, int CC>
-__device__ __forceinline__ void sum_slices(float4 (&z)[Q], const float* row) {
+__device__ __forceinline__ void sum_cols(float (&z)[Q], const float* row) {
   constexpr int PER = (16 / Q) < CC ? (16 / Q) : CC;
 #pragma unroll
   for (int s0 = 0; s0 < CC; s0 += PER) {
-    float4 w[PER][Q];
+    float w[PER][Q];
 #pragma unroll
     for (int bb = 0; bb < PER; ++bb)
 #pragma unroll
-      for (int qq = 0; qq < Q; ++qq)
-        w[bb][qq] = tc::ld_cluster_f4(tc::cluster_addr(row + 32 * qq, (uint32_t)(s0 + bb)));
+      for (int j = 0; j < Q; ++j) w[bb][j] = tc::ld_cluster_f32(tc::cluster_addr(row + 32 * j, (uint32_t)(s0 + bb)));
 #pragma unroll
     for (int bb = 0; bb < PER; ++bb)
 #pragma unroll
-      for (int qq = 0; qq < Q; ++qq) {
-        if (s0 + bb == 0) {
-          z[qq] = w[bb][qq];
-        } else {
-          z[qq].x = __fadd_rn(z[qq].x, w[bb][qq].x); z[qq].y = __fadd_rn(z[qq].y, w[bb][qq].y);
-          z[qq].z = __fadd_rn(z[qq].z, w[bb][qq].z); z[qq].w = __fadd_rn(z[qq].w, w[bb][qq].w);
-        }
-      }
+      for (int j = 0; j < Q; ++j) z[j] = (s0 + bb == 0) ? w[bb][j] : __fadd_rn(z[j], w[bb][j]);
   }
 }
 
-template <int Q>
+template <int Q, int G>
 __global__ void __launch_bounds__(THREADS, 1)
     router_fused_kernel(const __grid_constant__ CUtensorMap mU, const __grid_constant__ CUtensorMap mE,
                         FusedArgs a) {
@@ -211,53 +204,60 @@ __global__ void __launch_bounds__(THREADS, 1)
   // this barrier, also after a timed-out wait)
   tc::cluster_sync();
 
-  // -------------------------------- reduce over the slices, decide, P contributions --
+  // ------------- reduce over the slices, decide, P contributions: a warp per token pair --
+  // A warp takes tokens tl and tl + 8 together (two independent reduction chains) and
+  // loads the next pair's partials over distributed shared memory while it decides.
   const bool aborted = *abort_flag != 0;
-  for (int pass = 0; pass * 32 < R; ++pass) {
-    const int tl = pass * 32 + warp * 4 + (lane >> 3), part_id = lane & 7;
-    const int t = my0 + tl;
-    const bool valid = !aborted && tl < ntok;
-    const int rrow = c * R + tl;                 // row of the partial tiles
-    float4 z[Q];
+  {
+    constexpr int NW = THREADS / 32;
+    float bv[Q];
 #pragma unroll
-    for (int qq = 0; qq < Q; ++qq) z[qq] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) {                                 // slice order: the same sum everywhere
-      const float* row = part + (size_t)rrow * LD + 4 * part_id;
-      if (C == 2) sum_slices<Q, 2>(z, row);
-      else if (C == 4) sum_slices<Q, 4>(z, row);
-      else sum_slices<Q, 8>(z, row);
-    }
-    float sv[Q][4], bv[Q][4];
+    for (int j = 0; j < Q; ++j) bv[j] = __ldg(a.b + lane + 32 * j);
+    auto load_pair = [&](int tl0, float (&z)[2][Q]) {
 #pragma unroll
-    for (int qq = 0; qq < Q; ++qq) {
-      const float4 bb = __ldg(reinterpret_cast<const float4*>(a.b + 32 * qq + 4 * part_id));
-      bv[qq][0] = bb.x; bv[qq][1] = bb.y; bv[qq][2] = bb.z; bv[qq][3] = bb.w;
-      sv[qq][0] = sigmoid_f32(z[qq].x); sv[qq][1] = sigmoid_f32(z[qq].y);
-      sv[qq][2] = sigmoid_f32(z[qq].z); sv[qq][3] = sigmoid_f32(z[qq].w);
-    }
-    if (valid && p.s_out) {
-#pragma unroll
-      for (int qq = 0; qq < Q; ++qq)
-        *reinterpret_cast<float4*>(p.s_out + (size_t)t * N + 32 * qq + 4 * part_id) =
-            make_float4(sv[qq][0], sv[qq][1], sv[qq][2], sv[qq][3]);
-    }
-    if (want_p) {
-      float rs = 0.f;
-#pragma unroll
-      for (int qq = 0; qq < Q; ++qq)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) rs = __fadd_rn(rs, sv[qq][j]);
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, o));
-      if (valid) {
-        const float inv = __frcp_rn(rs);
-#pragma unroll
-        for (int qq = 0; qq < Q; ++qq)
-          *reinterpret_cast<float4*>(sp_tile + (size_t)tl * N + 32 * qq + 4 * part_id) =
-              make_float4(sv[qq][0] * inv, sv[qq][1] * inv, sv[qq][2] * inv, sv[qq][3] * inv);
+      for (int n = 0; n < 2; ++n) {
+        const int tl = min(tl0 + n * NW, max(ntok - 1, 0));          // a spare token re-reads a valid row
+        const float* row = part + (size_t)(c * R + tl) * LD + lane;  // row of the partial tiles
+        if (C == 2) sum_cols<Q, 2>(z[n], row);
+        else if (C == 4) sum_cols<Q, 4>(z[n], row);
+        else sum_cols<Q, 8>(z[n], row);
       }
+    };
+    float z[2][Q];
+    if (warp < ntok && !aborted) load_pair(warp, z);
+    for (int tl0 = warp; tl0 < ntok && !aborted; tl0 += 2 * NW) {
+      float sv[2][Q];
+      int tt[2];
+      bool ok[2];
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        tt[n] = my0 + tl0 + n * NW;
+        ok[n] = tl0 + n * NW < ntok;
+#pragma unroll
+        for (int j = 0; j < Q; ++j) sv[n][j] = sigmoid_f32(z[n][j]);
+      }
+      if (tl0 + 2 * NW < ntok) load_pair(tl0 + 2 * NW, z);            // in flight while deciding
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        if (!ok[n]) continue;
+        if (p.s_out) {
+#pragma unroll
+          for (int j = 0; j < Q; ++j) p.s_out[(size_t)tt[n] * N + lane + 32 * j] = sv[n][j];
+        }
+        if (want_p) {
+          float rs = 0.f;
+#pragma unroll
+          for (int j = 0; j < Q; ++j) rs = __fadd_rn(rs, sv[n][j]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, o));
+          const float inv = __frcp_rn(rs);
+          const int tl = tl0 + n * NW;
+#pragma unroll
+          for (int j = 0; j < Q; ++j) sp_tile[(size_t)tl * N + lane + 32 * j] = sv[n][j] * inv;
+        }
+      }
+      warp_decide<Q, G, 2>(sv, bv, tt, ok, p);
     }
-    oct_decide<Q>(sv, bv, part_id, t, valid, p);
   }
   __syncthreads();
 
@@ -408,10 +408,18 @@ cudaError_t launch_router_fused(const void* u, const void* e, int d, const float
     if (e2 != cudaSuccess) return e2;
     return launch_pdl(kernel, dim3(((p.T + BM - 1) / BM) * C), dim3(THREADS), smem, st, (unsigned)C, mU, mE, a);
   };
-  switch (p.N_r) {
-    case 64: err = go(router_fused_kernel<2>); break;
-    case 128: err = go(router_fused_kernel<4>); break;
-    default: err = go(router_fused_kernel<8>); break;
+  // N_r = 32 Q experts in G groups (G divides Q: router_fused_ok)
+  switch (p.N_r * 16 + p.G) {
+    case 64 * 16 + 1: err = go(router_fused_kernel<2, 1>); break;
+    case 64 * 16 + 2: err = go(router_fused_kernel<2, 2>); break;
+    case 128 * 16 + 1: err = go(router_fused_kernel<4, 1>); break;
+    case 128 * 16 + 2: err = go(router_fused_kernel<4, 2>); break;
+    case 128 * 16 + 4: err = go(router_fused_kernel<4, 4>); break;
+    case 256 * 16 + 1: err = go(router_fused_kernel<8, 1>); break;
+    case 256 * 16 + 2: err = go(router_fused_kernel<8, 2>); break;
+    case 256 * 16 + 4: err = go(router_fused_kernel<8, 4>); break;
+    case 256 * 16 + 8: err = go(router_fused_kernel<8, 8>); break;
+    default: return cudaErrorInvalidValue;
   }
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
