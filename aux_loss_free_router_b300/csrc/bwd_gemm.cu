@@ -75,6 +75,7 @@ struct BwdArgs {
   float* o_fs0;               // kDWD / kDWGU: the shared experts' dW_down / dW_gate
   float* o_fs1;               // kDWGU: the shared experts' dW_up
   int32_t* err;
+  int mn3d = 0;               // MN-major maps are 3-D: one copy per operand per K step
 };
 
 // One output tile: M index = TMEM lane, N index = accumulator column.
@@ -167,8 +168,10 @@ __host__ __device__ constexpr uint32_t idesc(bool a_mn, bool b_mn, int n) {
 // x, x + 64, ...; K-major -> one (64, ROWS) box.
 template <bool MN, int ROWS>
 __device__ __forceinline__ void load_op(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int x_mn,
-                                        int k_or_row) {
-  if (MN) {
+                                        int k_or_row, bool mn3d) {
+  if (MN && mn3d) {
+    tc::tma_load_3d(dst, m, bar, 0, k_or_row, x_mn / 64);   // ROWS/64 chunks in one copy
+  } else if (MN) {
 #pragma unroll
     for (int c = 0; c < ROWS / 64; ++c) tc::tma_load_2d(dst + c * 8192, m, bar, x_mn + 64 * c, k_or_row);
   } else {
@@ -247,25 +250,25 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint8_t* sa = base + st * STAGE;
           uint8_t* sb = sa + OPA;
           if (KIND == kDH) {
-            load_op<true, BM>(sa, sh ? &m1 : &m0, bar, b.m0, e * g.d + ks * BK);
-            load_op<false, BN>(sb, &m4, bar, b.a_row0, ks * BK);
+            load_op<true, BM>(sa, sh ? &m1 : &m0, bar, b.m0, e * g.d + ks * BK, g.mn3d != 0);
+            load_op<false, BN>(sb, &m4, bar, b.a_row0, ks * BK, g.mn3d != 0);
           } else if (KIND == kDX) {
             const int nkI = b.nk / 2, ph = ks >= nkI, kk = ks - ph * nkI;
             const CUtensorMap* ma = ph ? (sh ? &m3 : &m1) : (sh ? &m2 : &m0);
-            load_op<true, BM>(sa, ma, bar, b.m0, e * g.I + kk * BK);
-            load_op<false, BN>(sb, ph ? &m5 : &m4, bar, b.a_row0, kk * BK);
+            load_op<true, BM>(sa, ma, bar, b.m0, e * g.I + kk * BK, g.mn3d != 0);
+            load_op<false, BN>(sb, ph ? &m5 : &m4, bar, b.a_row0, kk * BK, g.mn3d != 0);
           } else if (KIND == kDWD) {
-            load_op<true, BM>(sa, &m0, bar, b.m0, b.a_row0 + ks * BK);
-            load_op<true, BN>(sb, &m4, bar, b.n0, b.b_row0 + ks * BK);
+            load_op<true, BM>(sa, &m0, bar, b.m0, b.a_row0 + ks * BK, g.mn3d != 0);
+            load_op<true, BN>(sb, &m4, bar, b.n0, b.b_row0 + ks * BK, g.mn3d != 0);
           } else if (KIND == kDWGU) {
-            load_op<true, BM>(sa, b.part ? &m1 : &m0, bar, b.m0, b.a_row0 + ks * BK);
-            load_op<true, BN>(sb, sh ? &m5 : &m4, bar, b.n0, b.b_row0 + ks * BK);
+            load_op<true, BM>(sa, b.part ? &m1 : &m0, bar, b.m0, b.a_row0 + ks * BK, g.mn3d != 0);
+            load_op<true, BN>(sb, sh ? &m5 : &m4, bar, b.n0, b.b_row0 + ks * BK, g.mn3d != 0);
           } else if (KIND == kDUR) {
-            load_op<false, BM>(sa, &m0, bar, b.m0, ks * BK);
-            load_op<true, BN>(sb, &m4, bar, b.n0, ks * BK);
+            load_op<false, BM>(sa, &m0, bar, b.m0, ks * BK, g.mn3d != 0);
+            load_op<true, BN>(sb, &m4, bar, b.n0, ks * BK, g.mn3d != 0);
           } else {
-            load_op<true, BM>(sa, &m0, bar, b.m0, ks * BK);
-            load_op<true, BN>(sb, &m4, bar, b.n0, ks * BK);
+            load_op<true, BM>(sa, &m0, bar, b.m0, ks * BK, g.mn3d != 0);
+            load_op<true, BN>(sb, &m4, bar, b.n0, ks * BK, g.mn3d != 0);
           }
         }
       }
@@ -523,6 +526,17 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
   const long long tok_tiles =
       (long long)s.T * s.K_r / BN + s.N_r + (long long)s.N_s * ((s.T + BN - 1) / BN);
   CUtensorMap m[6];
+  // MN-major operands: one 3-D box of 2 (A, slots 0-3) or 4 (B, slots 4-5) 64-element
+  // chunks per K step when every MN extent (d, I, N_r) is a multiple of 64, else 2-D
+  // boxes of one chunk each
+  if (s.d % 64 == 0 && s.I % 64 == 0 && s.N_r % 64 == 0) {
+    CUtensorMap probe;
+    g.mn3d = make_tmap_mn3d(&probe, kBF16, io.u, s.d, s.T, (uint64_t)s.d * 2, 64, BN / 64) ? 1 : 0;
+  }
+  auto mn = [&](int slot, const void* p, uint64_t inner, uint64_t rows) {
+    return g.mn3d ? make_tmap_mn3d(&m[slot], kBF16, p, inner, rows, inner * 2, 64, slot < 4 ? BM / 64 : BN / 64)
+                  : map_mn(&m[slot], p, inner, rows);
+  };
   auto same = [&](int from) {       // unused map slots: copies of a valid map
     for (int i = from; i < 6; ++i)
       if (i != 4) m[i] = m[0];
@@ -531,7 +545,7 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
 
   if (io.experts) {
     // dH = dY W_down, then the SwiGLU backward -> dA, dC
-    if (!map_mn(&m[0], io.w_down, s.I, (uint64_t)s.N_r * s.d) || !map_mn(&m[1], wsd, s.I, Es * s.d) ||
+    if (!mn(0, io.w_down, s.I, (uint64_t)s.N_r * s.d) || !mn(1, wsd, s.I, Es * s.d) ||
         !map_k(&m[4], io.dY, s.d, R, BN))
       return cudaErrorInvalidValue;
     same(2);
@@ -540,16 +554,16 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
     if ((err = launch_kind<kDH>(m, g, tok_tiles * ((s.I + BM - 1) / BM), st)) != cudaSuccess) return err;
 
     // dX = dA W_gate + dC W_up
-    if (!map_mn(&m[0], io.w_gate, s.d, (uint64_t)s.N_r * s.I) ||
-        !map_mn(&m[1], io.w_up, s.d, (uint64_t)s.N_r * s.I) || !map_mn(&m[2], wsg, s.d, Es * s.I) ||
-        !map_mn(&m[3], wsu, s.d, Es * s.I) || !map_k(&m[4], io.dA, s.I, R, BN) || !map_k(&m[5], io.dC, s.I, R, BN))
+    if (!mn(0, io.w_gate, s.d, (uint64_t)s.N_r * s.I) ||
+        !mn(1, io.w_up, s.d, (uint64_t)s.N_r * s.I) || !mn(2, wsg, s.d, Es * s.I) ||
+        !mn(3, wsu, s.d, Es * s.I) || !map_k(&m[4], io.dA, s.I, R, BN) || !map_k(&m[5], io.dC, s.I, R, BN))
       return cudaErrorInvalidValue;
     g.o_bf0 = io.dX;
     g.o_bf1 = nullptr;
     if ((err = launch_kind<kDX>(m, g, tok_tiles * ((s.d + BM - 1) / BM), st)) != cudaSuccess) return err;
 
     // dW_down[e] = dY^T h over the expert's rows
-    if (!map_mn(&m[0], io.dY, s.d, R) || !map_mn(&m[4], io.h, s.I, R)) return cudaErrorInvalidValue;
+    if (!mn(0, io.dY, s.d, R) || !mn(4, io.h, s.I, R)) return cudaErrorInvalidValue;
     same(1);
     g.o_f0 = io.dw_down;
     g.o_fs0 = io.dws_down;
@@ -558,8 +572,8 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
       return err;
 
     // dW_gate[e] = dA^T x, dW_up[e] = dC^T x (x: x_perm rows, or u for the shared experts)
-    if (!map_mn(&m[0], io.dA, s.I, R) || !map_mn(&m[1], io.dC, s.I, R) ||
-        !map_mn(&m[4], io.x_perm, s.d, (uint64_t)s.T * s.K_r) || !map_mn(&m[5], io.u, s.d, s.T))
+    if (!mn(0, io.dA, s.I, R) || !mn(1, io.dC, s.I, R) ||
+        !mn(4, io.x_perm, s.d, (uint64_t)s.T * s.K_r) || !mn(5, io.u, s.d, s.T))
       return cudaErrorInvalidValue;
     m[2] = m[3] = m[0];
     g.o_f0 = io.dw_gate;
@@ -573,14 +587,14 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
   if (!io.router) return cudaSuccess;
 
   // router: du = dz e, de = dz^T u
-  if (!map_k(&m[0], io.dz, s.N_r, s.T, BM) || !map_mn(&m[4], io.e, s.d, s.N_r)) return cudaErrorInvalidValue;
+  if (!map_k(&m[0], io.dz, s.N_r, s.T, BM) || !mn(4, io.e, s.d, s.N_r)) return cudaErrorInvalidValue;
   same(1);
   g.o_f0 = io.du_router;
   g.o_f1 = g.o_fs0 = g.o_fs1 = nullptr;
   if ((err = launch_kind<kDUR>(m, g, (long long)((s.T + BM - 1) / BM) * ((s.d + BN - 1) / BN), st)) !=
       cudaSuccess)
     return err;
-  if (!map_mn(&m[0], io.dz, s.N_r, s.T) || !map_mn(&m[4], io.u, s.d, s.T)) return cudaErrorInvalidValue;
+  if (!mn(0, io.dz, s.N_r, s.T) || !mn(4, io.u, s.d, s.T)) return cudaErrorInvalidValue;
   same(1);
   g.o_f0 = io.de;
   return launch_kind<kDE>(m, g, (long long)((s.N_r + BM - 1) / BM) * ((s.d + BN - 1) / BN), st);

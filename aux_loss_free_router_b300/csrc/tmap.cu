@@ -43,6 +43,19 @@ bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_mn3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t mn,
+                    uint64_t rows, uint64_t row_bytes, uint32_t box_rows, uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || mn % 64 != 0) return false;
+  const cuuint64_t dims[3] = {64, rows, mn / 64};
+  const cuuint64_t strides[2] = {row_bytes, 128};
+  const cuuint32_t box[3] = {64, box_rows, box_chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;

@@ -14,4 +14,12 @@ namespace moe {
 bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 
+// The same row-major 2-byte-element tensor [rows, mn] seen as [mn/64 chunks][rows][64]:
+// one box of box_chunks x box_rows x 64 lands in shared memory as box_chunks 128-byte
+// swizzled [box_rows][64] blocks one after another, the MN-major operand layout of an
+// MMA, in one copy instead of box_chunks.  mn must be a multiple of 64; false if not,
+// or if the driver rejects the map.
+bool make_tmap_mn3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t mn,
+                    uint64_t rows, uint64_t row_bytes, uint32_t box_rows, uint32_t box_chunks);
+
 }  // namespace moe
