@@ -42,7 +42,7 @@ constexpr int OPA = BM * BK * 2;           // A of a K step: 16 KB
 constexpr int OPB = BN * BK * 2;           // B of a K step: 32 KB
 constexpr int STAGE = OPA + OPB;
 constexpr int TMEM_COLS = 512, ACC = 256;
-constexpr int SCR = 16 * 32 * 4;           // per epilogue warp: 16 columns x 32 rows fp32
+constexpr int SCR = 32 * 32 * 4;           // per epilogue warp: 32 x 32 fp32 (the store box)
 
 enum : int { kDH = 0, kDX = 1, kDWD = 2, kDWGU = 3, kDUR = 4, kDE = 5 };
 
@@ -194,6 +194,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     bwd_gemm_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
                     const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
                     const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5,
+                    const __grid_constant__ CUtensorMap o0, const __grid_constant__ CUtensorMap o1,
+                    const __grid_constant__ CUtensorMap o2, const __grid_constant__ CUtensorMap o3,
                     BwdArgs g) {
   using Tr = Traits<KIND>;
   extern __shared__ uint8_t smem_raw[];
@@ -416,41 +418,40 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
         }
       } else {
-        // lane = output row m0 + 32q + lane, column = n0 + c: fp32 rows
-        int Mx, Nx;
-        float* out;
+        // lane = output row m0 + 32q + lane, column = n0 + c: fp32 rows, 32 x 32 blocks
+        // written to the warp's scratch as one 128-byte-swizzled box and stored by TMA
+        // (o0/o1: routed / shared outputs; kDWGU o2/o3 for dW_up; kDUR, kDE: o0)
+        const CUtensorMap* om = &o0;
+        int z = 0;
         if (KIND == kDWD || KIND == kDWGU) {
           const bool sh = b.seg >= g.N_r;
-          const int e = sh ? b.seg - g.N_r : b.seg;
-          Mx = KIND == kDWD ? g.d : g.I;
-          Nx = KIND == kDWD ? g.I : g.d;
-          float* o0 = KIND == kDWGU && b.part ? (sh ? g.o_fs1 : g.o_f1) : (sh ? g.o_fs0 : g.o_f0);
-          out = o0 + (size_t)e * Mx * Nx;
-        } else {
-          Mx = KIND == kDUR ? g.T : g.N_r;
-          Nx = g.d;
-          out = g.o_f0;
+          z = sh ? b.seg - g.N_r : b.seg;
+          om = KIND == kDWGU && b.part ? (sh ? &o3 : &o2) : (sh ? &o1 : &o0);
         }
-        // each lane writes its row's 32 columns per TMEM load as eight 16-byte pieces
-        // (staging through shared memory for 128-byte row stores measured slower: the
-        // extra shared-memory traffic competes with the MMAs' operand reads)
-        const int row = b.m0 + q * 32 + lane;
+        const int Nx = (KIND == kDWD) ? g.I : g.d;
+        const int Mx = KIND == kDWD ? g.d : KIND == kDWGU ? g.I : KIND == kDUR ? g.T : g.N_r;
+        const int y0 = b.m0 + q * 32;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
+          if (b.n0 + c0 >= Nx) break;
           uint32_t r[32];
           tc::tmem_ld32(t_base + c0, r);
           tc::tmem_ld_wait();
-          if (row < Mx) {
-            float* dst = out + (size_t)row * Nx + b.n0 + c0;
+          if (lane == 0) tc::bulk_wait_read();   // the previous box has left the scratch
+          __syncwarp();
+          uint8_t* rowp = reinterpret_cast<uint8_t*>(scr) + lane * 128;
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              if (b.n0 + c0 + 4 * v + 4 <= Nx) {
-                float4 val = b.nk > 0 ? make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]))
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4*>(dst + 4 * v) = val;
-              }
-            }
+          for (int v = 0; v < 8; ++v) {
+            const float4 val = b.nk > 0 ? make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(rowp + ((v ^ (lane & 7)) << 4)) = val;   // 128-byte swizzle
+          }
+          tc::fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0 && y0 < Mx) {   // rows past Mx (and columns past Nx) are clipped
+            tc::tma_store_3d(om, scr, b.n0 + c0, y0, z);
+            tc::bulk_commit();
           }
         }
       }
@@ -460,6 +461,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
+  if (warp >= 2 && lane == 0) tc::bulk_wait_all();   // this warp's output stores are done
   tc::fence_before_sync();
   __syncthreads();
   if (*abort_flag && warp == 0 && lane == 0) {
@@ -479,6 +481,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 constexpr CUtensorMapDataType kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
+// fp32 output [E][rows][cols] seen by TMA stores of 32 x 32 boxes (rows past `rows` and
+// columns past `cols` are clipped).
+bool out_map(CUtensorMap* m, const float* p, uint64_t cols, uint64_t rows, uint64_t E) {
+  return make_tmap_3d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p, cols, rows, E, cols * 4, rows * cols * 4, 32, 32);
+}
+
 // MN-major map: inner = the M/N extent (contiguous), outer = K rows; box 64 x 64.
 bool map_mn(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows) {
   return make_tmap_2d(m, kBF16, p, inner, rows, inner * 2, 64, 64);
@@ -489,7 +497,8 @@ bool map_k(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows, uint32_
 }
 
 template <int KIND>
-cudaError_t launch_kind(const CUtensorMap* m, const BwdArgs& g, long long tiles_ub, cudaStream_t st) {
+cudaError_t launch_kind(const CUtensorMap* m, const CUtensorMap* o, const BwdArgs& g, long long tiles_ub,
+                        cudaStream_t st) {
   static std::mutex mu;
   static bool attr_set[64] = {};
   auto k = bwd_gemm_kernel<KIND>;
@@ -506,7 +515,7 @@ cudaError_t launch_kind(const CUtensorMap* m, const BwdArgs& g, long long tiles_
     }
   }
   const int grid = (int)std::max<long long>(1, std::min<long long>(device_sm_count(), tiles_ub));
-  k<<<grid, THREADS, kSmemBytes, st>>>(m[0], m[1], m[2], m[3], m[4], m[5], g);
+  k<<<grid, THREADS, kSmemBytes, st>>>(m[0], m[1], m[2], m[3], m[4], m[5], o[0], o[1], o[2], o[3], g);
   return cudaGetLastError();
 }
 
@@ -551,7 +560,8 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
     same(2);
     g.o_bf0 = io.dA;
     g.o_bf1 = io.dC;
-    if ((err = launch_kind<kDH>(m, g, tok_tiles * ((s.I + BM - 1) / BM), st)) != cudaSuccess) return err;
+    const CUtensorMap od[4] = {m[0], m[0], m[0], m[0]};
+    if ((err = launch_kind<kDH>(m, od, g, tok_tiles * ((s.I + BM - 1) / BM), st)) != cudaSuccess) return err;
 
     // dX = dA W_gate + dC W_up
     if (!mn(0, io.w_gate, s.d, (uint64_t)s.N_r * s.I) ||
@@ -560,14 +570,20 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
       return cudaErrorInvalidValue;
     g.o_bf0 = io.dX;
     g.o_bf1 = nullptr;
-    if ((err = launch_kind<kDX>(m, g, tok_tiles * ((s.d + BM - 1) / BM), st)) != cudaSuccess) return err;
+    const CUtensorMap ox[4] = {m[0], m[0], m[0], m[0]};
+    if ((err = launch_kind<kDX>(m, ox, g, tok_tiles * ((s.d + BM - 1) / BM), st)) != cudaSuccess) return err;
 
     // dW_down[e] = dY^T h over the expert's rows
     if (!mn(0, io.dY, s.d, R) || !mn(4, io.h, s.I, R)) return cudaErrorInvalidValue;
     same(1);
     g.o_f0 = io.dw_down;
     g.o_fs0 = io.dws_down;
-    if ((err = launch_kind<kDWD>(m, g, (long long)segs * ((s.d + BM - 1) / BM) * ((s.I + BN - 1) / BN),
+    CUtensorMap ow[4];
+    if (!out_map(&ow[0], io.dw_down, s.I, s.d, s.N_r) || !out_map(&ow[1], s.N_s ? io.dws_down : io.dw_down, s.I, s.d,
+                                                                   s.N_s ? s.N_s : s.N_r))
+      return cudaErrorInvalidValue;
+    ow[2] = ow[3] = ow[0];
+    if ((err = launch_kind<kDWD>(m, ow, g, (long long)segs * ((s.d + BM - 1) / BM) * ((s.I + BN - 1) / BN),
                                  st)) != cudaSuccess)
       return err;
 
@@ -580,7 +596,12 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
     g.o_f1 = io.dw_up;
     g.o_fs0 = io.dws_gate;
     g.o_fs1 = io.dws_up;
-    if ((err = launch_kind<kDWGU>(m, g, 2LL * segs * ((s.I + BM - 1) / BM) * ((s.d + BN - 1) / BN),
+    CUtensorMap og[4];
+    const int Es2 = s.N_s ? s.N_s : s.N_r;
+    if (!out_map(&og[0], io.dw_gate, s.d, s.I, s.N_r) || !out_map(&og[1], s.N_s ? io.dws_gate : io.dw_gate, s.d, s.I, Es2) ||
+        !out_map(&og[2], io.dw_up, s.d, s.I, s.N_r) || !out_map(&og[3], s.N_s ? io.dws_up : io.dw_up, s.d, s.I, Es2))
+      return cudaErrorInvalidValue;
+    if ((err = launch_kind<kDWGU>(m, og, g, 2LL * segs * ((s.I + BM - 1) / BM) * ((s.d + BN - 1) / BN),
                                   st)) != cudaSuccess)
       return err;
   }
@@ -591,13 +612,19 @@ cudaError_t launch_bwd_gemms(const BwdGemmIo& io, cudaStream_t st) {
   same(1);
   g.o_f0 = io.du_router;
   g.o_f1 = g.o_fs0 = g.o_fs1 = nullptr;
-  if ((err = launch_kind<kDUR>(m, g, (long long)((s.T + BM - 1) / BM) * ((s.d + BN - 1) / BN), st)) !=
+  CUtensorMap ou[4];
+  if (!out_map(&ou[0], io.du_router, s.d, s.T, 1)) return cudaErrorInvalidValue;
+  ou[1] = ou[2] = ou[3] = ou[0];
+  if ((err = launch_kind<kDUR>(m, ou, g, (long long)((s.T + BM - 1) / BM) * ((s.d + BN - 1) / BN), st)) !=
       cudaSuccess)
     return err;
   if (!mn(0, io.dz, s.N_r, s.T) || !mn(4, io.u, s.d, s.T)) return cudaErrorInvalidValue;
   same(1);
   g.o_f0 = io.de;
-  return launch_kind<kDE>(m, g, (long long)((s.N_r + BM - 1) / BM) * ((s.d + BN - 1) / BN), st);
+  CUtensorMap oe[4];
+  if (!out_map(&oe[0], io.de, s.d, s.N_r, 1)) return cudaErrorInvalidValue;
+  oe[1] = oe[2] = oe[3] = oe[0];
+  return launch_kind<kDE>(m, oe, g, (long long)((s.N_r + BM - 1) / BM) * ((s.d + BN - 1) / BN), st);
 }
 
 }  // namespace moe

@@ -19,6 +19,11 @@ bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, ui
 // swizzled [box_rows][64] blocks one after another, the MN-major operand layout of an
 // MMA, in one copy instead of box_chunks.  mn must be a multiple of 64; false if not,
 // or if the driver rejects the map.
+// 3-D tensor [d2][d1][d0] (strides in bytes for dims 1 and 2), box [1][box1][box0] with
+// 128-byte swizzling (box0 * element size must be 128).
+bool make_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1,
+                  uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1);
+
 bool make_tmap_mn3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t mn,
                     uint64_t rows, uint64_t row_bytes, uint32_t box_rows, uint32_t box_chunks);
 
