@@ -275,13 +275,14 @@ __global__ void __launch_bounds__(256) fp8_colquant_kernel(ColQuantSrc src, cons
 //               kind::f8f6f4 MMAs of K = 32 into one of two 256-column TMEM buffers;
 //   warps 2..17 promote each block into fp32 registers: acc += P * (sa[row] * sb[col]),
 //               four warps per TMEM lane quarter, 64 columns each, and store the tile.
+//               Output: 32 x 32 fp32 boxes written to per-warp scratch, stored by TMA.
 //               A block's 256 column scales sit in a shared-memory double buffer: the
 //               epilogue loads the next block's while it promotes this one (an mbarrier
 //               per buffer says all 512 epilogue threads have stored theirs).
 constexpr int WG_BM = 128, WG_BK = 128, WG_BN = 256, WG_STAGES = 3;
 constexpr int WG_A = WG_BM * WG_BK, WG_B = WG_BN * WG_BK, WG_STAGE = WG_A + WG_B;
 constexpr int WG_EPI_WARPS = 16, WG_THREADS = 64 + WG_EPI_WARPS * 32;
-constexpr int WG_SCR = 32 * 33 * 4;   // per epilogue warp: 32 rows x 32 columns (+1 pad), fp32
+constexpr int WG_SCR = 32 * 32 * 4;   // per epilogue warp: a 32 x 32 fp32 store box
 
 struct WgCtrl {
   uint64_t full[WG_STAGES], empty[WG_STAGES], pfull[2], pempty[2], sfill[2], fin;
@@ -306,7 +307,8 @@ struct WgArgs {
 };
 
 __global__ void __launch_bounds__(WG_THREADS, 1)
-    fp8_wgrad_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB, WgArgs g) {
+    fp8_wgrad_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
+                     const __grid_constant__ CUtensorMap mO, const __grid_constant__ CUtensorMap mOs, WgArgs g) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_off = tc::smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_off & 1023u)) & 1023u);
@@ -471,24 +473,32 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
       }
       if (!alive) break;
       if (cols_ok) {
-        // 32 rows x 64 columns through the warp's scratch, 32 columns at a time, so that
-        // each store writes 128 contiguous bytes of one row
-        float* out = seg < g.N_r ? g.out + (size_t)seg * g.M * g.N : g.out_s + (size_t)(seg - g.N_r) * g.M * g.N;
-        float* scr = scr_all + (warp - 2) * (WG_SCR / 4);
-        float* dst = out + (size_t)(row - lane) * g.N + col0 + lane;
+        // 32 rows x 64 columns as two 32 x 32 boxes: written to the warp's scratch with
+        // the 128-byte swizzle, stored by TMA (mO routed experts, mOs shared ones)
+        const CUtensorMap* om = seg < g.N_r ? &mO : &mOs;
+        const int z = seg < g.N_r ? seg : seg - g.N_r;
+        uint8_t* scr = reinterpret_cast<uint8_t*>(scr_all) + (warp - 2) * WG_SCR;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          if (lane == 0) tc::bulk_wait_read();   // the previous box has left the scratch
+          __syncwarp();
+          uint8_t* rowp = scr + lane * 128;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) scr[lane * 33 + j] = acc[32 * h + j];
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(rowp + ((v ^ (lane & 7)) << 4)) =
+                make_float4(acc[32 * h + 4 * v], acc[32 * h + 4 * v + 1], acc[32 * h + 4 * v + 2], acc[32 * h + 4 * v + 3]);
+          tc::fence_proxy_async_shared();
           __syncwarp();
-#pragma unroll 8
-          for (int r = 0; r < 32; ++r) dst[(size_t)r * g.N + 32 * h] = scr[r * 33 + lane];
-          __syncwarp();
+          if (lane == 0) {
+            tc::tma_store_3d(om, scr, col0 + 32 * h, row - lane, z);
+            tc::bulk_commit();
+          }
         }
       }
     }
   }
 
+  if (warp >= 2 && lane == 0) tc::bulk_wait_all();   // this warp's output stores are done
   tc::fence_before_sync();
   __syncthreads();
   if (*abort_flag && warp == 0 && lane == 0) {
@@ -539,10 +549,18 @@ cudaError_t launch_fp8_colquant(const ColQuantSrc& src, const int32_t* expert_of
 cudaError_t launch_fp8_wgrad(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                              int M, int N, long long Rp, const int32_t* expert_offset, int T, int K_r,
                              int N_r, int N_s, float* out, float* out_s, cudaStream_t st) {
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mO, mOs;
+  const CUtensorMapDataType kF32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   if (!make_tmap_2d(&mA, kU8, qa, (uint64_t)Rp, (uint64_t)M, (uint64_t)Rp, WG_BK, WG_BM) ||
-      !make_tmap_2d(&mB, kU8, qb, (uint64_t)Rp, (uint64_t)N, (uint64_t)Rp, WG_BK, WG_BN))
+      !make_tmap_2d(&mB, kU8, qb, (uint64_t)Rp, (uint64_t)N, (uint64_t)Rp, WG_BK, WG_BN) ||
+      !make_tmap_3d(&mO, kF32, out, N, M, N_r, (uint64_t)N * 4, (uint64_t)M * N * 4, 32, 32))
     return cudaErrorInvalidValue;
+  if (N_s > 0) {
+    if (!make_tmap_3d(&mOs, kF32, out_s, N, M, N_s, (uint64_t)N * 4, (uint64_t)M * N * 4, 32, 32))
+      return cudaErrorInvalidValue;
+  } else {
+    mOs = mO;   // never used
+  }
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -556,7 +574,7 @@ cudaError_t launch_fp8_wgrad(const uint8_t* qa, const float* sa, const uint8_t* 
   const long long tiles = (long long)(N_r + N_s) * (M / WG_BM) * ((N + WG_BN - 1) / WG_BN);
   const int grid = (int)std::max<long long>(1, std::min<long long>(device_sm_count(), tiles));
   WgArgs g{sa, sb, M, N, T, K_r, N_r, N_s, expert_offset, out, out_s, dev_error_ptr()};
-  fp8_wgrad_kernel<<<grid, WG_THREADS, kWgSmem, st>>>(mA, mB, g);
+  fp8_wgrad_kernel<<<grid, WG_THREADS, kWgSmem, st>>>(mA, mB, mO, mOs, g);
   return cudaGetLastError();
 }
 
