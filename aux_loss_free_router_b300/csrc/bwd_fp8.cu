@@ -458,7 +458,9 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
           tc::tmem_ld_wait();
           const float sb[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[g0 + j] = fmaf(__uint_as_float(pv[j]), sa * sb[j], acc[g0 + j]);
+          for (int j = 0; j < 8; j += 2)
+            tc::fma2_scaled(acc[g0 + j], acc[g0 + j + 1], __uint_as_float(pv[j]), __uint_as_float(pv[j + 1]), sa,
+                            sb[j], sb[j + 1]);
         }
         tc::fence_before_sync();
         tc::mbar_arrive(&C.pempty[buf]);

@@ -271,12 +271,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc::tmem_ld8(t_base + col, *reinterpret_cast<uint32_t(*)[8]>(&pv[x]));
           }
           tc::tmem_ld_wait();
+          // the group's 8 columns share one scale (the gate / up boundary is at 32)
+          const float sc = sa * (MODE == 0 && g0 >= 32 ? sb1 : sb0);
 #pragma unroll
-          for (int j = 0; j < kLoadGroup; ++j) {
-            const int c = g0 + j;
-            const float sc = sa * (MODE == 0 && c >= 32 ? sb1 : sb0);
-            acc[c] = fmaf(__uint_as_float(pv[j]), sc, acc[c]);
-          }
+          for (int j = 0; j < kLoadGroup; j += 2)
+            tc::fma2(acc[g0 + j], acc[g0 + j + 1], __uint_as_float(pv[j]), __uint_as_float(pv[j + 1]), sc);
         }
         tc::fence_before_sync();
         tc::mbar_arrive(&C.pempty[buf]);
