@@ -99,22 +99,20 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
                : "memory");
 }
-// Paired fp32 arithmetic (one f32x2 instruction for two lanes of values; each half is
-// the IEEE result of the scalar operation): a += p * s for (a0, a1) and (p0, p1) with
-// one scale s, and with scales sa * (sb0, sb1).
+// Paired fp32 arithmetic (one f32x2 instruction for two values; each half is the IEEE
+// result of the scalar operation): a += p * s for (a0, a1) and (p0, p1) with one scale s,
+// and with scales sa * (sb0, sb1).
 __device__ __forceinline__ void fma2(float& a0, float& a1, float p0, float p1, float s) {
-  asm("{\n\t.reg .b64 ra, rp, rs;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rp, {%2, %3};\n\t"
-      "mov.b64 rs, {%4, %4};\n\tfma.rn.f32x2 ra, rp, rs, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(p0), "f"(p1), "f"(s));
+  const float2 r = __ffma2_rn(make_float2(p0, p1), make_float2(s, s), make_float2(a0, a1));
+  a0 = r.x;
+  a1 = r.y;
 }
 __device__ __forceinline__ void fma2_scaled(float& a0, float& a1, float p0, float p1, float sa, float sb0,
                                             float sb1) {
-  asm("{\n\t.reg .b64 ra, rp, ra2, rb2;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rp, {%2, %3};\n\t"
-      "mov.b64 ra2, {%4, %4};\n\tmov.b64 rb2, {%5, %6};\n\tmul.rn.f32x2 rb2, ra2, rb2;\n\t"
-      "fma.rn.f32x2 ra, rp, rb2, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(p0), "f"(p1), "f"(sa), "f"(sb0), "f"(sb1));
+  const float2 sc = __fmul2_rn(make_float2(sa, sa), make_float2(sb0, sb1));
+  const float2 r = __ffma2_rn(make_float2(p0, p1), sc, make_float2(a0, a1));
+  a0 = r.x;
+  a1 = r.y;
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
