@@ -74,7 +74,7 @@ struct Fp8Args {
   __nv_bfloat16* save_c = nullptr;
 };
 
-__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 __device__ __forceinline__ uint32_t e4m3_code(float x, float scale) {
   return (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
