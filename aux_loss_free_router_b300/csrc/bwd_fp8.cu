@@ -103,8 +103,8 @@ __global__ void __launch_bounds__(256) fp8_swiglu_bwd_kernel(
   float amax_a = 0.f, amax_c = 0.f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float sg = 1.f / (1.f + expf(-va[k]));
-    const float silu = va[k] / (1.f + expf(-va[k]));
+    const float sg = __fdividef(1.f, 1.f + __expf(-va[k]));
+    const float silu = va[k] * sg;
     const float dsilu = sg * (1.f + va[k] * (1.f - sg));
     ga[k] = vh[k] * vc[k] * dsilu;
     gc[k] = vh[k] * silu;

@@ -179,7 +179,7 @@ __device__ __forceinline__ void load_op(uint8_t* dst, const CUtensorMap* m, uint
   }
 }
 
-__device__ __forceinline__ float sigm(float x) { return __frcp_rn(1.f + __expf(-x)); }
+__device__ __forceinline__ float sigm(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 // m0..m5 per kind:
 //   kDH:   m0 W_down routed  [N_r*d, I] MN   m1 W_down shared  m4 dY [R, d] K
