@@ -30,8 +30,8 @@ namespace moe {
 
 namespace {
 
-__device__ __forceinline__ uint32_t e4m3_code(float x, float scale) {
-  return (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+__device__ __forceinline__ uint32_t e4m3_code(float x, float scale, float inv) {
+  return (uint32_t)__nv_cvt_float_to_fp8(div_by_scale(x, scale, inv), __NV_SATFINITE, __NV_E4M3);
 }
 
 __device__ __forceinline__ float e4m3_value(uint32_t code) {
@@ -117,11 +117,12 @@ __global__ void __launch_bounds__(256) fp8_swiglu_bwd_kernel(
     amax_c = fmaxf(amax_c, __shfl_xor_sync(0xffffffffu, amax_c, s));
   }
   const float sa = tile_scale(amax_a), sc = tile_scale(amax_c);
+  const float ia = __frcp_rn(sa), ic = __frcp_rn(sc);
   uint32_t qa = 0, qc = 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    qa |= e4m3_code(ga[k], sa) << (8 * k);
-    qc |= e4m3_code(gc[k], sc) << (8 * k);
+    qa |= e4m3_code(ga[k], sa, ia) << (8 * k);
+    qc |= e4m3_code(gc[k], sc, ic) << (8 * k);
   }
   uint8_t* qrow = ac_q + (size_t)r * 2 * I;
   *reinterpret_cast<uint32_t*>(qrow + t * 128 + lane * 4) = qa;
@@ -253,12 +254,13 @@ __global__ void __launch_bounds__(256) fp8_colquant_kernel(ColQuantSrc src, cons
   red[part][col] = amax;
   __syncthreads();
   const float s = tile_scale(fmaxf(fmaxf(red[0][col], red[1][col]), fmaxf(red[2][col], red[3][col])));
+  const float inv = __frcp_rn(s);
   uint32_t w[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     w[k] = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) w[k] |= e4m3_code(tile[part * 32 + 4 * k + j][col], s) << (8 * j);
+    for (int j = 0; j < 4; ++j) w[k] |= e4m3_code(tile[part * 32 + 4 * k + j][col], s, inv) << (8 * j);
   }
   uint4* dst = reinterpret_cast<uint4*>(q + (size_t)(c0 + col) * Rp + (size_t)b * 128 + part * 32);
   dst[0] = make_uint4(w[0], w[1], w[2], w[3]);

@@ -66,6 +66,20 @@ __device__ __forceinline__ KeyIdxVal warp_argmax(KeyIdxVal a) {
 
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
+// x / scale for E4M3 quantisation from inv = RN(1 / scale), taken once per tile: q =
+// RN(x inv), the remainder r = x - q scale exact by fma, then RN(q + r inv) (Markstein's
+// correction step).  It is meant only for a quotient that is then rounded to E4M3: over
+// 4e9 operand pairs of the quantisers' shape (|x| <= amax, scale = amax / 448, amax from
+// 2^-63 to 2^64) the E4M3 codes of this quotient and of the IEEE one (__fdiv_rn) were
+// identical (the fp32 quotients themselves can differ where x/scale is far below the
+// smallest E4M3 step), and the quantiser tests compare the codes with the oracle's fp32
+// division.
+__device__ __forceinline__ float div_by_scale(float x, float scale, float inv) {
+  const float q = __fmul_rn(x, inv);
+  const float r = __fmaf_rn(-q, scale, x);
+  return __fmaf_rn(r, inv, q);
+}
+
 // Programmatic dependent launch.  The forward kernels are launched with launch_pdl, so
 // the GPU may schedule a kernel while the one before it in the stream still runs.  Each
 // such kernel calls pdl_wait() before its first access to global memory that another

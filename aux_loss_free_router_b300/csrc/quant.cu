@@ -15,8 +15,8 @@ __device__ __forceinline__ float block_scale(float amax) {
   return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
 }
 
-__device__ __forceinline__ uint8_t to_e4m3(float x, float scale) {
-  return (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+__device__ __forceinline__ uint8_t to_e4m3(float x, float scale, float inv) {
+  return (uint8_t)__nv_cvt_float_to_fp8(div_by_scale(x, scale, inv), __NV_SATFINITE, __NV_E4M3);
 }
 
 // One warp per (row, 128-column tile); each lane owns 4 consecutive values.
@@ -43,9 +43,10 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const TIn* __restrict_
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float sc = block_scale(amax);
+  const float inv = __frcp_rn(sc);
   uint32_t packed = 0;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) packed |= (uint32_t)to_e4m3(v[k], sc) << (8 * k);
+  for (int k = 0; k < 4; ++k) packed |= (uint32_t)to_e4m3(v[k], sc, inv) << (8 * k);
   *reinterpret_cast<uint32_t*>(q + r * cols + tc * 128 + lane * 4) = packed;
   if (lane == 0) scale[w] = sc;
 }
@@ -73,10 +74,11 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const TIn* __restric
   float m = 0.f;
   for (int k = 0; k < (int)(blockDim.x >> 5); ++k) m = fmaxf(m, red[k]);
   const float sc = block_scale(m);
+  const float inv = __frcp_rn(sc);
   uint8_t* qb = q + br * 128 * cols + bc * 128;
   for (int e = threadIdx.x; e < 128 * 128; e += blockDim.x) {
     const int r = e >> 7, c = e & 127;
-    qb[(long long)r * cols + c] = to_e4m3(to_f32(base[(long long)r * cols + c]), sc);
+    qb[(long long)r * cols + c] = to_e4m3(to_f32(base[(long long)r * cols + c]), sc, inv);
   }
   if (threadIdx.x == 0) scale[br * gridDim.x + bc] = sc;
 }

@@ -76,8 +76,8 @@ struct Fp8Args {
 
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
-__device__ __forceinline__ uint32_t e4m3_code(float x, float scale) {
-  return (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+__device__ __forceinline__ uint32_t e4m3_code(float x, float scale, float inv) {
+  return (uint32_t)__nv_cvt_float_to_fp8(div_by_scale(x, scale, inv), __NV_SATFINITE, __NV_E4M3);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int x = 0; x < 4; ++x) tile_amax = fmaxf(tile_amax, C.amax[tb][x][row_in_tile]);
         const float scale = tile_amax > 0.f ? __fdiv_rn(tile_amax, 448.f) : 1.f;
+        const float inv = __frcp_rn(scale);
         if (row_ok) {
           uint8_t* hq = static_cast<uint8_t*>(args.out) + out_row * N + tcd.n * 128 + cq * 32;
 #pragma unroll
@@ -323,8 +324,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
               const int j = v * 16 + x * 4;
-              w[x] = e4m3_code(acc[j], scale) | (e4m3_code(acc[j + 1], scale) << 8) |
-                     (e4m3_code(acc[j + 2], scale) << 16) | (e4m3_code(acc[j + 3], scale) << 24);
+              w[x] = e4m3_code(acc[j], scale, inv) | (e4m3_code(acc[j + 1], scale, inv) << 8) |
+                     (e4m3_code(acc[j + 2], scale, inv) << 16) | (e4m3_code(acc[j + 3], scale, inv) << 24);
             }
             reinterpret_cast<uint4*>(hq)[v] = make_uint4(w[0], w[1], w[2], w[3]);
           }

@@ -112,6 +112,26 @@ def test_expert_ffn_call_equals_the_two_step_calls(fp8):
     assert torch.equal(y, lay.y)
 
 
+def test_quantize_wide_magnitudes_bit_exact():
+    """Codes over 4 M values whose tiles span 2^-60 .. 2^60 and whose values sit down to
+    2^-40 below their tile's largest: the library divides by the scale through a
+    reciprocal and one correction step, and must still give the oracle's codes (its
+    fp32 division) everywhere."""
+    g = torch.Generator(device="cuda").manual_seed(21)
+    rows, cols = 4096, 1024
+    x = torch.randn(rows, cols, device="cuda", generator=g)
+    mag = torch.exp2(torch.randint(-60, 60, (rows, cols // 128, 1), device="cuda", generator=g).float())
+    spread = torch.exp2(-torch.randint(0, 40, (rows, cols), device="cuda", generator=g).float())
+    x = (x.view(rows, cols // 128, 128) * mag).view(rows, cols) * spread
+    q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(rows, cols // 128, dtype=torch.float32, device="cuda")
+    moe.quantize_e4m3(x, 1, q, sc)
+    torch.cuda.synchronize()
+    ref_q, ref_sc = ofp8.quantize_1x128(to_np(x))
+    np.testing.assert_array_equal(to_np(sc), ref_sc)
+    np.testing.assert_array_equal(_codes_to_values(q), ref_q)
+
+
 def test_quantize_fp32_input_bit_exact():
     g = torch.Generator(device="cuda").manual_seed(13)
     x = torch.randn(64, 384, device="cuda", generator=g) * 10.0
