@@ -180,7 +180,8 @@ __device__ __forceinline__ void segment_blocks(int* blk, int* seg_rows, const in
 }
 
 // ------------------------------------------------- Wgrad operand quantisation ----
-// One CTA per (128-token block, 64 columns).
+// Work items (128-token block, 64 columns), taken by a grid of CTAs that each build the
+// block table once and then walk items blockIdx.x, blockIdx.x + gridDim.x, ...
 constexpr int CQ_COLS = 64;
 
 __global__ void __launch_bounds__(256) fp8_colquant_kernel(ColQuantSrc src, const int32_t* __restrict__ off,
@@ -194,78 +195,82 @@ __global__ void __launch_bounds__(256) fp8_colquant_kernel(ColQuantSrc src, cons
   const int nseg = N_r + N_s;
   if (threadIdx.x < 32) segment_blocks(blk, seg_rows, off, T, K_r, N_r, N_s, err);
   __syncthreads();
-  const int b = blockIdx.y;
-  if (b >= blk[nseg]) return;
-  int lo = 0, hi = nseg;                       // the segment: last i with blk[i] <= b
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (blk[mid] <= b) lo = mid; else hi = mid;
-  }
-  const int seg = lo;
-  const int r0 = (b - blk[seg]) * 128;
-  const int n_valid = min(128, seg_rows[seg] - r0);
-  const int c0 = blockIdx.x * CQ_COLS;
-  const bool sh = seg >= N_r;
-  const long long src_row0 = sh ? (long long)(seg - N_r) * src.shared_stride + r0 : (long long)off[seg] + r0;
-  const void* base = sh ? src.shared : src.routed;
-  const float* bscale = sh ? src.shared_scale : src.routed_scale;
-  {
-    const int row = threadIdx.x >> 1, half = threadIdx.x & 1;    // 32 columns each
-    float v[32];
-    if (row < n_valid) {
-      const long long gr = src_row0 + row;
-      if (bscale == nullptr) {
-        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) +
-                                                        (size_t)gr * C + c0 + half * 32);
+  const int ncc = C / CQ_COLS;
+  const long long items = (long long)blk[nseg] * ncc;
+  for (long long item = blockIdx.x; item < items; item += gridDim.x) {
+    const int b = (int)(item / ncc);
+    const int c0 = (int)(item - (long long)b * ncc) * CQ_COLS;
+    int lo = 0, hi = nseg;                       // the segment: last i with blk[i] <= b
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (blk[mid] <= b) lo = mid; else hi = mid;
+    }
+    const int seg = lo;
+    const int r0 = (b - blk[seg]) * 128;
+    const int n_valid = min(128, seg_rows[seg] - r0);
+    const bool sh = seg >= N_r;
+    const long long src_row0 = sh ? (long long)(seg - N_r) * src.shared_stride + r0 : (long long)off[seg] + r0;
+    const void* base = sh ? src.shared : src.routed;
+    const float* bscale = sh ? src.shared_scale : src.routed_scale;
+    {
+      const int row = threadIdx.x >> 1, half = threadIdx.x & 1;    // 32 columns each
+      float v[32];
+      if (row < n_valid) {
+        const long long gr = src_row0 + row;
+        if (bscale == nullptr) {
+          const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) +
+                                                          (size_t)gr * C + c0 + half * 32);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 x = p[k];
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+          for (int k = 0; k < 4; ++k) {
+            const uint4 x = p[k];
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            v[8 * k + 2 * j] = __low2float(h[j]);
-            v[8 * k + 2 * j + 1] = __high2float(h[j]);
+            for (int j = 0; j < 4; ++j) {
+              v[8 * k + 2 * j] = __low2float(h[j]);
+              v[8 * k + 2 * j + 1] = __high2float(h[j]);
+            }
+          }
+        } else {
+          const float s = bscale[(size_t)gr * (C / 128) + (c0 >> 7)];
+          const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(base) + (size_t)gr * C +
+                                                          c0 + half * 32);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint4 x = p[k];
+            const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[16 * k + j] = e4m3_value((wv[j >> 2] >> (8 * (j & 3))) & 0xffu) * s;
           }
         }
       } else {
-        const float s = bscale[(size_t)gr * (C / 128) + (c0 >> 7)];
-        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(base) + (size_t)gr * C +
-                                                        c0 + half * 32);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const uint4 x = p[k];
-          const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[16 * k + j] = e4m3_value((wv[j >> 2] >> (8 * (j & 3))) & 0xffu) * s;
-        }
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
       }
-    } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      for (int j = 0; j < 32; ++j) tile[row][half * 32 + j] = v[j];
     }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) tile[row][half * 32 + j] = v[j];
-  }
-  __syncthreads();
-  const int col = threadIdx.x & (CQ_COLS - 1), part = threadIdx.x >> 6;   // 32 rows each
-  float amax = 0.f;
+    __syncthreads();
+    const int col = threadIdx.x & (CQ_COLS - 1), part = threadIdx.x >> 6;   // 32 rows each
+    float amax = 0.f;
 #pragma unroll 8
-  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(tile[part * 32 + j][col]));
-  red[part][col] = amax;
-  __syncthreads();
-  const float s = tile_scale(fmaxf(fmaxf(red[0][col], red[1][col]), fmaxf(red[2][col], red[3][col])));
-  const float inv = __frcp_rn(s);
-  uint32_t w[8];
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(tile[part * 32 + j][col]));
+    red[part][col] = amax;
+    __syncthreads();
+    const float s = tile_scale(fmaxf(fmaxf(red[0][col], red[1][col]), fmaxf(red[2][col], red[3][col])));
+    const float inv = __frcp_rn(s);
+    uint32_t w[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    w[k] = 0;
+    for (int k = 0; k < 8; ++k) {
+      w[k] = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) w[k] |= e4m3_code(tile[part * 32 + 4 * k + j][col], s, inv) << (8 * j);
+      for (int j = 0; j < 4; ++j) w[k] |= e4m3_code(tile[part * 32 + 4 * k + j][col], s, inv) << (8 * j);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(q + (size_t)(c0 + col) * Rp + (size_t)b * 128 + part * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    if (part == 0) scale[(size_t)b * C + c0 + col] = s;
+    __syncthreads();                             // tile and red are free for the next item
   }
-  uint4* dst = reinterpret_cast<uint4*>(q + (size_t)(c0 + col) * Rp + (size_t)b * 128 + part * 32);
-  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  if (part == 0) scale[(size_t)b * C + c0 + col] = s;
 }
 
 // ------------------------------------------------------------------- Wgrad GEMM ----
@@ -543,10 +548,11 @@ cudaError_t launch_fp8_swiglu_bwd(const void* dH, const void* a, const void* c, 
 cudaError_t launch_fp8_colquant(const ColQuantSrc& src, const int32_t* expert_offset, int T, int K_r,
                                 int N_r, int N_s, int C, uint8_t* q, float* scale, long long Rp,
                                 cudaStream_t st) {
-  const long long blocks_ub = Rp / 128;
-  if (blocks_ub == 0) return cudaSuccess;
-  fp8_colquant_kernel<<<dim3(C / CQ_COLS, (unsigned)blocks_ub), 256, 0, st>>>(
-      src, expert_offset, T, K_r, N_r, N_s, C, q, scale, Rp, dev_error_ptr());
+  const long long items_ub = (Rp / 128) * (C / CQ_COLS);
+  if (items_ub == 0) return cudaSuccess;
+  const int grid = (int)std::min<long long>(items_ub, 8LL * device_sm_count());   // about 6 resident per SM
+  fp8_colquant_kernel<<<grid, 256, 0, st>>>(src, expert_offset, T, K_r, N_r, N_s, C, q, scale, Rp,
+                                            dev_error_ptr());
   return cudaGetLastError();
 }
 
