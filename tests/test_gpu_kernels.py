@@ -115,6 +115,30 @@ def test_router_shapes_bit_exact(N_r, K_r, G, M, T, d, n_seq):
                                rtol=1e-5)
 
 
+@pytest.mark.parametrize("T,offsets", [
+    (100, [0, 0, 40, 40, 100]),           # one cluster: empty first and middle sequences
+    (300, [0, 128, 128, 129, 300, 300]),  # several clusters: empty sequences at a boundary and at the end
+])
+def test_router_p_sums_with_empty_sequences(T, offsets):
+    """The fused router's P sums where some sequences hold no token: those rows are zero,
+    the others match the oracle (a batch of <= 128 tokens adds its sums inside one
+    cluster, a larger one through the fixed-point accumulators)."""
+    n_seq = len(offsets) - 1
+    cfg = synth.MoEConfig("route-empty", T=T, d=256, N_r=128, K_r=8, N_s=0, I=128, G=4, M=2,
+                          dtype="bf16", bias="uniform", seed=T, n_seq=1)
+    x = synth.make_inputs(cfg, device="cuda", with_weights=False)
+    x["seq_offsets"] = torch.tensor(offsets, dtype=torch.int32, device="cuda")
+    cfg = cfg.replace(n_seq=n_seq)
+    sh, idx, gate, s, psum = _route(cfg, x)
+    assert moe.device_error() == 0
+    s_np = to_np(s)
+    ref = oracle.seq_p_sums(s_np, np.array(offsets))
+    np.testing.assert_allclose(to_np(psum), ref, rtol=1e-5, atol=1e-6)
+    for j in range(n_seq):
+        if offsets[j + 1] == offsets[j]:
+            assert (to_np(psum)[j] == 0).all()
+
+
 @pytest.mark.parametrize("N_r,K_r,G,M", [(256, 8, 8, 4), (64, 6, 1, 1), (128, 8, 4, 2)])
 def test_router_exact_ties_go_to_lower_index(N_r, K_r, G, M):
     """Zero centroids give s = 0.5 for every expert, and biases repeat in steps of three,
