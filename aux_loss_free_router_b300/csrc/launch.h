@@ -37,8 +37,9 @@ cudaError_t launch_router_select(const float* z_part, int S, const float* b, con
                                  cudaStream_t st);
 // Fused routing (affinity GEMM, sigmoid, keys, group limit, Top-K_r, gates, P sums in
 // one launch) for bf16 layers: 64, 128 or 256 experts, K_r <= 8, groups of whole
-// 32-expert blocks with K_r/M <= 2, d >= 128.  done_ctr: one int of scratch (zeroed on
-// the stream before the kernel when P sums are wanted).
+// 32-expert blocks with K_r/M <= 2, d >= 128.  done_ctr: scratch of 256 bytes (the
+// counter) and then the [n_seq, N_r] fixed-point P accumulators, zeroed on the stream
+// before the kernel when P sums are wanted and the batch is more than one cluster.
 bool router_fused_ok(int N_r, int K_r, int G, int M, int d);
 cudaError_t launch_router_fused(const void* u, const void* e, int d, const float* b,
                                 const RouteOut& p, float* seq_p_sum, int* done_ctr,

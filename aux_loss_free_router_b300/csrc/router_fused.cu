@@ -65,8 +65,8 @@ struct FusedArgs {
   const float* b;
   int d, C;
   int one_cluster;               // the launch is one cluster (T <= 128): P sums over DSMEM
-  int* done_ctr;                 // zeroed before the launch (more than one cluster)
-  unsigned long long* p_acc;     // [n_seq, N_r] fixed-point P sums, zeroed before the launch
+  int* done_ctr;                 // zeroed before a launch of more than one cluster
+  unsigned long long* p_acc;     // [n_seq, N_r] fixed-point P sums, zeroed with done_ctr
   float* seq_p_sum;              // [n_seq, N_r] or null
   int32_t* err;
 };

@@ -317,8 +317,9 @@ def run_ours(args, cfg, ws, rank, local):
     clk = clocks.stop()
     ms = max_over_ranks(ws, t0.elapsed_time(t1) / K)
     stage_names = ["route", "dispatch", "gate_up", "down", "combine_bias_stat"]
-    stages = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
-              for i, n in enumerate(stage_names)}
+    stage_ms = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)]
+                for i, n in enumerate(stage_names)}
+    stages = {n: statistics.mean(v) for n, v in stage_ms.items()}
     if moe.device_error() != 0:
         raise RuntimeError("device error word set during the timed steps")
     del graph
@@ -386,6 +387,8 @@ def run_ours(args, cfg, ws, rank, local):
         "combine_bias_stat": {"ms": stages["combine_bias_stat"],
                               "GB/s": wk["combine_bytes"] / (stages["combine_bias_stat"] / 1e3) / 1e9},
     }
+    for n, v in stage_ms.items():      # the per-stage median over the K timed steps
+        kernels[n]["ms_median"] = statistics.median(v)
     wq = 1 if cfg.fp8 else 2
     layer_roof_ms = 1e3 * max(wk["layer_flop"] / (peak * 1e12),
                               ((cfg.N_r + cfg.N_s) * 3 * cfg.I * cfg.d * wq + cfg.T * cfg.d * 6)

@@ -211,8 +211,8 @@ MOE_API moe_status moe_quantize_e4m3(const void* x, moe_dtype x_dt, int64_t rows
  * moe_expert_ffn: both, with h in the workspace (moe_expert_ffn_workspace bytes).
  * expert_offset [N_r+1] comes from moe_dispatch.
  * The bf16 GEMMs hand out their tiles from one of 64 device counters built into the
- * library, taken round-robin per call and zeroed on the call's stream before its kernel;
- * so at most 64 bf16 gate/up or down calls may be in flight on a device at one time. */
+ * library, taken round-robin per call; the last CTA of a call puts its counter back to
+ * zero, so at most 64 bf16 gate/up or down calls may be in flight on a device at once. */
 MOE_API size_t moe_expert_ffn_workspace(moe_shape sh, moe_dtype w_dt);
 MOE_API moe_status moe_expert_gate_up(const void* x_perm, const float* x_perm_scale,
                               const void* u, const float* u_scale,
