@@ -3,9 +3,10 @@
 Sizes: the tiny fp32 layer and the mid bf16 layer are compared element by element;
 the DeepSeek-V3-shaped layer is compared at full size: routing, dispatch and the bias
 update on every token, h' on 66 sampled tokens, and the expert GEMMs' output on every
-row of four whole segments (largest, smallest, one of 257-512 rows, the shared expert).  Edge cases: ragged token counts and
-hidden sizes that are not tile multiples, an empty batch, a single token, experts with
-no tokens and an expert with every token.
+row of four whole segments (largest, smallest, one of 257-512 rows, the shared
+expert); a 65536-token batch at the mid sizes is compared the same way on sampled
+tokens.  Edge cases: ragged token counts and hidden sizes that are not tile multiples,
+an empty batch, a single token, experts with no tokens and an expert with every token.
 """
 import numpy as np
 import pytest
@@ -56,6 +57,21 @@ def test_v3_layer_full_size_sampled():
     check_seq_stat(cfg, r, idx)
     check_output_sampled(cfg, r, sample, BF16_REL, BF16_ABS)
     check_segments_full(cfg, r)
+
+
+def test_largest_batch_sampled():
+    """65536 tokens in 8 sequences at the mid layer's sizes (d=2048, 64 experts top-6, 2
+    shared, I=1408): 512 router clusters, about 6 k rows per expert segment (24 token
+    tiles of gate/up, 12 of down), 393 k rows in the FFN row space.  Routing, dispatch,
+    the bias update and the statistic on every token; h' on 66 sampled tokens."""
+    cfg = synth.MoEConfig("large", T=65536, d=2048, N_r=64, K_r=6, N_s=2, I=1408, n_seq=8,
+                          dtype="bf16", bias="uniform", seed=11)
+    r = run_layer(cfg)
+    idx, _ = check_routing(cfg, r)
+    check_seq_stat(cfg, r, idx)
+    sample = np.random.default_rng(1).choice(cfg.T, 64, replace=False)
+    sample = np.concatenate([sample, [0, cfg.T - 1]])
+    check_output_sampled(cfg, r, sample, BF16_REL, BF16_ABS)
 
 
 def check_segments_full(cfg, r):

@@ -60,6 +60,21 @@ def test_noalloc_dispatch_matches_workspace_dispatch_twice():
     assert moe.device_error() == 0
 
 
+@pytest.mark.gpu
+def test_noalloc_dispatch_at_its_largest_batch():
+    """65536 tokens with 256 experts: ceil(T/32) * N_r fills the built-in scratch exactly."""
+    T, N_r, K_r, d = 65536, 256, 8, 128
+    sh = moe.make_shape(T, d, N_r, K_r, 0, 128, 1, 1)
+    g = torch.Generator(device="cuda").manual_seed(9)
+    u = torch.randn(T, d, generator=g, device="cuda").to(torch.bfloat16)
+    idx = _routing(np.random.default_rng(9), T, N_r, K_r, 1.0)
+    ref, got = _dispatch_pair(idx, u, sh, T, N_r, K_r, d)
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+    assert int(got[0].sum()) == T * K_r
+    assert moe.device_error() == 0
+
+
 def test_noalloc_dispatch_rejects_batches_beyond_its_scratch():
     moe_build.build()
     lib = moe.load_library()
