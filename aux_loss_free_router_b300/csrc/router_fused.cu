@@ -20,6 +20,14 @@
 // totals to fp32 seq_p_sum.  A batch of at most 128 tokens is one cluster: there CTA 0
 // adds the CTAs' run sums over distributed shared memory instead (fp32, token order).
 // C is chosen so that the clusters fill the SMs: 2 at 8192 tokens, 8 for decode batches.
+//
+// With 256 experts and at least 2048 tokens the product is formed by CTA pairs instead
+// (cta_group::2 MMAs of M = 256 tokens): a cluster of C CTAs takes 256 tokens, its C/2
+// pairs split d, and in each pair the even CTA holds tokens 0..127 of the product and the
+// odd one tokens 128..255, each loading its own 128 token rows and half of the centroid
+// rows per K step.  An SM then takes in a third less per K step (the centroid slice is
+// the larger part of a single CTA's intake).  The decisions are as above, over the C/2
+// partial tiles that hold a token; 16 warps decide.
 #include <algorithm>
 
 #include "launch.h"
@@ -34,10 +42,13 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BK = 64, STAGES = 4, THREADS = 256;
+// pair launches: CTA pairs multiply 256 tokens at a time, each CTA taking in half of the
+// centroids per K step, through a deeper ring; 16 warps decide
+constexpr int PSTAGES = 6, PTHREADS = 512;
 constexpr int A_BYTES = BM * BK * 2;
 
 struct FCtrl {
-  uint64_t full[STAGES], empty[STAGES], tfull, fin;
+  uint64_t full[PSTAGES], empty[PSTAGES], tfull, fin;
   uint32_t tmem_base;
   int abort_flag;
   int is_last;
@@ -51,13 +62,17 @@ struct FCtrl {
 __host__ __device__ constexpr int part_stride(int n_r) { return n_r + 4; }
 
 // Shared memory: the TMA ring during the K loop; afterwards the same space holds the
-// partial tile [128][N_r + 4] and the normalised affinities of the CTA's 128/C tokens
-// [128/C][N_r].  The control block follows the larger of the two.
-__host__ __device__ constexpr size_t fused_ctrl_offset(int n_r, int C) {
-  return (size_t)STAGES * (A_BYTES + (size_t)n_r * BK * 2) >
-                 (size_t)BM * part_stride(n_r) * 4 + (size_t)(BM / C) * n_r * 4
-             ? (size_t)STAGES * (A_BYTES + (size_t)n_r * BK * 2)
-             : (size_t)BM * part_stride(n_r) * 4 + (size_t)(BM / C) * n_r * 4;
+// partial tile [128][N_r + 4] and the normalised affinities of the CTA's 128/KS tokens
+// [128/KS][N_r] (KS: the K slices of a cluster, C for single-CTA launches and C/2 for
+// pair launches).  The control block follows the larger of the two.
+__host__ __device__ constexpr size_t fused_ring_bytes(int n_r, bool pair) {
+  return (size_t)(pair ? PSTAGES : STAGES) * (A_BYTES + (size_t)(pair ? n_r / 2 : n_r) * BK * 2);
+}
+__host__ __device__ constexpr size_t fused_ctrl_offset(int n_r, int C, bool pair) {
+  return fused_ring_bytes(n_r, pair) >
+                 (size_t)BM * part_stride(n_r) * 4 + (size_t)(BM / (pair ? C / 2 : C)) * n_r * 4
+             ? fused_ring_bytes(n_r, pair)
+             : (size_t)BM * part_stride(n_r) * 4 + (size_t)(BM / (pair ? C / 2 : C)) * n_r * 4;
 }
 
 struct FusedArgs {
@@ -74,10 +89,10 @@ struct FusedArgs {
 constexpr double kFix = 4294967296.0;   // 2^32: fixed-point units of the P accumulators
 
 // z[j] = sum over the CC slices, in slice order, of the value at row + 32*j in the
-// partial tile of each CTA of the cluster.  The loads of a batch of slices (at most 16
-// values) are all issued before the first add.
-template <int Q, int CC>
-__device__ __forceinline__ void sum_cols(float (&z)[Q], const float* row) {
+// partial tile of slice s's CTA, cluster rank s*RS + hf.  The loads of a batch of slices
+// (at most 16 values) are all issued before the first add.
+template <int Q, int CC, int RS>
+__device__ __forceinline__ void sum_cols(float (&z)[Q], const float* row, int hf) {
   constexpr int PER = (16 / Q) < CC ? (16 / Q) : CC;
 #pragma unroll
   for (int s0 = 0; s0 < CC; s0 += PER) {
@@ -85,7 +100,8 @@ __device__ __forceinline__ void sum_cols(float (&z)[Q], const float* row) {
 #pragma unroll
     for (int bb = 0; bb < PER; ++bb)
 #pragma unroll
-      for (int j = 0; j < Q; ++j) w[bb][j] = tc::ld_cluster_f32(tc::cluster_addr(row + 32 * j, (uint32_t)(s0 + bb)));
+      for (int j = 0; j < Q; ++j)
+        w[bb][j] = tc::ld_cluster_f32(tc::cluster_addr(row + 32 * j, (uint32_t)((s0 + bb) * RS + hf)));
 #pragma unroll
     for (int bb = 0; bb < PER; ++bb)
 #pragma unroll
@@ -93,38 +109,51 @@ __device__ __forceinline__ void sum_cols(float (&z)[Q], const float* row) {
   }
 }
 
-template <int Q, int G>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int Q, int G, bool PAIR>
+__global__ void __launch_bounds__(PAIR ? PTHREADS : THREADS, 1)
     router_fused_kernel(const __grid_constant__ CUtensorMap mU, const __grid_constant__ CUtensorMap mE,
                         FusedArgs a) {
   constexpr int N = 32 * Q;
   constexpr int LD = part_stride(N);
+  constexpr int STG = PAIR ? PSTAGES : STAGES;
+  constexpr int NTHR = PAIR ? PTHREADS : THREADS;
+  constexpr int NB = PAIR ? N / 2 : N;                 // centroid rows this CTA loads
   extern __shared__ uint8_t smem_raw[];
   pdl_release();
   pdl_wait();
   const uint32_t raw_off = tc::smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_off & 1023u)) & 1023u);
-  constexpr int SBYTES = A_BYTES + N * BK * 2;
+  constexpr int SBYTES = A_BYTES + NB * BK * 2;
   // after the K loop the ring's space holds the partial tile [128][LD] and the
   // normalised affinities of this CTA's tokens [R][N] (P sums)
   float* part = reinterpret_cast<float*>(base);
   float* sp_tile = part + BM * LD;
-  FCtrl& F = *reinterpret_cast<FCtrl*>(base + fused_ctrl_offset(N, a.C));
+  FCtrl& F = *reinterpret_cast<FCtrl*>(base + fused_ctrl_offset(N, a.C, PAIR));
 
   const RouteOut& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = a.C;
   const int c = (int)tc::cluster_rank();
-  const int tile0 = (blockIdx.x / C) * BM;                 // first token of the cluster
+  // A single-CTA launch: the cluster's C CTAs each multiply the cluster's 128 tokens
+  // over one slice of d.  A pair launch: the cluster's C/2 CTA pairs each multiply its
+  // 256 tokens over one slice of d; the even CTA of a pair holds the first 128 tokens of
+  // the product, the odd one the next 128.
+  const int KS = PAIR ? C / 2 : C;                          // slices of d
+  const int ks = PAIR ? c >> 1 : c;                         // this CTA's slice
+  const int hf = PAIR ? c & 1 : 0;                          // this CTA's half of a pair tile
+  const int tile0 = (blockIdx.x / C) * (PAIR ? 2 * BM : BM);  // first token of the cluster
+  const int row0 = tile0 + hf * BM;                         // this CTA's 128 product rows
   const int nk = (a.d + BK - 1) / BK;
-  const int kb0 = c * nk / C, kb1 = (c + 1) * nk / C;     // this CTA's slice of d (>= 1 block)
-  const int R = BM / C;
-  const int my0 = tile0 + c * R;                           // this CTA's tokens
+  const int kb0 = ks * nk / KS, kb1 = (ks + 1) * nk / KS;   // this CTA's slice of d (>= 1 block)
+  const int R = BM / KS;
+  const int my0 = row0 + ks * R;                            // the tokens this CTA decides
   const int ntok = max(0, min(R, p.T - my0));
   const bool want_p = p.pwin != nullptr;
+  const bool leader = !PAIR || hf == 0;                     // issues the MMAs
+  const uint16_t pmask = (uint16_t)(3u << (2 * ks));        // PAIR: the pair's two ranks
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < STG; ++i) {
       tc::mbar_init(&F.full[i], 1);
       tc::mbar_init(&F.empty[i], 1);
     }
@@ -136,12 +165,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (want_p && (int)threadIdx.x < ntok) F.seqid[threadIdx.x] = seq_of(my0 + threadIdx.x, p.seq_offsets, p.n_seq);
   if (warp == 1) {
-    tc::tmem_alloc(&F.tmem_base, N < 32 ? 32 : N);
-    tc::tmem_relinquish();
+    if constexpr (PAIR) {
+      tc::tmem_alloc_pair(&F.tmem_base, N < 32 ? 32 : N);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(&F.tmem_base, N < 32 ? 32 : N);
+      tc::tmem_relinquish();
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  // pairs: both CTAs' barriers exist before a copy or a commit reaches the peer's
+  if constexpr (PAIR) tc::cluster_sync();
   const uint32_t tmem_base = F.tmem_base;
   volatile int* abort_flag = &F.abort_flag;
 
@@ -149,43 +185,62 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
-        const int st = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
+        const int st = it % STG;
+        const uint32_t ph = (it / STG) & 1;
         if (!tc::mbar_wait(&F.empty[st], ph ^ 1, abort_flag, a.err)) break;
-        tc::mbar_arrive_expect_tx(&F.full[st], (uint32_t)SBYTES);
         uint8_t* sa = base + st * SBYTES;
-        tc::tma_load_2d(sa, &mU, &F.full[st], kb * BK, tile0);
-        tc::tma_load_2d(sa + A_BYTES, &mE, &F.full[st], kb * BK, 0);
+        if constexpr (PAIR) {
+          // both CTAs' copies complete on the even CTA's barrier
+          const uint32_t bar = tc::cluster_addr(&F.full[st], (uint32_t)(c & ~1));
+          if (leader) tc::mbar_arrive_expect_tx(&F.full[st], (uint32_t)(2 * SBYTES));
+          tc::tma_load_2d_pair(sa, &mU, bar, kb * BK, row0);
+          tc::tma_load_2d_pair(sa + A_BYTES, &mE, bar, kb * BK, hf * NB);
+        } else {
+          tc::mbar_arrive_expect_tx(&F.full[st], (uint32_t)SBYTES);
+          tc::tma_load_2d(sa, &mU, &F.full[st], kb * BK, tile0);
+          tc::tma_load_2d(sa + A_BYTES, &mE, &F.full[st], kb * BK, 0);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16(BM, N);
+    if (lane == 0 && leader) {
+      const uint32_t idesc = tc::idesc_bf16(PAIR ? 2 * BM : BM, N);
       bool ok = true;
       for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
-        const int st = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
+        const int st = it % STG;
+        const uint32_t ph = (it / STG) & 1;
         if (!tc::mbar_wait(&F.full[st], ph, abort_flag, a.err)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t s0 = tc::smem_u32(base + st * SBYTES);
         const uint64_t ad = tc::sdesc_sw128(s0), bd = tc::sdesc_sw128(s0 + A_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          tc::mma_bf16(tmem_base, ad + 2 * kk, bd + 2 * kk, idesc, (it | kk) != 0);
-        tc::mma_commit(&F.empty[st]);
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          if constexpr (PAIR) tc::mma_bf16_pair(tmem_base, ad + 2 * kk, bd + 2 * kk, idesc, (it | kk) != 0);
+          else tc::mma_bf16(tmem_base, ad + 2 * kk, bd + 2 * kk, idesc, (it | kk) != 0);
+        }
+        if constexpr (PAIR) tc::mma_commit_pair_mask(&F.empty[st], pmask);
+        else tc::mma_commit(&F.empty[st]);
       }
-      if (ok) tc::mma_commit(&F.tfull);
-      tc::mma_commit(&F.fin);
+      if constexpr (PAIR) {
+        if (ok) tc::mma_commit_pair_mask(&F.tfull, pmask);
+        tc::mma_commit_pair_mask(&F.fin, pmask);
+      } else {
+        if (ok) tc::mma_commit(&F.tfull);
+        tc::mma_commit(&F.fin);
+      }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // TMEM -> shared memory: lane quarter q = warp - 4 holds tokens 32q .. 32q + 31
-    const int q = warp - 4;
+  } else if (warp >= 4 && warp < (PAIR ? 12 : 8)) {
+    // TMEM -> shared memory: lane quarter q = warp & 3 holds tokens 32q .. 32q + 31;
+    // pair launches split the columns over two warps per quarter
+    const int q = warp & 3;
+    constexpr int CW = PAIR ? N / 2 : N;                  // columns per drain warp
+    const int cbeg = PAIR ? ((warp - 4) >> 2) * CW : 0;
     const bool got = tc::mbar_wait(&F.tfull, 0, abort_flag, a.err);
     if (__all_sync(0xffffffffu, got)) {
       tc::fence_after_sync();
       float* row = part + (size_t)(q * 32 + lane) * LD;
 #pragma unroll 1
-      for (int c0 = 0; c0 < N; c0 += 32) {
+      for (int c0 = cbeg; c0 < cbeg + CW; c0 += 32) {
         uint32_t z[32];
         tc::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + c0, z);
         tc::tmem_ld_wait();
@@ -209,7 +264,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // loads the next pair's partials over distributed shared memory while it decides.
   const bool aborted = *abort_flag != 0;
   {
-    constexpr int NW = THREADS / 32;
+    constexpr int NW = NTHR / 32;
     float bv[Q];
 #pragma unroll
     for (int j = 0; j < Q; ++j) bv[j] = __ldg(a.b + lane + 32 * j);
@@ -217,10 +272,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
         const int tl = min(tl0 + n * NW, max(ntok - 1, 0));          // a spare token re-reads a valid row
-        const float* row = part + (size_t)(c * R + tl) * LD + lane;  // row of the partial tiles
-        if (C == 2) sum_cols<Q, 2>(z[n], row);
-        else if (C == 4) sum_cols<Q, 4>(z[n], row);
-        else sum_cols<Q, 8>(z[n], row);
+        const float* row = part + (size_t)(ks * R + tl) * LD + lane;  // row of the partial tiles
+        if constexpr (PAIR) {
+          if (KS == 1) sum_cols<Q, 1, 2>(z[n], row, hf);
+          else if (KS == 2) sum_cols<Q, 2, 2>(z[n], row, hf);
+          else sum_cols<Q, 4, 2>(z[n], row, hf);
+        } else {
+          if (C == 2) sum_cols<Q, 2, 1>(z[n], row, 0);
+          else if (C == 4) sum_cols<Q, 4, 1>(z[n], row, 0);
+          else sum_cols<Q, 8, 1>(z[n], row, 0);
+        }
       }
     };
     float z[2][Q];
@@ -261,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   __syncthreads();
 
-  if (a.one_cluster) {
+  if (!PAIR && a.one_cluster) {
     // One cluster covers the batch: each CTA leaves its run sums in shared memory and
     // CTA 0 adds them per sequence over distributed shared memory, in token order (fp32;
     // no atomics and no scratch to zero).
@@ -361,7 +422,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) {
     __syncwarp();
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem_base, N < 32 ? 32 : N);
+    if constexpr (PAIR) tc::tmem_dealloc_pair(tmem_base, N < 32 ? 32 : N);
+    else tc::tmem_dealloc(tmem_base, N < 32 ? 32 : N);
   }
 }
 
@@ -376,7 +438,23 @@ int fused_cluster(int T, int d) {
   return C;
 }
 
-size_t fused_smem(int n_r, int C) { return fused_ctrl_offset(n_r, C) + sizeof(FCtrl) + 1024; }
+// Pair launches, for 256 experts and batches of at least kPairMinTokens (the centroid
+// slice is then two thirds of what a single CTA takes in per K step; with 64 experts
+// the pairs measured slower): C/2 pairs per 256-token tile,
+// C/2 the largest power of two up to 4 with the clusters still fitting the SMs in one
+// wave, and no more slices than d's 64-wide blocks.
+constexpr int kPairMinTokens = 2048;
+int fused_cluster_pair(int T, int d) {
+  const int tiles = (T + 2 * BM - 1) / (2 * BM);
+  const int nk = (d + BK - 1) / BK;
+  int KS = 1;
+  while (KS < 4 && (long long)tiles * 2 * KS * 2 <= device_sm_count() && KS * 2 <= nk) KS *= 2;
+  return 2 * KS;
+}
+
+size_t fused_smem(int n_r, int C, bool pair) {
+  return fused_ctrl_offset(n_r, C, pair) + sizeof(FCtrl) + 1024;
+}
 
 }  // namespace
 
@@ -390,37 +468,46 @@ cudaError_t launch_router_fused(const void* u, const void* e, int d, const float
   if (p.T == 0) return cudaSuccess;
   CUtensorMap mU, mE;
   const uint64_t rb = (uint64_t)d * 2;
+  // large batches: CTA pairs (each CTA loads half of the centroid rows per K step)
+  const bool pair = p.T >= kPairMinTokens && p.N_r == 256;
   if (!make_tmap_2d(&mU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, d, p.T, rb, BK, BM) ||
-      !make_tmap_2d(&mE, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, e, d, p.N_r, rb, BK, p.N_r))
+      !make_tmap_2d(&mE, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, e, d, p.N_r, rb, BK, pair ? p.N_r / 2 : p.N_r))
     return cudaErrorInvalidValue;
-  const int C = fused_cluster(p.T, d);
+  const int C = pair ? fused_cluster_pair(p.T, d) : fused_cluster(p.T, d);
   // scratch: the counter, then the fixed-point accumulators, zeroed together
   unsigned long long* p_acc = reinterpret_cast<unsigned long long*>(done_ctr + 64);
-  const int one = (p.T + BM - 1) / BM == 1 ? 1 : 0;
+  const int tile = pair ? 2 * BM : BM;
+  const int one = (p.T + tile - 1) / tile == 1 ? 1 : 0;   // never for pair launches
   FusedArgs a{p, b, d, C, one, done_ctr, p_acc, seq_p_sum, dev_error_ptr()};
   cudaError_t err = cudaSuccess;
   if (p.pwin && !one)
     err = cudaMemsetAsync(done_ctr, 0, 256 + (size_t)p.n_seq * p.N_r * sizeof(unsigned long long), st);
   if (err != cudaSuccess) return err;
-  const size_t smem = fused_smem(p.N_r, C);
-  auto go = [&](auto kernel) {
-    cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e2 != cudaSuccess) return e2;
-    return launch_pdl(kernel, dim3(((p.T + BM - 1) / BM) * C), dim3(THREADS), smem, st, (unsigned)C, mU, mE, a);
+  const size_t smem = fused_smem(p.N_r, C, pair);
+  const dim3 grid(((p.T + tile - 1) / tile) * C);
+  auto go = [&](auto single, auto paired) {
+    auto run = [&](auto kernel, int threads) {
+      cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e2 != cudaSuccess) return e2;
+      return launch_pdl(kernel, grid, dim3(threads), smem, st, (unsigned)C, mU, mE, a);
+    };
+    return pair ? run(paired, PTHREADS) : run(single, THREADS);
   };
   // N_r = 32 Q experts in G groups (G divides Q: router_fused_ok)
+#define MOE_RF(Q, G) go(router_fused_kernel<Q, G, false>, router_fused_kernel<Q, G, true>)
   switch (p.N_r * 16 + p.G) {
-    case 64 * 16 + 1: err = go(router_fused_kernel<2, 1>); break;
-    case 64 * 16 + 2: err = go(router_fused_kernel<2, 2>); break;
-    case 128 * 16 + 1: err = go(router_fused_kernel<4, 1>); break;
-    case 128 * 16 + 2: err = go(router_fused_kernel<4, 2>); break;
-    case 128 * 16 + 4: err = go(router_fused_kernel<4, 4>); break;
-    case 256 * 16 + 1: err = go(router_fused_kernel<8, 1>); break;
-    case 256 * 16 + 2: err = go(router_fused_kernel<8, 2>); break;
-    case 256 * 16 + 4: err = go(router_fused_kernel<8, 4>); break;
-    case 256 * 16 + 8: err = go(router_fused_kernel<8, 8>); break;
+    case 64 * 16 + 1: err = MOE_RF(2, 1); break;
+    case 64 * 16 + 2: err = MOE_RF(2, 2); break;
+    case 128 * 16 + 1: err = MOE_RF(4, 1); break;
+    case 128 * 16 + 2: err = MOE_RF(4, 2); break;
+    case 128 * 16 + 4: err = MOE_RF(4, 4); break;
+    case 256 * 16 + 1: err = MOE_RF(8, 1); break;
+    case 256 * 16 + 2: err = MOE_RF(8, 2); break;
+    case 256 * 16 + 4: err = MOE_RF(8, 4); break;
+    case 256 * 16 + 8: err = MOE_RF(8, 8); break;
     default: return cudaErrorInvalidValue;
   }
+#undef MOE_RF
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

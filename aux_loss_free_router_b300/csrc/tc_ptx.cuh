@@ -369,5 +369,15 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
       : "memory");
 }
 
+// The same for a pair that is not ranks 0 and 1 of its cluster: `mask` has the bits of
+// the pair's two cluster ranks (3 << 2p for the pair of ranks 2p, 2p + 1).
+__device__ __forceinline__ void mma_commit_pair_mask(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
 }  // namespace tc
 }  // namespace moe

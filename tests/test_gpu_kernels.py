@@ -101,6 +101,10 @@ def test_combine_v3_shape_sampled():
     (48, 5, 3, 1, 130, 128, 2),      # three groups of 16, the best group keeps all five
     (96, 6, 3, 3, 164, 256, 4),      # three groups of 32: one thread per token
     (200, 10, 1, 1, 77, 256, 1),     # ten of 200 experts
+    # 256 experts, batches of 2048 tokens or more: the fused router's CTA-pair launches
+    (256, 8, 8, 4, 2200, 384, 4),    # last 256-token tile partly past T, four slices of d
+    (256, 6, 1, 1, 2100, 256, 2),    # the last tile's odd CTA holds no token
+    (256, 8, 4, 2, 2048, 128, 1),    # two slices of d, one 64-wide block each
 ])
 def test_router_shapes_bit_exact(N_r, K_r, G, M, T, d, n_seq):
     cfg = synth.MoEConfig("route", T=T, d=d, N_r=N_r, K_r=K_r, N_s=0, I=128, G=G, M=M,
@@ -115,16 +119,17 @@ def test_router_shapes_bit_exact(N_r, K_r, G, M, T, d, n_seq):
                                rtol=1e-5)
 
 
-@pytest.mark.parametrize("T,offsets", [
-    (100, [0, 0, 40, 40, 100]),           # one cluster: empty first and middle sequences
-    (300, [0, 128, 128, 129, 300, 300]),  # several clusters: empty sequences at a boundary and at the end
+@pytest.mark.parametrize("T,offsets,N_r,G,M", [
+    (100, [0, 0, 40, 40, 100], 128, 4, 2),           # one cluster: empty first and middle sequences
+    (300, [0, 128, 128, 129, 300, 300], 128, 4, 2),  # several clusters: empty sequences at a boundary and at the end
+    (2300, [0, 256, 256, 1000, 2300, 2300], 256, 8, 4),  # CTA-pair launch
 ])
-def test_router_p_sums_with_empty_sequences(T, offsets):
+def test_router_p_sums_with_empty_sequences(T, offsets, N_r, G, M):
     """The fused router's P sums where some sequences hold no token: those rows are zero,
     the others match the oracle (a batch of <= 128 tokens adds its sums inside one
     cluster, a larger one through the fixed-point accumulators)."""
     n_seq = len(offsets) - 1
-    cfg = synth.MoEConfig("route-empty", T=T, d=256, N_r=128, K_r=8, N_s=0, I=128, G=4, M=2,
+    cfg = synth.MoEConfig("route-empty", T=T, d=256, N_r=N_r, K_r=8, N_s=0, I=128, G=G, M=M,
                           dtype="bf16", bias="uniform", seed=T, n_seq=1)
     x = synth.make_inputs(cfg, device="cuda", with_weights=False)
     x["seq_offsets"] = torch.tensor(offsets, dtype=torch.int32, device="cuda")
