@@ -8,7 +8,9 @@
 // s_{i,t} normalised over the selected set.  pwwt.cn notes §1.3: with the group limit
 // only the M groups with the largest sums of their K_r/M best keys are eligible; here a
 // group is Q/G whole 32-expert blocks and K_r/M <= 2.  Keys are fp32(s + b), ties go to
-// the lower expert (and group) index: the decisions are those of route_oct.cuh.
+// the lower expert (and group) index: the decisions are those of route_oct.cuh.  Each
+// lane sorts its Q keys once, so a Top-K_r round needs two warp reductions over the
+// lanes' leading keys and a shift of the winning lane's list.
 #pragma once
 
 #include <math_constants.h>
@@ -27,6 +29,31 @@ __device__ __forceinline__ uint32_t key_code(float k) {
 
 __device__ __forceinline__ float code_key(uint32_t c) {
   return __uint_as_float((c & 0x80000000u) ? (c & 0x7fffffffu) : ~c);
+}
+
+// Sorts Q = 2, 4 or 8 values in descending order with a fixed comparator network.
+template <int Q>
+__device__ __forceinline__ void sort_desc(uint64_t (&k)[Q]) {
+  auto cx = [&](int a, int b) {   // k[a] >= k[b] afterwards
+    const uint64_t x = k[a], y = k[b];
+    const bool sw = y > x;
+    k[a] = sw ? y : x;
+    k[b] = sw ? x : y;
+  };
+  if constexpr (Q == 2) {
+    cx(0, 1);
+  } else if constexpr (Q == 4) {
+    cx(0, 1); cx(2, 3); cx(0, 2); cx(1, 3); cx(1, 2);
+  } else {
+    static_assert(Q == 8, "Q is 2, 4 or 8");
+    // Batcher's odd-even merge sort of eight values: 19 comparators
+    cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
+    cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
+    cx(1, 2); cx(5, 6);
+    cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
+    cx(2, 4); cx(3, 5);
+    cx(1, 2); cx(3, 4); cx(5, 6);
+  }
 }
 
 // Group limit, Top-K_r and gates of NT tokens at once (independent chains, so the warp
@@ -88,37 +115,53 @@ __device__ __forceinline__ void warp_decide(const float (&s)[NT][Q], const float
     }
   }
 
-  // K_r rounds: the warp's best remaining code, ties to the lower expert index
-  unsigned taken[NT];
-  int my_idx[NT];
-  float my_s[NT], total[NT];
+  // Each lane orders its Q keys once, as 64-bit values (code, then Q-1-j: a higher
+  // code first, and of equal codes the lower expert index, since lane l holds experts
+  // l + 32j); a round then looks only at each lane's head.
+  uint64_t k[NT][Q];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) { taken[n] = 0; my_idx[n] = 0; my_s[n] = 0.f; total[n] = 0.f; }
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int j = 0; j < Q; ++j) k[n][j] = ((uint64_t)u[n][j] << 32) | (uint32_t)(Q - 1 - j);
+#pragma unroll
+  for (int n = 0; n < NT; ++n) sort_desc<Q>(k[n]);
+
+  // K_r rounds: the warp's best head code (redux max), of equal ones the lowest expert
+  // index (redux min); the lane that held it drops its head
+  int my_idx[NT];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) my_idx[n] = 0;
   for (int r = 0; r < p.K_r; ++r) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      uint32_t best = 0u;
-      int bj = 0;
-      float bs = 0.f;
-#pragma unroll
-      for (int j = 0; j < Q; ++j) {
-        const uint32_t c = ((taken[n] >> j) & 1u) ? 0u : u[n][j];
-        if (c > best) { best = c; bj = j; bs = s[n][j]; }
-      }
-      const uint32_t m = __reduce_max_sync(0xffffffffu, best);
-      const uint32_t cand = (best == m && m != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+      const uint32_t head = (uint32_t)(k[n][0] >> 32);
+      const uint32_t m = __reduce_max_sync(0xffffffffu, head);
+      const uint32_t e = (uint32_t)lane + 32u * (uint32_t)(Q - 1 - (int)(uint32_t)k[n][0]);
+      const uint32_t cand = (head == m && m != 0u) ? e : 0xffffffffu;
       const uint32_t w = __reduce_min_sync(0xffffffffu, cand);
-      if (cand == w) taken[n] |= 1u << bj;   // the lane that holds expert w
-      const float sw = __shfl_sync(0xffffffffu, bs, (int)(w & 31u));
-      total[n] = __fadd_rn(total[n], sw);
-      if (lane == r) { my_idx[n] = (int)w; my_s[n] = sw; }
+      const bool won = cand == w;
+#pragma unroll
+      for (int j = 0; j + 1 < Q; ++j) k[n][j] = won ? k[n][j + 1] : k[n][j];
+      k[n][Q - 1] = won ? 0ull : k[n][Q - 1];
+      if (lane == r) my_idx[n] = (int)w;
     }
   }
+  // gates: lane r < K_r fetches the raw s of its expert; the normaliser adds them in
+  // round order
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
+    const int w = my_idx[n];
+    float my_s = 0.f;
+#pragma unroll
+    for (int j = 0; j < Q; ++j) {
+      const float v = __shfl_sync(0xffffffffu, s[n][j], w & 31);
+      my_s = (w >> 5) == j ? v : my_s;
+    }
+    float total = 0.f;
+    for (int r = 0; r < p.K_r; ++r) total = __fadd_rn(total, __shfl_sync(0xffffffffu, my_s, r));
     if (valid[n] && lane < p.K_r) {
-      p.topk_idx[(size_t)t[n] * p.K_r + lane] = my_idx[n];
-      p.topk_gate[(size_t)t[n] * p.K_r + lane] = __fdiv_rn(my_s[n], total[n]);
+      p.topk_idx[(size_t)t[n] * p.K_r + lane] = w;
+      p.topk_gate[(size_t)t[n] * p.K_r + lane] = __fdiv_rn(my_s, total);
     }
   }
 }

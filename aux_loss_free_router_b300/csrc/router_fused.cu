@@ -55,6 +55,7 @@ struct FCtrl {
   int nruns;            // one-cluster launches: runs of one sequence among this CTA's tokens
   int seqid[BM];
   int runseq[BM];       // ... and the sequence of each run
+  float psh[2][256];    // P sums of one run: the two halves of the tokens, per expert
 };
 
 // Row stride (floats) of a partial tile in shared memory: N_r + 4 keeps the float4
@@ -376,14 +377,44 @@ __global__ void __launch_bounds__(PAIR ? PTHREADS : THREADS, 1)
     }
   } else {
     if (want_p && !aborted && ntok > 0) {
-      for (int i = threadIdx.x; i < N; i += blockDim.x) {
-        float acc = 0.f;
-        for (int r = 0; r < ntok; ++r) {
-          acc = __fadd_rn(acc, sp_tile[(size_t)r * N + i]);
-          if (r == ntok - 1 || F.seqid[r + 1] != F.seqid[r]) {   // end of a run
-            const unsigned long long v = (unsigned long long)__double2ll_rn((double)acc * kFix);
-            atomicAdd(a.p_acc + (size_t)F.seqid[r] * N + i, v);
-            acc = 0.f;
+      if (F.seqid[0] == F.seqid[ntok - 1]) {
+        // the CTA's tokens lie in one sequence (the usual case): with two threads per
+        // expert, each adds a fixed half of the tokens in order, and the halves are added
+        // in order before the one fixed-point update
+        const int SH = (int)blockDim.x >= 2 * N ? 2 : 1;
+        const int half = (ntok + SH - 1) / SH;
+        if ((int)threadIdx.x < SH * N) {
+          const int i = (int)threadIdx.x % N, h = (int)threadIdx.x / N;
+          const int r1 = min(ntok, (h + 1) * half);
+          int r = h * half;
+          float acc = 0.f;
+          for (; r + 8 <= r1; r += 8) {
+            float v[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) v[x] = sp_tile[(size_t)(r + x) * N + i];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) acc = __fadd_rn(acc, v[x]);
+          }
+          for (; r < r1; ++r) acc = __fadd_rn(acc, sp_tile[(size_t)r * N + i]);
+          F.psh[h][i] = acc;
+        }
+        __syncthreads();
+        if ((int)threadIdx.x < N) {
+          const int i = (int)threadIdx.x;
+          const float acc = SH == 2 ? __fadd_rn(F.psh[0][i], F.psh[1][i]) : F.psh[0][i];
+          const unsigned long long v = (unsigned long long)__double2ll_rn((double)acc * kFix);
+          atomicAdd(a.p_acc + (size_t)F.seqid[0] * N + i, v);
+        }
+      } else {
+        for (int i = threadIdx.x; i < N; i += blockDim.x) {
+          float acc = 0.f;
+          for (int r = 0; r < ntok; ++r) {
+            acc = __fadd_rn(acc, sp_tile[(size_t)r * N + i]);
+            if (r == ntok - 1 || F.seqid[r + 1] != F.seqid[r]) {   // end of a run
+              const unsigned long long v = (unsigned long long)__double2ll_rn((double)acc * kFix);
+              atomicAdd(a.p_acc + (size_t)F.seqid[r] * N + i, v);
+              acc = 0.f;
+            }
           }
         }
       }
