@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "MoEError", "Shape", "load_library", "route", "dispatch", "dispatch_noalloc", "quantize_e4m3",
-    "expert_gate_up", "expert_down", "expert_ffn", "combine", "bias_update",
+    "expert_gate_up", "expert_gate_up_gather", "expert_down", "expert_ffn", "combine", "bias_update",
     "seq_balance_stat", "device_error", "quantize_weights", "route_workspace_bytes",
     "backward", "backward_workspace_bytes",
     "dispatch_workspace_bytes", "expert_ffn_workspace_bytes", "MoELayer",
@@ -67,6 +67,7 @@ _SIGS = {
     "moe_quantize_e4m3": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I32, _P, _P, _P]),
     "moe_expert_ffn_workspace": (_S, [Shape, ctypes.c_int]),
     "moe_expert_gate_up": (ctypes.c_int, [_P, _P, _P, _P, _P, Shape, ctypes.POINTER(_Weights), _P, _P, _P]),
+    "moe_expert_gate_up_gather": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.POINTER(_Weights), _P, _P]),
     "moe_expert_down": (ctypes.c_int, [_P, _P, _P, Shape, ctypes.POINTER(_Weights), _P, _P]),
     "moe_expert_ffn": (ctypes.c_int, [_P, _P, _P, _P, _P, Shape, ctypes.POINTER(_Weights), _P, _P, _S, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, ctypes.c_int, _P, _P, Shape, _P, ctypes.c_int, _P]),
@@ -104,6 +105,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 # Kernels each call enqueues for a non-empty batch (the launch count of a step).
 _KERNELS = {"moe_route": 2, "moe_dispatch": 3, "moe_dispatch_noalloc": 3, "moe_quantize_e4m3": 1, "moe_expert_gate_up": 1,
+            "moe_expert_gate_up_gather": 1,
             "moe_expert_down": 1, "moe_expert_ffn": 2, "moe_combine": 1, "moe_bias_update": 1,
             "moe_seq_balance_stat": 1,
             # gate/up recompute, per-token prep, six GEMMs, combine (+ counts with the
@@ -257,6 +259,14 @@ def expert_gate_up(x_perm, u, expert_offset, sh: Shape, weights: dict, h, x_perm
           _ptr(expert_offset), sh, ctypes.byref(wt), _ptr(h), _ptr(h_scale), _stream(stream))
 
 
+def expert_gate_up_gather(u, perm_token, expert_offset, sh: Shape, weights: dict, h, stream=None):
+    """bf16 gate/up reading the routed rows' tokens straight from u (row r is
+    u[perm_token[r]]): the dispatch can skip writing x_perm."""
+    wt = _weights(weights)
+    _call("moe_expert_gate_up_gather", _ptr(u), _ptr(perm_token), _ptr(expert_offset), sh,
+          ctypes.byref(wt), _ptr(h), _stream(stream))
+
+
 def expert_down(h, expert_offset, sh: Shape, weights: dict, y, h_scale=None, stream=None):
     wt = _weights(weights)
     _call("moe_expert_down", _ptr(h), _ptr(h_scale), _ptr(expert_offset), sh, ctypes.byref(wt),
@@ -405,6 +415,10 @@ class MoELayer:
     # within 2e-2 max-abs: a bf16 store alone errs by up to 0.0156 once |h'| >= 4)
     fp8: bool = False   # expert GEMMs in E4M3: weights quantised here once (128x128
     # blocks), tokens every step (1x128 tiles); routing stays on the bf16 tokens
+    gather_rows: bool = False   # bf16: gate/up reads the routed rows' tokens straight
+    # from u and the dispatch writes no x_perm (saves the x_perm buffer, T*K_r*d values;
+    # backward() then gathers x_perm itself).  Off by default: the gate/up GEMM runs
+    # about 2.6 times longer that way (its rows are copied by one warp's cp.async)
 
     def __post_init__(self):
         dev, dt = self.e.device, self.e.dtype
@@ -443,6 +457,8 @@ class MoELayer:
         # the bias update and the statistic run on a second stream beside the expert FFNs
         self._side = torch.cuda.Stream(device=dev) if dev.type == "cuda" else None
         self.ws_dispatch = _workspace(dispatch_workspace_bytes(self.shape), dev)
+        self._gather = self.gather_rows and not self.fp8 and dt == torch.bfloat16
+        self._x_perm_current = False
 
     def step(self, u: torch.Tensor, seq_offsets: torch.Tensor, update_bias: bool = True,
              events: Optional[list] = None, stream=None,
@@ -473,12 +489,19 @@ class MoELayer:
             expert_down(self.h_mid, self.expert_offset, sh, self.ffn_weights, self.y,
                         self.h_scale, stream=stream)
         else:
+            g = self._gather
             dispatch(self.topk_idx, sh, self.load, self.expert_offset, self.perm_token,
-                     self.inv_row, u, self.x_perm, workspace=self.ws_dispatch, stream=stream)
+                     self.inv_row, None if g else u, None if g else self.x_perm,
+                     workspace=self.ws_dispatch, stream=stream)
+            self._x_perm_current = not g
             joined = self._end_of_step(main, seq_offsets, update_bias)
             ev(2)
-            expert_gate_up(self.x_perm, u, self.expert_offset, sh, self.ffn_weights, self.h_mid,
-                           stream=stream)
+            if g:
+                expert_gate_up_gather(u, self.perm_token, self.expert_offset, sh, self.ffn_weights,
+                                      self.h_mid, stream=stream)
+            else:
+                expert_gate_up(self.x_perm, u, self.expert_offset, sh, self.ffn_weights, self.h_mid,
+                               stream=stream)
             ev(3)
             expert_down(self.h_mid, self.expert_offset, sh, self.ffn_weights, self.y,
                         stream=stream)
@@ -577,6 +600,12 @@ class MoELayer:
                          self.shape, self.ffn_weights, self._dgrad_w, dh, self._grads, seq_offsets, n_seq,
                          self.alpha if seq_offsets is not None else 0.0, workspace=self._bwd_ws, stream=stream)
             return self._grads
+        if not self._x_perm_current:
+            # the forward read its rows straight from u: gather x_perm (the same
+            # permutation, recomputed from the step's selection)
+            dispatch(self.topk_idx, self.shape, self.load, self.expert_offset, self.perm_token,
+                     self.inv_row, u, self.x_perm, workspace=self.ws_dispatch, stream=stream)
+            self._x_perm_current = True
         backward(u, self.e, self.s_out, self.topk_idx, self.topk_gate, self.expert_offset,
                  self.inv_row, self.x_perm, self.y, self.shape, self.weights, dh, self._grads,
                  seq_offsets, n_seq, self.alpha if seq_offsets is not None else 0.0,

@@ -263,6 +263,19 @@ moe_status moe_expert_gate_up(const void* x_perm, const float* x_perm_scale, con
   return cuda_status(err);
 }
 
+moe_status moe_expert_gate_up_gather(const void* u, const int32_t* perm_token,
+                                     const int32_t* expert_offset, moe_shape sh,
+                                     const moe_expert_weights* w, void* h, void* stream) {
+  moe_status st = check_shape(sh);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(sh, w)) != MOE_OK) return st;
+  if (w->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (sh.T == 0) return MOE_OK;
+  if (!ok_ptr(u) || !aligned16(u) || !ok_ptr(perm_token) || !ok_ptr(expert_offset) || !ok_ptr(h))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_ffn_up_tc_gather(ffn_shape(sh), u, perm_token, expert_offset, w, h, S(stream)));
+}
+
 moe_status moe_expert_down(const void* h, const float* h_scale, const int32_t* expert_offset,
                            moe_shape sh, const moe_expert_weights* w, void* y, void* stream) {
   moe_status st = check_shape(sh);

@@ -73,6 +73,11 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
                              const int32_t* expert_offset, const moe_expert_weights* w,
                              void* h, cudaStream_t st, void* save_a = nullptr,
                              void* save_c = nullptr);
+// The same with the routed token rows read straight from u at the rows perm_token gives
+// (no x_perm); bf16 only.
+cudaError_t launch_ffn_up_tc_gather(const FfnShape& s, const void* u, const int32_t* perm_token,
+                                    const int32_t* expert_offset, const moe_expert_weights* w, void* h,
+                                    cudaStream_t st);
 cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h,
                                const int32_t* expert_offset, const moe_expert_weights* w,
                                void* y, cudaStream_t st);

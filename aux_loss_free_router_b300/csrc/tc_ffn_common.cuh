@@ -30,6 +30,10 @@ struct TcArgs {
   // in the same row space and layout as h (kept for the backward pass)
   __nv_bfloat16* save_a = nullptr;
   __nv_bfloat16* save_c = nullptr;
+  // gate/up reading the routed token rows straight from u: u [T, d] and perm_token
+  // [T*K_r] (the token of each row of the routed row space)
+  const __nv_bfloat16* u = nullptr;
+  const int32_t* perm = nullptr;
 };
 
 // silu(g) * u = g * u / (1 + e^-g), with the fast reciprocal division (the result is

@@ -35,6 +35,15 @@
 // Tokens past the end of a tile's segment are loaded (or zero-filled past the tensor
 // end) but sit beyond the MMA's N or are not stored; features past I are computed from
 // the next expert's rows (or zeros) and not stored.
+//
+// GATHER variant (moe_expert_gate_up_gather): a routed tile's token rows come straight
+// from u at the rows perm_token gives, copied by the 32 lanes of warp 0 with cp.async
+// into the same swizzled layout; each CTA counts its lanes' copies of a stage on a
+// gfull barrier, the even CTA's MMA thread waits on its own, and the odd CTA's idle MMA
+// warp relays its CTA's to the even CTA's full barrier.  A generic-to-async proxy fence
+// precedes the MMAs' reads.  h is bit-identical to the x_perm path's; at the
+// DeepSeek-V3 shape the kernel ran about 2.6 times longer (one warp issues every
+// copy), so the layer keeps x_perm by default.
 #include "tc_ffn_common.cuh"
 #include "tmap.h"
 
@@ -53,6 +62,7 @@ constexpr int XCH = 2 * 16 * 128 * 4;           // raw values [2 buffers][16 tok
 
 struct Ctrl {
   uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], xfull[2], xempty[2], fin;
+  uint64_t gfull[STAGES];   // token rows gathered from u: the gather lanes' copies done
   uint64_t tq_full[TQ], tq_empty[TQ];
   int tq[TQ];
   uint32_t tmem_base;
@@ -63,6 +73,7 @@ struct Ctrl {
 constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + XCH + sizeof(Ctrl) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
+template <bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gate_up_kernel(const __grid_constant__ CUtensorMap mX_r, const __grid_constant__ CUtensorMap mX_s,
                   const __grid_constant__ CUtensorMap mW0_r, const __grid_constant__ CUtensorMap mW1_r,
@@ -86,8 +97,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      tc::mbar_init(&C.full[i], 1);
+      tc::mbar_init(&C.full[i], GATHER ? 2 : 1);   // gathering: and the odd CTA's relay
       tc::mbar_init(&C.empty[i], 1);
+      tc::mbar_init(&C.gfull[i], 32);               // the 32 gather lanes
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&C.tfull[i], 1);
@@ -98,8 +110,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < TQ; ++i) {
       tc::mbar_init(&C.tq_full[i], 1);
       // readers of a tile index: the even CTA's MMA thread, the four epilogue warps of
-      // each CTA and the odd CTA's producer
-      tc::mbar_init(&C.tq_empty[i], 10);
+      // each CTA and the odd CTA's producer (and, gathering, the odd CTA's relay)
+      tc::mbar_init(&C.tq_empty[i], GATHER ? 11 : 10);
     }
     tc::mbar_init(&C.fin, 1);
     C.abort_flag = 0;
@@ -149,7 +161,97 @@ __global__ void __launch_bounds__(THREADS, 1)
     return t;
   };
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // -------------------------------------------- producer, rows gathered from u --
+    // Lane 0 claims tiles and issues the weights' TMA copies (and, for a shared
+    // expert's tile, the token rows' copy: those rows are consecutive rows of u).  For a
+    // routed tile every lane copies 16-byte pieces of this CTA's token rows of the K step
+    // from u, at the rows perm gives, into the 128-byte-swizzled layout the MMA reads:
+    // lane l takes piece l & 7 of rows (l >> 3) + 4i.  Each lane's copies of a stage are
+    // counted on the stage's gfull barrier.
+    constexpr unsigned FULLM = 0xffffffffu;
+    int it = 0;
+    int tile = 0;
+    if (lane == 0) tile = leader ? claim_tile(0) : next_tile(0);
+    tile = __shfl_sync(FULLM, tile, 0);
+    const int chunk = lane & 7;
+    for (int k = 0; tile >= 0; ++k) {
+      if (__shfl_sync(FULLM, *abort_flag, 0)) break;
+      int next = -1;
+      if (lane == 0) {
+        if (leader) next = claim_tile(k + 1);             // one tile ahead of the loads
+        else release_tile(k);
+      }
+      next = __shfl_sync(FULLM, next, 0);
+      if (leader && next == -2) break;
+      const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
+      const bool shared = tcd.seg >= s.N_r;
+      const int e = shared ? tcd.seg - s.N_r : tcd.seg;
+      const int n_tok = tcd.n_tok;
+      const int half = ((n_tok + 15) & ~15) >> 1;     // token rows per CTA
+      const bool small = half <= SMALL_ROWS;
+      const CUtensorMap* mX = small ? &mXs_s : &mX_s;
+      const uint32_t stage_tx =
+          (uint32_t)A_BYTES + (shared ? (uint32_t)((small ? SMALL_ROWS : BT / 2) * BK * 2) : 0u);
+      const int x_row = tcd.tok0 + (int)rank * half;   // the CTA's first row within the segment
+      const CUtensorMap* mW0 = shared ? &mW0_s : &mW0_r;
+      const CUtensorMap* mW1 = shared ? &mW1_s : &mW1_r;
+      const int w_row = e * N + tcd.n * 128 + (int)rank * (128 / 2);
+      // this lane's rows: the token (-1: zero-filled, past the tile's tokens; -2: not
+      // copied, past the CTA's half of the MMA)
+      int tokr[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int rho = (lane >> 3) + 4 * i;
+        int t = -2;
+        if (!shared && rho < half) {
+          t = -1;
+          if ((int)rank * half + rho < n_tok) {
+            t = __ldg(args.perm + tcd.row0 + x_row + rho);
+            if (t < 0 || t >= s.T) {                    // not a token: report, copy zeros
+              record_error(args.err, MOE_ERR_INVALID_ARG);
+              t = -1;
+            }
+          }
+        }
+        tokr[i] = t;
+      }
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int st = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        const bool got = tc::mbar_wait(&C.empty[st], ph ^ 1, abort_flag, args.err);
+        if (!__all_sync(FULLM, got)) { ok = false; break; }
+        uint8_t* sa = base + st * STAGE_BYTES;
+        if (lane == 0) {
+          const uint32_t bar = tc::cluster_addr(&C.full[st], 0);   // the even CTA's barrier
+          if (leader) tc::mbar_arrive_expect_tx(&C.full[st], 2 * stage_tx);
+          tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);                 // 64 gate rows
+          tc::tma_load_2d_pair(sa + A_BYTES / 2, mW1, bar, kb * BK, w_row);   // 64 up rows
+          if (shared) tc::tma_load_2d_pair(sa + A_BYTES, mX, bar, kb * BK, x_row);
+        }
+        if (!shared) {
+          const uint32_t sb = tc::smem_u32(sa + A_BYTES);
+          const int col = kb * BK + chunk * 8;           // d is a multiple of 8
+          const bool in_row = col < s.d;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int rho = (lane >> 3) + 4 * i;
+            if (tokr[i] >= -1) {
+              const bool copy = tokr[i] >= 0 && in_row;
+              const __nv_bfloat16* src = copy ? args.u + (size_t)tokr[i] * s.d + col : args.u;
+              tc::cp_async16(sb + (uint32_t)(rho * 128 + ((chunk ^ (rho & 7)) << 4)), src, copy ? 16u : 0u);
+            }
+          }
+        }
+        tc::cp_async_mbar_arrive(&C.gfull[st]);
+      }
+      if (!ok) break;
+      if (!leader) next = lane == 0 ? next_tile(k + 1) : 0;
+      tile = __shfl_sync(FULLM, next, 0);
+    }
+    tc::cp_async_wait_all();
+  } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer --
       int it = 0;
@@ -212,6 +314,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int st = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!tc::mbar_wait(&C.full[st], ph, abort_flag, args.err)) { ok = false; break; }
+          if constexpr (GATHER) {
+            // this CTA's gathered rows have landed (the odd CTA's: its relay's arrival on
+            // full); the generic-proxy copies are ordered before the MMA's reads
+            if (!tc::mbar_wait(&C.gfull[st], ph, abort_flag, args.err)) { ok = false; break; }
+            tc::fence_proxy_async_shared();
+          }
           tc::fence_after_sync();
           const uint32_t s0 = tc::smem_u32(base + st * STAGE_BYTES);
           const uint64_t a = tc::sdesc_sw128(s0), b = tc::sdesc_sw128(s0 + A_BYTES);
@@ -225,6 +333,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // every pair MMA has finished once `fin` flips (in both CTAs)
       tc::mma_commit_pair(&C.fin);
+    } else if (GATHER && lane == 0) {
+      // ------------------------------------------- relay (odd CTA, gathering) --
+      // Once this CTA's gather lanes' copies of a stage have landed, order them before
+      // the pair MMA's reads and arrive on the even CTA's full barrier of the stage.
+      int it = 0;
+      bool ok = true;
+      for (int tcount = 0; ok; ++tcount) {
+        const int tile = next_tile(tcount);
+        if (tile < 0 || *abort_flag) break;
+        release_tile(tcount);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int st = it % STAGES;
+          if (!tc::mbar_wait(&C.gfull[st], (it / STAGES) & 1, abort_flag, args.err)) { ok = false; break; }
+          tc::fence_proxy_async_shared();
+          tc::mbar_arrive_cluster(tc::cluster_addr(&C.full[st], 0));
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue --
@@ -352,7 +477,38 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
   static int fit[64] = {};
   TcArgs a{s, expert_offset, static_cast<__nv_bfloat16*>(h), dev_error_ptr(), nullptr,
            static_cast<__nv_bfloat16*>(save_a), static_cast<__nv_bfloat16*>(save_c)};
-  return launch_pairs(tc_gate_up_kernel, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st);
+  return launch_pairs(tc_gate_up_kernel<false>, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st);
+}
+
+cudaError_t launch_ffn_up_tc_gather(const FfnShape& s, const void* u, const int32_t* perm_token,
+                                    const int32_t* expert_offset, const moe_expert_weights* w, void* h,
+                                    cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  CUtensorMap m[8];
+  const uint64_t rb = (uint64_t)s.d * 2;
+  // tokens of the shared experts: 128-row and 32-row boxes of u (the routed rows are
+  // gathered by the kernel's lanes); weights: 64-row boxes
+  bool ok = make_tmap_2d(&m[1], kBF16, u, s.d, s.T, rb, BK, BT / 2) &&
+            make_tmap_2d(&m[7], kBF16, u, s.d, s.T, rb, BK, SMALL_ROWS) &&
+            make_tmap_2d(&m[2], kBF16, w->gate, s.d, (uint64_t)s.N_r * s.I, rb, BK, 64) &&
+            make_tmap_2d(&m[3], kBF16, w->up, s.d, (uint64_t)s.N_r * s.I, rb, BK, 64);
+  if (ok && s.N_s > 0) {
+    ok = make_tmap_2d(&m[4], kBF16, w->s_gate, s.d, (uint64_t)s.N_s * s.I, rb, BK, 64) &&
+         make_tmap_2d(&m[5], kBF16, w->s_up, s.d, (uint64_t)s.N_s * s.I, rb, BK, 64);
+  } else {
+    m[4] = m[2];
+    m[5] = m[3];
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  m[0] = m[1];
+  m[6] = m[7];
+  const long long t_ub = (long long)s.T * s.K_r / BT + s.N_r + (long long)s.N_s * ((s.T + BT - 1) / BT);
+  static std::mutex mu;
+  static int fit[64] = {};
+  TcArgs a{s, expert_offset, static_cast<__nv_bfloat16*>(h), dev_error_ptr(), nullptr};
+  a.u = static_cast<const __nv_bfloat16*>(u);
+  a.perm = perm_token;
+  return launch_pairs(tc_gate_up_kernel<true>, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st);
 }
 
 }  // namespace moe

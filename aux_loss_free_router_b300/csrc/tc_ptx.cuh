@@ -259,6 +259,23 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// ------------------------------------------------------------ cp.async -----------
+
+// 16 bytes from global memory to shared memory, through L2 only; with src_bytes = 0
+// nothing is read and the 16 bytes are zero.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued before has completed (the
+// arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------ CTA pairs (cluster of two) -----
 
 __device__ __forceinline__ uint32_t cluster_rank() {

@@ -200,6 +200,67 @@ def test_expert_gemms_every_token_tile_size():
         assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref), (r0, len(xs))
 
 
+@pytest.mark.parametrize("d,I,seed", [(320, 384, 31), (2048, 1408, 32)])
+def test_gate_up_gather_matches_x_perm_bit_for_bit(d, I, seed):
+    """Gate/up reading the routed rows straight from u (row r = u[perm[r]]) against gate/up
+    on x_perm = u[perm]: the MMAs see the same operands in the same order, so h is
+    identical bit for bit.  Segments of every token-tile height as above, a d that ends
+    inside a 64-wide K step (the gathered pieces past d are zeros), tokens repeated and
+    in any order."""
+    counts = [0, 1, 8, 15, 16, 17, 31, 32, 33, 47, 64, 65, 80, 100, 127, 128, 129, 150,
+              176, 200, 239, 241, 255, 256, 257, 300, 400, 511, 513, 700, 0, 3]
+    N_r, K_r, N_s = len(counts), 4, 1
+    counts[-1] += -sum(counts) % K_r
+    T = sum(counts) // K_r
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(seed)
+    rnd = lambda *shape, std=1.0: (torch.randn(*shape, device=dev, generator=g) * std).bfloat16()
+    u = rnd(T, d)
+    perm = torch.randint(0, T, (T * K_r,), device=dev, generator=g, dtype=torch.int32)
+    x_perm = u[perm.long()].contiguous()
+    w = {"w_gate": rnd(N_r, I, d, std=d ** -0.5), "w_up": rnd(N_r, I, d, std=d ** -0.5),
+         "w_down": rnd(N_r, d, I, std=I ** -0.5), "ws_gate": rnd(N_s, I, d, std=d ** -0.5),
+         "ws_up": rnd(N_s, I, d, std=d ** -0.5), "ws_down": rnd(N_s, d, I, std=I ** -0.5)}
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device=dev)
+    sh = moe.make_shape(T, d, N_r, K_r, N_s, I)
+    h_ref = torch.empty(T * K_r + N_s * T, I, dtype=torch.bfloat16, device=dev)
+    h = torch.full_like(h_ref, float("nan"))
+    moe.expert_gate_up(x_perm, u, off, sh, w, h_ref)
+    moe.expert_gate_up_gather(u, perm, off, sh, w, h)
+    torch.cuda.synchronize()
+    assert moe.device_error() == 0
+    assert torch.equal(h, h_ref)
+
+
+def test_gate_up_gather_bad_token_is_a_zero_row_and_reported():
+    """A perm entry outside [0, T) is read as a zero row (its h row is that of a zero
+    token), the other rows are untouched, and the device error word reads
+    MOE_ERR_INVALID_ARG."""
+    T, d, I, N_r, K_r = 64, 256, 128, 4, 2
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(41)
+    rnd = lambda *shape, std=1.0: (torch.randn(*shape, device=dev, generator=g) * std).bfloat16()
+    u = rnd(T, d)
+    perm = torch.arange(T * K_r, device=dev, dtype=torch.int32) % T
+    perm[5], perm[77] = -3, T
+    x_perm = u[perm.long().clamp(0, T - 1)].contiguous()
+    x_perm[5].zero_()
+    x_perm[77].zero_()
+    w = {"w_gate": rnd(N_r, I, d, std=d ** -0.5), "w_up": rnd(N_r, I, d, std=d ** -0.5),
+         "w_down": rnd(N_r, d, I, std=I ** -0.5)}
+    off = torch.tensor([0, 40, 90, 100, T * K_r], dtype=torch.int32, device=dev)
+    sh = moe.make_shape(T, d, N_r, K_r, 0, I)
+    h_ref = torch.empty(T * K_r, I, dtype=torch.bfloat16, device=dev)
+    h = torch.empty_like(h_ref)
+    moe.expert_gate_up(x_perm, u, off, sh, w, h_ref)
+    torch.cuda.synchronize()
+    assert moe.device_error() == 0
+    moe.expert_gate_up_gather(u, perm, off, sh, w, h)
+    torch.cuda.synchronize()
+    assert moe.STATUS[moe.device_error()] == "MOE_ERR_INVALID_ARG"   # read and cleared
+    assert torch.equal(h, h_ref)
+
+
 def test_out_of_range_expert_index_is_skipped_and_reported():
     """One topk_idx entry outside [0, N_r): dispatch skips it (no count, inv_row = -1,
     no gathered row), combine leaves it out, the device error word reads

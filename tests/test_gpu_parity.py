@@ -211,12 +211,40 @@ def test_layer_is_deterministic():
         np.testing.assert_array_equal(r1[k], r2[k], err_msg=k)
 
 
+def test_layer_reading_rows_from_u_is_bit_identical():
+    """MoELayer(gather_rows=True): gate/up reads the routed rows straight from u and the
+    dispatch writes no x_perm.  h' equals the default layer's bit for bit, and backward()
+    (which then gathers x_perm itself) gives the same gradients."""
+    cfg = synth.config("mid", T=512, n_seq=2)
+    x = synth.make_inputs(cfg, device="cuda")
+    w = {k: x[k] for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")}
+    outs = []
+    for gather in (False, True):
+        lay = moe.MoELayer(T=cfg.T, d=cfg.d, N_r=cfg.N_r, K_r=cfg.K_r, N_s=cfg.N_s, I=cfg.I,
+                           G=cfg.G, M=cfg.M, e=x["e"], b=x["b"].clone(), weights=w,
+                           n_seq=cfg.n_seq, alpha=cfg.alpha, want_s=True, gather_rows=gather)
+        h = lay.step(x["u"], x["seq_offsets"], update_bias=False).clone()
+        g = torch.Generator(device="cuda").manual_seed(3)
+        dh = torch.randn(cfg.T, cfg.d, generator=g, device="cuda")
+        grads = {k: v.clone() for k, v in lay.backward(x["u"], dh, x["seq_offsets"]).items()}
+        torch.cuda.synchronize()
+        assert moe.device_error() == 0
+        outs.append((h, grads))
+    assert torch.equal(outs[0][0], outs[1][0])
+    for k in outs[0][1]:
+        assert torch.equal(outs[0][1][k], outs[1][1][k]), k
+
+
 def test_gathered_rows_are_token_rows():
+    """The dispatch's row gather writes x_perm = u[perm_token]."""
     cfg = synth.config("mid", T=512, n_seq=1)
     r = run_layer(cfg)
     layer, u = r["layer"], r["inputs"]["u"]
-    perm = layer.perm_token.long()
-    assert torch.equal(layer.x_perm, u[perm])
+    xp = torch.empty_like(layer.x_perm)
+    moe.dispatch(layer.topk_idx, layer.shape, layer.load, layer.expert_offset, layer.perm_token,
+                 layer.inv_row, u, xp)
+    torch.cuda.synchronize()
+    assert torch.equal(xp, u[layer.perm_token.long()])
 
 
 def test_bias_update_moves_toward_balance_over_steps():
