@@ -418,7 +418,7 @@ class MoELayer:
     gather_rows: bool = False   # bf16: gate/up reads the routed rows' tokens straight
     # from u and the dispatch writes no x_perm (saves the x_perm buffer, T*K_r*d values;
     # backward() then gathers x_perm itself).  Off by default: the gate/up GEMM runs
-    # about 2.6 times longer that way (its rows are copied by one warp's cp.async)
+    # about 2.5 times longer that way
 
     def __post_init__(self):
         dev, dt = self.e.device, self.e.dtype

@@ -90,7 +90,8 @@ __device__ __forceinline__ void release_tile_counter(int* ctr) {
 // programmatic-serialization attribute.
 template <typename Kernel>
 cudaError_t launch_pairs(Kernel kernel, int* fit_cache, std::mutex& mu, size_t smem,
-                         long long tiles_ub, const CUtensorMap* m, TcArgs a, cudaStream_t st) {
+                         long long tiles_ub, const CUtensorMap* m, TcArgs a, cudaStream_t st,
+                         int threads = THREADS) {
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[1];
@@ -100,7 +101,7 @@ cudaError_t launch_pairs(Kernel kernel, int* fit_cache, std::mutex& mu, size_t s
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (device_sm_count() / 2));
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;

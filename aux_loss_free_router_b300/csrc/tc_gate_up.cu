@@ -37,13 +37,14 @@
 // the next expert's rows (or zeros) and not stored.
 //
 // GATHER variant (moe_expert_gate_up_gather): a routed tile's token rows come straight
-// from u at the rows perm_token gives, copied by the 32 lanes of warp 0 with cp.async
-// into the same swizzled layout; each CTA counts its lanes' copies of a stage on a
-// gfull barrier, the even CTA's MMA thread waits on its own, and the odd CTA's idle MMA
-// warp relays its CTA's to the even CTA's full barrier.  A generic-to-async proxy fence
-// precedes the MMAs' reads.  h is bit-identical to the x_perm path's; at the
-// DeepSeek-V3 shape the kernel ran about 2.6 times longer (one warp issues every
-// copy), so the layer keeps x_perm by default.
+// from u at the rows perm_token gives, copied by the 128 lanes of warps 0 and 6..8 with
+// cp.async into the same swizzled layout; each CTA counts its lanes' copies of a stage
+// on a gfull barrier, the even CTA's MMA thread waits on its own, and the odd CTA's idle
+// MMA warp relays its CTA's to the even CTA's full barrier.  A generic-to-async proxy
+// fence precedes the MMAs' reads.  h is bit-identical to the x_perm path's; the kernel
+// ran about 2.5 times longer (a stage's round trip through the copies, the barriers and
+// the relay is longer than the six-stage ring covers), so the layer keeps x_perm by
+// default.
 #include "tc_ffn_common.cuh"
 #include "tmap.h"
 
@@ -54,6 +55,8 @@ namespace {
 using namespace ffn_tc;
 
 constexpr int STAGES = 6, BT = 256;
+// gathering from u: warp 0 and warps 6..8 copy the routed token rows (128 lanes)
+constexpr int GWARPS = 4, GTHREADS = THREADS + 32 * (GWARPS - 1);
 constexpr int A_BYTES = 128 * BK * 2;           // this CTA's 128 weight rows
 constexpr int B_BYTES = (BT / 2) * BK * 2;      // this CTA's half of the token rows
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
@@ -74,7 +77,7 @@ constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + XCH + sizeof(Ctrl) 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 template <bool GATHER>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
     tc_gate_up_kernel(const __grid_constant__ CUtensorMap mX_r, const __grid_constant__ CUtensorMap mX_s,
                   const __grid_constant__ CUtensorMap mW0_r, const __grid_constant__ CUtensorMap mW1_r,
                   const __grid_constant__ CUtensorMap mW0_s, const __grid_constant__ CUtensorMap mW1_s,
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < STAGES; ++i) {
       tc::mbar_init(&C.full[i], GATHER ? 2 : 1);   // gathering: and the odd CTA's relay
       tc::mbar_init(&C.empty[i], 1);
-      tc::mbar_init(&C.gfull[i], 32);               // the 32 gather lanes
+      tc::mbar_init(&C.gfull[i], 32 * GWARPS);      // the gather lanes
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&C.tfull[i], 1);
@@ -110,8 +113,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < TQ; ++i) {
       tc::mbar_init(&C.tq_full[i], 1);
       // readers of a tile index: the even CTA's MMA thread, the four epilogue warps of
-      // each CTA and the odd CTA's producer (and, gathering, the odd CTA's relay)
-      tc::mbar_init(&C.tq_empty[i], GATHER ? 11 : 10);
+      // each CTA and the odd CTA's producer (and, gathering, the odd CTA's relay and the
+      // three more gather warps of each CTA)
+      tc::mbar_init(&C.tq_empty[i], GATHER ? 11 + 2 * (GWARPS - 1) : 10);
     }
     tc::mbar_init(&C.fin, 1);
     C.abort_flag = 0;
@@ -161,29 +165,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     return t;
   };
 
-  if (warp == 0 && GATHER) {
+  if (GATHER && (warp == 0 || warp >= 6)) {
     // -------------------------------------------- producer, rows gathered from u --
-    // Lane 0 claims tiles and issues the weights' TMA copies (and, for a shared
-    // expert's tile, the token rows' copy: those rows are consecutive rows of u).  For a
-    // routed tile every lane copies 16-byte pieces of this CTA's token rows of the K step
-    // from u, at the rows perm gives, into the 128-byte-swizzled layout the MMA reads:
-    // lane l takes piece l & 7 of rows (l >> 3) + 4i.  Each lane's copies of a stage are
-    // counted on the stage's gfull barrier.
+    // Warp 0's lane 0 claims tiles (even CTA) and issues the weights' TMA copies (and,
+    // for a shared expert's tile, the token rows' copy: those rows are consecutive rows
+    // of u).  For a routed tile the 128 lanes of warps 0 and 6..8 copy 16-byte pieces of
+    // this CTA's token rows of the K step from u, at the rows perm gives, into the
+    // 128-byte-swizzled layout the MMA reads: gather lane g takes piece g & 7 of rows
+    // (g >> 3) + 16i.  Each lane's copies of a stage are counted on the stage's gfull
+    // barrier.
     constexpr unsigned FULLM = 0xffffffffu;
+    const bool claimer = warp == 0 && leader;
+    const int gl = (warp == 0 ? 0 : warp - 5) * 32 + lane;
     int it = 0;
     int tile = 0;
-    if (lane == 0) tile = leader ? claim_tile(0) : next_tile(0);
+    if (lane == 0) tile = claimer ? claim_tile(0) : next_tile(0);
     tile = __shfl_sync(FULLM, tile, 0);
-    const int chunk = lane & 7;
+    const int chunk = gl & 7;
     for (int k = 0; tile >= 0; ++k) {
       if (__shfl_sync(FULLM, *abort_flag, 0)) break;
       int next = -1;
       if (lane == 0) {
-        if (leader) next = claim_tile(k + 1);             // one tile ahead of the loads
+        if (claimer) next = claim_tile(k + 1);            // one tile ahead of the loads
         else release_tile(k);
       }
       next = __shfl_sync(FULLM, next, 0);
-      if (leader && next == -2) break;
+      if (claimer && next == -2) break;
       const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
       const bool shared = tcd.seg >= s.N_r;
       const int e = shared ? tcd.seg - s.N_r : tcd.seg;
@@ -199,10 +206,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int w_row = e * N + tcd.n * 128 + (int)rank * (128 / 2);
       // this lane's rows: the token (-1: zero-filled, past the tile's tokens; -2: not
       // copied, past the CTA's half of the MMA)
-      int tokr[32];
+      int tokr[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int rho = (lane >> 3) + 4 * i;
+      for (int i = 0; i < 8; ++i) {
+        const int rho = (gl >> 3) + 16 * i;
         int t = -2;
         if (!shared && rho < half) {
           t = -1;
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool got = tc::mbar_wait(&C.empty[st], ph ^ 1, abort_flag, args.err);
         if (!__all_sync(FULLM, got)) { ok = false; break; }
         uint8_t* sa = base + st * STAGE_BYTES;
-        if (lane == 0) {
+        if (warp == 0 && lane == 0) {
           const uint32_t bar = tc::cluster_addr(&C.full[st], 0);   // the even CTA's barrier
           if (leader) tc::mbar_arrive_expect_tx(&C.full[st], 2 * stage_tx);
           tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);                 // 64 gate rows
@@ -235,8 +242,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int col = kb * BK + chunk * 8;           // d is a multiple of 8
           const bool in_row = col < s.d;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int rho = (lane >> 3) + 4 * i;
+          for (int i = 0; i < 8; ++i) {
+            const int rho = (gl >> 3) + 16 * i;
             if (tokr[i] >= -1) {
               const bool copy = tokr[i] >= 0 && in_row;
               const __nv_bfloat16* src = copy ? args.u + (size_t)tokr[i] * s.d + col : args.u;
@@ -247,7 +254,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc::cp_async_mbar_arrive(&C.gfull[st]);
       }
       if (!ok) break;
-      if (!leader) next = lane == 0 ? next_tile(k + 1) : 0;
+      if (!claimer) next = lane == 0 ? next_tile(k + 1) : 0;
       tile = __shfl_sync(FULLM, next, 0);
     }
     tc::cp_async_wait_all();
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue --
     const int q = warp & 3;   // TMEM lane quarter this warp can access
     const uint32_t tempty0 = tc::cluster_addr(&C.tempty[0], 0);
@@ -508,7 +515,8 @@ cudaError_t launch_ffn_up_tc_gather(const FfnShape& s, const void* u, const int3
   TcArgs a{s, expert_offset, static_cast<__nv_bfloat16*>(h), dev_error_ptr(), nullptr};
   a.u = static_cast<const __nv_bfloat16*>(u);
   a.perm = perm_token;
-  return launch_pairs(tc_gate_up_kernel<true>, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st);
+  return launch_pairs(tc_gate_up_kernel<true>, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st,
+                      GTHREADS);
 }
 
 }  // namespace moe

@@ -225,9 +225,9 @@ MOE_API moe_status moe_expert_gate_up(const void* x_perm, const float* x_perm_sc
  * x_perm null).  h is bit-identical to moe_expert_gate_up's on x_perm = u[perm_token].
  * A perm_token entry outside [0, T) is read as a zero row and reported through
  * moe_device_error() (MOE_ERR_INVALID_ARG).  bf16 weights only; u 16-byte aligned.
- * It saves the x_perm buffer and the dispatch's row copy but not time: its rows are
- * copied by one warp per CTA, and at the DeepSeek-V3 shape the GEMM ran about 2.6
- * times longer than moe_expert_gate_up on x_perm. */
+ * It saves the x_perm buffer and the dispatch's row copy but not time: the GEMM ran
+ * about 2.5 times longer than moe_expert_gate_up on x_perm (DeepSeek-V3 and 64-expert
+ * shapes). */
 MOE_API moe_status moe_expert_gate_up_gather(const void* u, const int32_t* perm_token,
                               const int32_t* expert_offset, moe_shape sh,
                               const moe_expert_weights* w, void* h, void* stream);
