@@ -91,6 +91,16 @@ def test_dispatch_and_ffn_reject_bad_args(lib):
     assert lib.moe_dispatch(FAKE, sh, FAKE, moe.E4M3, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, ws, None) == 1
     w = moe._Weights(moe.BF16, FAKE, FAKE, None, None, None, None, FAKE, FAKE, FAKE, None, None, None)
     assert lib.moe_expert_gate_up(FAKE, None, FAKE, None, FAKE, sh, ctypes.byref(w), FAKE, None, None) == 1
+    # gate/up reading rows from u: every pointer needed, u 16-byte aligned, bf16 weights only
+    w.down = FAKE
+    assert lib.moe_expert_gate_up_gather(None, FAKE, FAKE, sh, ctypes.byref(w), FAKE, None) == 1
+    assert lib.moe_expert_gate_up_gather(FAKE + 8, FAKE, FAKE, sh, ctypes.byref(w), FAKE, None) == 1
+    assert lib.moe_expert_gate_up_gather(FAKE, None, FAKE, sh, ctypes.byref(w), FAKE, None) == 1
+    assert lib.moe_expert_gate_up_gather(FAKE, FAKE, FAKE, sh, ctypes.byref(w), None, None) == 1
+    assert lib.moe_expert_gate_up_gather(None, None, None, shape(T=0), ctypes.byref(w), None, None) == 0
+    w.dtype = moe.F32
+    assert lib.moe_expert_gate_up_gather(FAKE, FAKE, FAKE, sh, ctypes.byref(w), FAKE, None) == 1
+    w.dtype, w.down = moe.BF16, None
     assert lib.moe_expert_ffn(FAKE, None, FAKE, None, FAKE, sh, None, FAKE, FAKE, 1 << 30, None) == 1
     w.down = FAKE
     assert lib.moe_expert_ffn(FAKE, None, FAKE, None, FAKE, sh, ctypes.byref(w), FAKE, FAKE, 16, None) == 3
