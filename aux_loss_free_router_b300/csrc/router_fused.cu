@@ -469,16 +469,18 @@ int fused_cluster(int T, int d) {
   return C;
 }
 
-// Pair launches, for 256 experts and batches of at least kPairMinTokens (the centroid
-// slice is then two thirds of what a single CTA takes in per K step; with 64 experts
-// the pairs measured slower): C/2 pairs per 256-token tile,
-// C/2 the largest power of two up to 4 with the clusters still fitting the SMs in one
-// wave, and no more slices than d's 64-wide blocks.
+// Pair launches, for 256 experts, d >= 256 and batches of at least kPairMinTokens (the
+// centroid slice is then two thirds of what a single CTA takes in per K step; with 64
+// experts the pairs measured slower): C/2 pairs per 256-token tile, C/2 a power of two
+// from 2 to 4, the largest with the clusters still fitting the SMs in one wave and no more
+// slices than d's 64-wide blocks.  At least two slices: a CTA then decides at most 64
+// tokens, whose normalised affinities fit beside the partial tile in shared memory.
 constexpr int kPairMinTokens = 2048;
+bool fused_pair_ok(int T, int d, int N_r) { return T >= kPairMinTokens && N_r == 256 && d >= 4 * BK; }
 int fused_cluster_pair(int T, int d) {
   const int tiles = (T + 2 * BM - 1) / (2 * BM);
   const int nk = (d + BK - 1) / BK;
-  int KS = 1;
+  int KS = 2;
   while (KS < 4 && (long long)tiles * 2 * KS * 2 <= device_sm_count() && KS * 2 <= nk) KS *= 2;
   return 2 * KS;
 }
@@ -500,7 +502,7 @@ cudaError_t launch_router_fused(const void* u, const void* e, int d, const float
   CUtensorMap mU, mE;
   const uint64_t rb = (uint64_t)d * 2;
   // large batches: CTA pairs (each CTA loads half of the centroid rows per K step)
-  const bool pair = p.T >= kPairMinTokens && p.N_r == 256;
+  const bool pair = fused_pair_ok(p.T, d, p.N_r);
   if (!make_tmap_2d(&mU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, d, p.T, rb, BK, BM) ||
       !make_tmap_2d(&mE, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, e, d, p.N_r, rb, BK, pair ? p.N_r / 2 : p.N_r))
     return cudaErrorInvalidValue;

@@ -104,7 +104,8 @@ def test_combine_v3_shape_sampled():
     # 256 experts, batches of 2048 tokens or more: the fused router's CTA-pair launches
     (256, 8, 8, 4, 2200, 384, 4),    # last 256-token tile partly past T, four slices of d
     (256, 6, 1, 1, 2100, 256, 2),    # the last tile's odd CTA holds no token
-    (256, 8, 4, 2, 2048, 128, 1),    # two slices of d, one 64-wide block each
+    (256, 8, 4, 2, 2048, 256, 1),    # two slices of d, two 64-wide blocks each
+    (256, 8, 8, 4, 12288, 512, 3),   # 48 tiles: more clusters than fit in one wave
 ])
 def test_router_shapes_bit_exact(N_r, K_r, G, M, T, d, n_seq):
     cfg = synth.MoEConfig("route", T=T, d=d, N_r=N_r, K_r=K_r, N_s=0, I=128, G=G, M=M,
