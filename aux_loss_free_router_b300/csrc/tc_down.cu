@@ -84,6 +84,12 @@ constexpr int CHUNK = 128 * BK * 2;             // one operand of a K step: 16 K
 constexpr int NCHUNK = 13;                      // operand ring: 208 KB
 constexpr int TMEM_COLS = 512, SLOT_COLS = 256;
 constexpr int SCRATCH = 16 * 32 * 2;            // per epilogue warp: 16 tokens x 32 rows bf16
+// Small batches (at most 128 tokens, so no expert segment holds more): tiles of up to 128
+// tokens, one MMA each, through a ring of stages of 16 KB of weights and an 8 KB token box
+// (up to 64 rows a CTA), so that 8 K steps of weights are in flight where the chunk ring
+// holds 6 (a K step there gives a whole 16 KB chunk to a box of at most 4 KB).
+constexpr int S_BT = 128, S_XROWS = 64, S_STAGES = 8;
+constexpr int S_STAGE = CHUNK + S_XROWS * BK * 2;
 
 struct Ctrl {
   uint64_t full[NCHUNK], empty[NCHUNK], tfull[2], tempty[2], fin;
@@ -97,6 +103,8 @@ struct Ctrl {
 constexpr size_t kSmemBytes = (size_t)NCHUNK * CHUNK + 4 * SCRATCH + sizeof(Ctrl) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 static_assert(NCHUNK <= 32, "chunk parities are kept in one 32-bit word");
+static_assert(S_STAGES * S_STAGE <= NCHUNK * CHUNK && S_STAGES <= NCHUNK,
+              "the small-batch ring uses the chunk ring's space and barriers");
 
 // The MMA halves of a tile of n_tok tokens: N of each (multiples of 16; n1 = 0 when
 // one MMA covers the tile).
@@ -134,6 +142,7 @@ __device__ __forceinline__ int ring_next(int c, int by) {
   return c >= NCHUNK ? c - NCHUNK : c;
 }
 
+template <bool SMALL>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_down_kernel(const __grid_constant__ CUtensorMap mX_r, const __grid_constant__ CUtensorMap mX_s,
                   const __grid_constant__ CUtensorMap mW0_r, const __grid_constant__ CUtensorMap mW1_r,
@@ -184,7 +193,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tmem_alloc_pair(&C.tmem_base, TMEM_COLS);
     tc::tmem_relinquish_pair();
   }
-  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BT, n_ft, true, args.err);
+  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, SMALL ? S_BT : BT, n_ft, true,
+                  args.err);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -218,7 +228,45 @@ __global__ void __launch_bounds__(THREADS, 1)
     return t;
   };
 
-  if (warp == 0) {
+  if (warp == 0 && SMALL) {
+    if (lane == 0) {
+      // ---------------------------------------------- producer, small batches --
+      int it = 0;
+      int tile = leader ? claim_tile(0) : next_tile(0);
+      for (int k = 0; tile >= 0 && !*abort_flag; ++k) {
+        int next = -1;
+        if (leader) {
+          next = claim_tile(k + 1);                     // one tile ahead of the loads
+          if (next == -2) break;
+        } else {
+          release_tile(k);
+        }
+        const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
+        const bool shared = tcd.seg >= s.N_r;
+        const int e = shared ? tcd.seg - s.N_r : tcd.seg;
+        const int half = ((tcd.n_tok + 15) & ~15) >> 1;   // token rows a CTA: <= 64
+        const bool sm = half <= SMALL_ROWS;
+        const CUtensorMap* mXb = sm ? &mXs_r : &mX_r;     // 32-row or 64-row boxes
+        const uint32_t stage_tx = (uint32_t)(CHUNK + (sm ? SMALL_ROWS : S_XROWS) * BK * 2);
+        const int x_row = tcd.out_row0 + tcd.tok0 + (int)rank * half;
+        const CUtensorMap* mW0 = shared ? &mW0_s : &mW0_r;
+        const int w_row = e * N + tcd.n * 256 + (int)rank * (256 / 2);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int st = it % S_STAGES;
+          const uint32_t ph = (it / S_STAGES) & 1;
+          if (!tc::mbar_wait(&C.empty[st], ph ^ 1, abort_flag, args.err)) { ok = false; break; }
+          const uint32_t bar = tc::cluster_addr(&C.full[st], 0);   // the even CTA's barrier
+          if (leader) tc::mbar_arrive_expect_tx(&C.full[st], 2 * stage_tx);
+          uint8_t* sa = base + st * S_STAGE;
+          tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);            // 128 down rows
+          tc::tma_load_2d_pair(sa + CHUNK, mXb, bar, kb * BK, x_row);
+        }
+        if (!ok) break;
+        tile = leader ? next : next_tile(k + 1);
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer --
       int ptr = 0;
@@ -272,6 +320,44 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
         tile = leader ? next : next_tile(k + 1);
       }
+    }
+  } else if (warp == 1 && SMALL) {
+    if (lane == 0 && leader) {
+      // -------------------------------------------- MMA issuer, small batches --
+      int it = 0;
+      Slots sl;
+      for (int tcount = 0;; ++tcount) {
+        const int tile = next_tile(tcount);
+        if (tile < 0 || *abort_flag) break;
+        release_tile(tcount);
+        const TileCoord tcd = decode_tile(C.tab, tile, n_ft);
+        int s0, s1;
+        sl.take(false, s0, s1);
+        if (!tc::mbar_wait(&C.tempty[s0], sl.parity(s0) ^ 1u, abort_flag, args.err)) break;
+        tc::fence_after_sync();
+        const uint32_t d0 = tmem_base + (uint32_t)(s0 * SLOT_COLS);
+        const uint32_t idesc0 = tc::idesc_bf16(256, (tcd.n_tok + 15) & ~15);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int st = it % S_STAGES;
+          if (!tc::mbar_wait(&C.full[st], (it / S_STAGES) & 1, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t a = tc::sdesc_sw128(tc::smem_u32(base + st * S_STAGE));
+          const uint64_t b0 = tc::sdesc_sw128(tc::smem_u32(base + st * S_STAGE + CHUNK));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_bf16_pair(d0, a + 2 * kk, b0 + 2 * kk, idesc0, (kb | kk) != 0);
+          tc::mma_commit_pair(&C.empty[st]);
+        }
+        if (!ok) break;
+        tc::mma_commit_pair(&C.tfull[s0]);
+        sl.used(s0);
+      }
+      // every pair MMA has finished once `fin` flips (in both CTAs)
+      tc::mma_commit_pair(&C.fin);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -419,7 +505,9 @@ cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h, const int32_t* 
   const uint64_t rows = (uint64_t)s.T * s.K_r + (uint64_t)s.N_s * s.T;
   // h: 128-row boxes (a CTA's half of a 256-token MMA) and 32-row boxes (MMAs of <= 64
   // tokens); W_down: 128-row boxes
-  bool ok = make_tmap_2d(&m[0], kBF16, h, s.I, rows, rb, BK, HALF / 2) &&
+  // small batches: the token box of a CTA is at most 64 rows (tiles of <= 128 tokens)
+  const bool small = s.T <= S_BT;
+  bool ok = make_tmap_2d(&m[0], kBF16, h, s.I, rows, rb, BK, small ? S_XROWS : HALF / 2) &&
             make_tmap_2d(&m[6], kBF16, h, s.I, rows, rb, BK, SMALL_ROWS) &&
             make_tmap_2d(&m[2], kBF16, w->down, s.I, (uint64_t)s.N_r * s.d, rb, BK, 128);
   if (ok && s.N_s > 0)
@@ -431,11 +519,14 @@ cudaError_t launch_ffn_down_tc(const FfnShape& s, const void* h, const int32_t* 
   m[3] = m[2];
   m[5] = m[4];
   m[7] = m[6];
-  const long long t_ub = (long long)s.T * s.K_r / BT + s.N_r + (long long)s.N_s * ((s.T + BT - 1) / BT);
+  const int bt = small ? S_BT : BT;
+  const long long t_ub = (long long)s.T * s.K_r / bt + s.N_r + (long long)s.N_s * ((s.T + bt - 1) / bt);
   static std::mutex mu;
-  static int fit[64] = {};
+  static int fit[64] = {}, fit_small[64] = {};
   TcArgs a{s, expert_offset, static_cast<__nv_bfloat16*>(y), dev_error_ptr(), nullptr};
-  return launch_pairs(tc_down_kernel, fit, mu, kSmemBytes, t_ub * ((s.d + 255) / 256), m, a, st);
+  if (small)
+    return launch_pairs(tc_down_kernel<true>, fit_small, mu, kSmemBytes, t_ub * ((s.d + 255) / 256), m, a, st);
+  return launch_pairs(tc_down_kernel<false>, fit, mu, kSmemBytes, t_ub * ((s.d + 255) / 256), m, a, st);
 }
 
 }  // namespace moe

@@ -60,12 +60,18 @@ constexpr int GWARPS = 4, GTHREADS = THREADS + 32 * (GWARPS - 1);
 constexpr int A_BYTES = 128 * BK * 2;           // this CTA's 128 weight rows
 constexpr int B_BYTES = (BT / 2) * BK * 2;      // this CTA's half of the token rows
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+// Small batches (at most 128 tokens): tiles of up to 128 tokens and stages of 16 KB of
+// weights and an 8 KB token box (up to 64 rows a CTA), 8 of them in the same space, so
+// that 8 K steps of weights are in flight instead of 6.
+constexpr int S_BT = 128, S_XROWS = 64, S_STAGES = 8;
+constexpr int S_STAGE_BYTES = A_BYTES + S_XROWS * BK * 2;   // 24 KB
+static_assert(S_STAGES * S_STAGE_BYTES <= STAGES * STAGE_BYTES, "small-batch ring in the same space");
 constexpr int TMEM_COLS = 512, ACC_COLS = 256;
 constexpr int XCH = 2 * 16 * 128 * 4;           // raw values [2 buffers][16 tokens][128 rows]
 
 struct Ctrl {
-  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], xfull[2], xempty[2], fin;
-  uint64_t gfull[STAGES];   // token rows gathered from u: the gather lanes' copies done
+  uint64_t full[S_STAGES], empty[S_STAGES], tfull[2], tempty[2], xfull[2], xempty[2], fin;
+  uint64_t gfull[S_STAGES];   // token rows gathered from u: the gather lanes' copies done
   uint64_t tq_full[TQ], tq_empty[TQ];
   int tq[TQ];
   uint32_t tmem_base;
@@ -76,7 +82,7 @@ struct Ctrl {
 constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + XCH + sizeof(Ctrl) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
-template <bool GATHER>
+template <bool GATHER, bool SMALL>
 __global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
     tc_gate_up_kernel(const __grid_constant__ CUtensorMap mX_r, const __grid_constant__ CUtensorMap mX_s,
                   const __grid_constant__ CUtensorMap mW0_r, const __grid_constant__ CUtensorMap mW1_r,
@@ -89,6 +95,8 @@ __global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
   float* xch = reinterpret_cast<float*>(base + STAGES * STAGE_BYTES);
   Ctrl& C = *reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES + XCH);
 
+  constexpr int NST = SMALL ? S_STAGES : STAGES;         // stages of the ring
+  constexpr int SB = SMALL ? S_STAGE_BYTES : STAGE_BYTES;  // bytes of a stage
   const FfnShape s = args.s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_rank();
@@ -99,7 +107,7 @@ __global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
   const int nk = (K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < NST; ++i) {
       tc::mbar_init(&C.full[i], GATHER ? 2 : 1);   // gathering: and the odd CTA's relay
       tc::mbar_init(&C.empty[i], 1);
       tc::mbar_init(&C.gfull[i], 32 * GWARPS);      // the gather lanes
@@ -131,7 +139,8 @@ __global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
     tc::tmem_alloc_pair(&C.tmem_base, TMEM_COLS);
     tc::tmem_relinquish_pair();
   }
-  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, BT, n_ft, true, args.err);
+  build_seg_table(C.tab, args.expert_offset, s.T, s.K_r, s.N_r, s.N_s, SMALL ? S_BT : BT, n_ft, true,
+                  args.err);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -225,11 +234,11 @@ __global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
       }
       bool ok = true;
       for (int kb = 0; kb < nk; ++kb, ++it) {
-        const int st = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
+        const int st = it % NST;
+        const uint32_t ph = (it / NST) & 1;
         const bool got = tc::mbar_wait(&C.empty[st], ph ^ 1, abort_flag, args.err);
         if (!__all_sync(FULLM, got)) { ok = false; break; }
-        uint8_t* sa = base + st * STAGE_BYTES;
+        uint8_t* sa = base + st * SB;
         if (warp == 0 && lane == 0) {
           const uint32_t bar = tc::cluster_addr(&C.full[st], 0);   // the even CTA's barrier
           if (leader) tc::mbar_arrive_expect_tx(&C.full[st], 2 * stage_tx);
@@ -279,19 +288,20 @@ __global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
         // a tile of <= 64 tokens loads 32-row token boxes (decode-sized batches)
         const bool small = half <= SMALL_ROWS;
         const CUtensorMap* mX = shared ? (small ? &mXs_s : &mX_s) : (small ? &mXs_r : &mX_r);
-        const uint32_t stage_tx = (uint32_t)(A_BYTES + (small ? SMALL_ROWS : BT / 2) * BK * 2);
+        const uint32_t stage_tx =
+            (uint32_t)(A_BYTES + (small ? SMALL_ROWS : (SMALL ? S_XROWS : BT / 2)) * BK * 2);
         const int x_row = (shared ? 0 : tcd.row0) + tcd.tok0 + (int)rank * half;
         const CUtensorMap* mW0 = shared ? &mW0_s : &mW0_r;
         const CUtensorMap* mW1 = shared ? &mW1_s : &mW1_r;
         const int w_row = e * N + tcd.n * 128 + (int)rank * (128 / 2);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int st = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
+          const int st = it % NST;
+          const uint32_t ph = (it / NST) & 1;
           if (!tc::mbar_wait(&C.empty[st], ph ^ 1, abort_flag, args.err)) { ok = false; break; }
           const uint32_t bar = tc::cluster_addr(&C.full[st], 0);   // the even CTA's barrier
           if (leader) tc::mbar_arrive_expect_tx(&C.full[st], 2 * stage_tx);
-          uint8_t* sa = base + st * STAGE_BYTES;
+          uint8_t* sa = base + st * SB;
           tc::tma_load_2d_pair(sa, mW0, bar, kb * BK, w_row);                   // 64 gate rows
           tc::tma_load_2d_pair(sa + A_BYTES / 2, mW1, bar, kb * BK, w_row);     // 64 up rows
           tc::tma_load_2d_pair(sa + A_BYTES, mX, bar, kb * BK, x_row);
@@ -318,8 +328,8 @@ __global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int st = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
+          const int st = it % NST;
+          const uint32_t ph = (it / NST) & 1;
           if (!tc::mbar_wait(&C.full[st], ph, abort_flag, args.err)) { ok = false; break; }
           if constexpr (GATHER) {
             // this CTA's gathered rows have landed (the odd CTA's: its relay's arrival on
@@ -328,7 +338,7 @@ __global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
             tc::fence_proxy_async_shared();
           }
           tc::fence_after_sync();
-          const uint32_t s0 = tc::smem_u32(base + st * STAGE_BYTES);
+          const uint32_t s0 = tc::smem_u32(base + st * SB);
           const uint64_t a = tc::sdesc_sw128(s0), b = tc::sdesc_sw128(s0 + A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
@@ -351,8 +361,8 @@ __global__ void __launch_bounds__(GATHER ? GTHREADS : THREADS, 1)
         if (tile < 0 || *abort_flag) break;
         release_tile(tcount);
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int st = it % STAGES;
-          if (!tc::mbar_wait(&C.gfull[st], (it / STAGES) & 1, abort_flag, args.err)) { ok = false; break; }
+          const int st = it % NST;
+          if (!tc::mbar_wait(&C.gfull[st], (it / NST) & 1, abort_flag, args.err)) { ok = false; break; }
           tc::fence_proxy_async_shared();
           tc::mbar_arrive_cluster(tc::cluster_addr(&C.full[st], 0));
         }
@@ -465,8 +475,11 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
   const uint64_t routed = (uint64_t)s.T * s.K_r;
   // tokens: 128-row boxes (a CTA's half of a 256-token tile) and 32-row boxes (tiles of
   // <= 64 tokens); weights: 64-row boxes
-  bool ok = make_tmap_2d(&m[0], kBF16, x_perm, s.d, routed, rb, BK, BT / 2) &&
-            make_tmap_2d(&m[1], kBF16, u, s.d, s.T, rb, BK, BT / 2) &&
+  // small batches: a CTA's token box is at most 64 rows (tiles of <= 128 tokens)
+  const bool small_batch = s.T <= S_BT;
+  const uint32_t xbox = small_batch ? S_XROWS : BT / 2;
+  bool ok = make_tmap_2d(&m[0], kBF16, x_perm, s.d, routed, rb, BK, xbox) &&
+            make_tmap_2d(&m[1], kBF16, u, s.d, s.T, rb, BK, xbox) &&
             make_tmap_2d(&m[6], kBF16, x_perm, s.d, routed, rb, BK, SMALL_ROWS) &&
             make_tmap_2d(&m[7], kBF16, u, s.d, s.T, rb, BK, SMALL_ROWS) &&
             make_tmap_2d(&m[2], kBF16, w->gate, s.d, (uint64_t)s.N_r * s.I, rb, BK, 64) &&
@@ -479,12 +492,16 @@ cudaError_t launch_ffn_up_tc(const FfnShape& s, const void* x_perm, const void* 
     m[5] = m[3];
   }
   if (!ok) return cudaErrorInvalidValue;
-  const long long t_ub = (long long)s.T * s.K_r / BT + s.N_r + (long long)s.N_s * ((s.T + BT - 1) / BT);
+  const int bt = small_batch ? S_BT : BT;
+  const long long t_ub = (long long)s.T * s.K_r / bt + s.N_r + (long long)s.N_s * ((s.T + bt - 1) / bt);
   static std::mutex mu;
-  static int fit[64] = {};
+  static int fit[64] = {}, fit_small[64] = {};
   TcArgs a{s, expert_offset, static_cast<__nv_bfloat16*>(h), dev_error_ptr(), nullptr,
            static_cast<__nv_bfloat16*>(save_a), static_cast<__nv_bfloat16*>(save_c)};
-  return launch_pairs(tc_gate_up_kernel<false>, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st);
+  if (small_batch)
+    return launch_pairs(tc_gate_up_kernel<false, true>, fit_small, mu, kSmemBytes,
+                        t_ub * ((s.I + 127) / 128), m, a, st);
+  return launch_pairs(tc_gate_up_kernel<false, false>, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st);
 }
 
 cudaError_t launch_ffn_up_tc_gather(const FfnShape& s, const void* u, const int32_t* perm_token,
@@ -515,7 +532,7 @@ cudaError_t launch_ffn_up_tc_gather(const FfnShape& s, const void* u, const int3
   TcArgs a{s, expert_offset, static_cast<__nv_bfloat16*>(h), dev_error_ptr(), nullptr};
   a.u = static_cast<const __nv_bfloat16*>(u);
   a.perm = perm_token;
-  return launch_pairs(tc_gate_up_kernel<true>, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st,
+  return launch_pairs(tc_gate_up_kernel<true, false>, fit, mu, kSmemBytes, t_ub * ((s.I + 127) / 128), m, a, st,
                       GTHREADS);
 }
 

@@ -201,6 +201,42 @@ def test_expert_gemms_every_token_tile_size():
         assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref), (r0, len(xs))
 
 
+def test_expert_gemms_small_batch_tiles():
+    """Batches of at most 128 tokens (the down GEMM's small-batch ring: tiles of up to 128
+    tokens, one MMA each): segments of every token-tile height up to 128 rows, one of 200
+    rows (two tiles), empty segments and d = 320, against the oracle's expert FFN."""
+    counts = [0, 1, 8, 15, 16, 17, 31, 32, 33, 47, 64, 65, 80, 100, 127, 128, 200, 0, 3]
+    N_r, K_r, N_s, d, I = len(counts), 8, 1, 320, 384
+    counts[-1] += -sum(counts) % K_r
+    T = sum(counts) // K_r
+    assert T <= 128
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(23)
+    rnd = lambda *shape, std=1.0: (torch.randn(*shape, device=dev, generator=g) * std).bfloat16()
+    x_perm, u = rnd(T * K_r, d), rnd(T, d)
+    w = {"w_gate": rnd(N_r, I, d, std=d ** -0.5), "w_up": rnd(N_r, I, d, std=d ** -0.5),
+         "w_down": rnd(N_r, d, I, std=I ** -0.5), "ws_gate": rnd(N_s, I, d, std=d ** -0.5),
+         "ws_up": rnd(N_s, I, d, std=d ** -0.5), "ws_down": rnd(N_s, d, I, std=I ** -0.5)}
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device=dev)
+    sh = moe.make_shape(T, d, N_r, K_r, N_s, I)
+    h = torch.empty(T * K_r + N_s * T, I, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(T * K_r + N_s * T, d, dtype=torch.bfloat16, device=dev)
+    moe.expert_gate_up(x_perm, u, off, sh, w, h)
+    moe.expert_down(h, off, sh, w, y)
+    torch.cuda.synchronize()
+    assert moe.device_error() == 0
+    yg, xn, un = to_np(y), to_np(x_perm), to_np(u)
+    wn = {k: to_np(v) for k, v in w.items()}
+    segs = [(xn[a:a + c], wn["w_gate"][i], wn["w_up"][i], wn["w_down"][i], a)
+            for i, (a, c) in enumerate(zip(np.cumsum([0] + counts[:-1]), counts)) if c]
+    segs.append((un, wn["ws_gate"][0], wn["ws_up"][0], wn["ws_down"][0], T * K_r))
+    for xs, wg, wu, wd, r0 in segs:
+        ref = oracle.expert_ffn(xs, wg, wu, wd)
+        got = yg[r0:r0 + len(xs)].astype(np.float64)
+        assert np.abs(got - ref).max() <= 2e-2, (r0, len(xs))
+        assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref), (r0, len(xs))
+
+
 @pytest.mark.parametrize("d,I,seed", [(320, 384, 31), (2048, 1408, 32)])
 def test_gate_up_gather_matches_x_perm_bit_for_bit(d, I, seed):
     """Gate/up reading the routed rows straight from u (row r = u[perm[r]]) against gate/up
