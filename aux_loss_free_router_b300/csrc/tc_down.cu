@@ -20,7 +20,9 @@
 // takes three chunks (weights, tokens 0..255, tokens 256..511) for a tile of more than
 // 256 tokens and two otherwise, so both kinds of tile keep the whole ring in flight.
 // Each chunk has an "empty" barrier (the MMAs that read it have finished); the first
-// chunk of a K step has the "full" barrier its TMA loads complete on.
+// chunk of a K step has the "full" barrier its TMA loads complete on.  Batches of at
+// most 128 tokens use the same space as a plain ring of 8 stages (16 KB of weights and an
+// 8 KB token box each) with tiles of up to 128 tokens.
 //
 // Persistent pairs (as many as fit) take the tiles of the segment schedule
 // (ffn_sched.cuh: segment-major, then token tile of up to 512, then feature tile of 256)

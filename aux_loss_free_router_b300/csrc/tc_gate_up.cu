@@ -25,7 +25,9 @@
 // work on neighbouring tiles and share their token and weight tiles through L2.  Warp
 // roles in each CTA:
 //   warp 0      TMA producer: this CTA's weight and token rows into a 6-stage ring
-//               (32 KB per stage); completion is counted on the even CTA's barrier.
+//               (32 KB per stage; for batches of at most 128 tokens, tiles of up to 128
+//               tokens and 8 stages of 24 KB); completion is counted on the even CTA's
+//               barrier.
 //   warp 1      allocates 512 TMEM columns (with the peer); in the even CTA one thread
 //               issues the pair MMAs into one of two 256-column accumulators.
 //   warps 2..5  epilogue: TMEM lanes 0..63 hold gate and lanes 64..127 up of the same
