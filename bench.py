@@ -42,13 +42,13 @@ import synth  # noqa: E402
 METRIC = "MoE-layer fwd tokens/s at d=7168, 256e top-8; tensor-pipe & HBM % of peak"
 
 # DRAM traffic of the gate/up GEMM, from one ncu capture (not measured in the bench
-# run): dram__bytes_read.sum + dram__bytes_write.sum = 2.2447 GB + 0.0358 GB on the
+# run): dram__bytes_read.sum + dram__bytes_write.sum = 2.2442 GB + 0.0354 GB on the
 # V3-shaped slice (32 experts, 1024 tokens, d=7168, I=2048, ~3 GB on the device), whose
-# algorithmic bytes are 2.108 GB: 1.082 bytes moved per algorithmic byte.  A full V3
+# algorithmic bytes are 2.108 GB: 1.081 bytes moved per algorithmic byte.  A full V3
 # launch holds eight times the slice's segments with the same mean load (256 tokens), so
 # its traffic is taken as that ratio times its own algorithmic bytes.  Valid only for
 # the kernel source with this hash.
-NCU_TRAFFIC = {"kernel_src_sha": "46684d38911740ea", "ratio": 2.2805e9 / 2.108e9,
+NCU_TRAFFIC = {"kernel_src_sha": "92b1cd4f04c98f6f", "ratio": 2.2796e9 / 2.108e9,
                "capture": "ncu --set full --clock-control none -k regex:tc_gate_up -s 3 -c 1 "
                           "python bench.py --config v3slice --steps 2 --warmup 3 --no-cpu-baseline"}
 
